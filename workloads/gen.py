@@ -1,0 +1,217 @@
+"""Seeded host-side (NumPy) input generators.
+
+Every array is drawn from ``numpy.random.default_rng([seed, sub])`` with a fixed sub-seed per
+tensor, so any case can be replayed from (config, seed).  bf16 workloads are rounded to bf16
+with round-to-nearest-even on the host; the returned float32 arrays hold exactly the values a
+bf16 tensor holds, so the oracle sees the stored inputs and the tolerance measures kernel error
+only.
+
+None of the method's arithmetic is here.  Draft tokens x_i ~ softmax(draft logits) are drawn by
+the Gumbel-max construction (argmax of logits plus Gumbel noise), which needs no softmax.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+SUB = dict(q=1, k=2, v=3, kv_len=4, tree=5, target=6, draft=7, tokens=8, uniforms=9,
+           ring_k=10, ring_v=11, new_k=12, new_v=13, pos=14, needles=15, gumbel=16, tree_tok=17)
+
+BF16_NAN = np.float32(np.nan)
+
+
+def rng_for(seed: int, what: str) -> np.random.Generator:
+    return np.random.default_rng([int(seed), SUB[what]])
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); NaN stays NaN. Returns float32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bits = x.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
+    out = rounded.astype(np.uint32).view(np.float32).copy()
+    out[np.isnan(x)] = np.nan
+    return out
+
+
+def store(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Values as stored in a tensor of ``dtype`` ("f32" or "bf16"), as float32."""
+    x = x.astype(np.float32)
+    return round_bf16(x) if dtype == "bf16" else x
+
+
+def kv_lengths(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """Per-sequence KV length uniform on the integers [lo, hi]."""
+    if lo == hi:
+        return np.full(B, lo, dtype=np.int32)
+    return rng_for(seed, "kv_len").integers(lo, hi + 1, size=B).astype(np.int32)
+
+
+def random_tree(N: int, max_depth: int, max_children: int, seed: int) -> np.ndarray:
+    """parent[N] int32 with parent[0] = -1 and parent[i] < i.
+
+    For i = 1..N-1 the parent is drawn uniformly among earlier nodes whose depth is below
+    ``max_depth`` and which have fewer than ``max_children`` children.
+    """
+    r = rng_for(seed, "tree")
+    parent = np.full(N, -1, dtype=np.int32)
+    depth = np.zeros(N, dtype=np.int64)
+    nchild = np.zeros(N, dtype=np.int64)
+    for i in range(1, N):
+        cands = [j for j in range(i) if depth[j] < max_depth and nchild[j] < max_children]
+        if not cands:
+            raise ValueError("tree capacity exhausted")
+        p = cands[int(r.integers(len(cands)))]
+        parent[i] = p
+        depth[i] = depth[p] + 1
+        nchild[p] += 1
+    return parent
+
+
+def attn_inputs(B: int, Hq: int, Hkv: int, D: int, nq: int, kv_len: np.ndarray, Lmax: int,
+                dtype: str, seed: int, tail_fill: str = "nan") -> dict:
+    """Q [B, nq, Hq, D], K/V [B, Hkv, Lmax, D] ~ N(0,1); K/V slots at or past kv_len[b] hold
+    NaN (``tail_fill="nan"``) or zeros, so a kernel that reads unused cache slots shows it."""
+    q = store(rng_for(seed, "q").standard_normal((B, nq, Hq, D), dtype=np.float32), dtype)
+    k = store(rng_for(seed, "k").standard_normal((B, Hkv, Lmax, D), dtype=np.float32), dtype)
+    v = store(rng_for(seed, "v").standard_normal((B, Hkv, Lmax, D), dtype=np.float32), dtype)
+    fill = np.float32(np.nan) if tail_fill == "nan" else np.float32(0.0)
+    for b in range(B):
+        k[b, :, int(kv_len[b]):, :] = fill
+        v[b, :, int(kv_len[b]):, :] = fill
+    return dict(q=q, k=k, v=v, kv_len=np.asarray(kv_len, dtype=np.int32))
+
+
+def _unit(x: np.ndarray) -> np.ndarray:
+    x = x.astype(np.float64)
+    return x / max(np.linalg.norm(x), 1e-30)
+
+
+def plant_chain_needles(inp: dict, nq: int, dtype: str, seed: int, strength: float = 6.0) -> dict:
+    """Plant keys that make mask mistakes visible (chain verify).
+
+    Per (b, kv head g): a "hit" key at a position every row sees, aligned with the query of
+    row 0 / head g*G, and for each row j < nq-1 a "trap" key at position L_b - nq + j + 1 (the
+    first key row j must NOT see), aligned with that row's query.  A kernel that leaks the causal
+    mask then puts a large weight on the trap's value row.
+    """
+    q, k = inp["q"], inp["k"]
+    B, _, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    r = rng_for(seed, "needles")
+    for b in range(B):
+        L = int(inp["kv_len"][b])
+        for g in range(Hkv):
+            h = g * G
+            if L - nq > 0:
+                p = int(r.integers(0, L - nq))
+                k[b, g, p] = strength * np.sqrt(D) * _unit(q[b, 0, h])
+            for j in range(nq - 1):
+                pos = L - nq + j + 1
+                k[b, g, pos] = 1.5 * strength * np.sqrt(D) * _unit(q[b, j, h])
+    inp["k"] = store(k, dtype)
+    return inp
+
+
+def plant_tree_needles(inp: dict, parent: np.ndarray, dtype: str, seed: int,
+                       strength: float = 9.0) -> dict:
+    """Plant tree traps: the key of tree node m is aligned with the query of a node i that is
+    neither m nor a descendant of m, i.e. a node that must not see m."""
+    q, k = inp["q"], inp["k"]
+    B, N, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    r = rng_for(seed, "needles")
+    anc = [set() for _ in range(N)]
+    for i in range(N):
+        j = i
+        while j >= 0:
+            anc[i].add(j)
+            j = int(parent[j])
+    for b in range(B):
+        L = int(inp["kv_len"][b])
+        for g in range(Hkv):
+            for m in range(1, N):
+                blind = [i for i in range(N) if m not in anc[i]]
+                if not blind:
+                    continue
+                i = blind[int(r.integers(len(blind)))]
+                k[b, g, L - N + m] = strength * np.sqrt(D) * _unit(q[b, i, g * G])
+    inp["k"] = store(k, dtype)
+    return inp
+
+
+def window_inputs(B: int, Hq: int, Hkv: int, D: int, W: int, pos: np.ndarray, dtype: str,
+                  seed: int) -> dict:
+    """Draft-window inputs: q [B, Hq, D]; ring K/V [B, Hkv, W, D]; pos[b] = tokens written
+    including the current one; new K/V [B, Hkv, D] for the current token.  Ring slots that no
+    token has reached yet (slot >= pos[b] while pos[b] < W) hold NaN."""
+    q = store(rng_for(seed, "q").standard_normal((B, Hq, D), dtype=np.float32), dtype)
+    kr = store(rng_for(seed, "ring_k").standard_normal((B, Hkv, W, D), dtype=np.float32), dtype)
+    vr = store(rng_for(seed, "ring_v").standard_normal((B, Hkv, W, D), dtype=np.float32), dtype)
+    kn = store(rng_for(seed, "new_k").standard_normal((B, Hkv, D), dtype=np.float32), dtype)
+    vn = store(rng_for(seed, "new_v").standard_normal((B, Hkv, D), dtype=np.float32), dtype)
+    pos = np.asarray(pos, dtype=np.int32)
+    for b in range(B):
+        if pos[b] < W:
+            kr[b, :, max(int(pos[b]) - 1, 0):, :] = np.nan
+            vr[b, :, max(int(pos[b]) - 1, 0):, :] = np.nan
+    return dict(q=q, k_ring=kr, v_ring=vr, k_new=kn, v_new=vn, pos=pos)
+
+
+def gumbel_max_draw(logits: np.ndarray, r: np.random.Generator) -> np.ndarray:
+    """One draw per row from softmax(logits) by the Gumbel-max construction: the argmax of
+    logits + Gumbel(0,1) noise.  (Input generation only: this is how a draft model's sampler
+    would pick x_i; the verify side never uses it.)"""
+    u = r.random(logits.shape)
+    u = np.clip(u, 1e-300, 1.0)
+    gumbel = -np.log(-np.log(u))
+    return np.argmax(logits.astype(np.float64) + gumbel, axis=-1).astype(np.int32)
+
+
+def chain_sample_inputs(B: int, gamma: int, V: int, seed: int, target_sigma: float = 2.0,
+                        draft_noise_sigma: float = 1.0, draft_corr: float = 0.0) -> dict:
+    """target_logits [B, gamma+1, V], draft_logits [B, gamma, V] fp32, draft_tokens [B, gamma]
+    drawn from the draft distributions, uniforms [B, gamma+1] in [0, 1) fp32."""
+    z = rng_for(seed, "target").standard_normal((B, gamma + 1, V), dtype=np.float32)
+    t = (target_sigma * z).astype(np.float32)
+    eps = rng_for(seed, "draft").standard_normal((B, gamma, V), dtype=np.float32)
+    if draft_corr > 0.0:
+        d = target_sigma * (draft_corr * z[:, :gamma] + np.sqrt(1.0 - draft_corr ** 2) * eps)
+    else:
+        d = t[:, :gamma] + draft_noise_sigma * eps
+    d = d.astype(np.float32)
+    x = gumbel_max_draw(d, rng_for(seed, "gumbel"))
+    u = rng_for(seed, "uniforms").random((B, gamma + 1), dtype=np.float32)
+    return dict(target_logits=t, draft_logits=d, draft_tokens=x, uniforms=u)
+
+
+def tree_sample_inputs(B: int, parent: np.ndarray, V: int, seed: int, target_sigma: float = 2.0,
+                       p_match: float = 0.6, planted_logit: float = 30.0) -> dict:
+    """target_logits [B, N, V] ~ N(0, sigma^2) and node_tokens [B, N].
+
+    For each node with children, its first child's token is, with probability ``p_match``, a
+    token whose logit in the parent's row is planted at ``planted_logit`` (far above any
+    N(0, sigma^2) draw at these vocabulary sizes); the other children get random ids distinct
+    from their siblings'."""
+    N = len(parent)
+    r = rng_for(seed, "tree_tok")
+    t = (target_sigma * rng_for(seed, "target").standard_normal((B, N, V), dtype=np.float32)).astype(np.float32)
+    tok = np.zeros((B, N), dtype=np.int32)
+    children = [[] for _ in range(N)]
+    for i in range(1, N):
+        children[int(parent[i])].append(i)
+    for b in range(B):
+        tok[b, 0] = int(r.integers(V))
+        for p in range(N):
+            kids = children[p]
+            if not kids:
+                continue
+            ids = r.choice(V, size=len(kids), replace=False).astype(np.int32)
+            if r.random() < p_match:
+                t[b, p, ids[0]] = np.float32(planted_logit)
+            for c, tid in zip(kids, ids):
+                tok[b, c] = tid
+    return dict(target_logits=t, node_tokens=tok)
