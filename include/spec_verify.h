@@ -1,0 +1,233 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify: the data-parallel hot path of speculative decoding
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * Three operations, each defined on the pages this library follows:
+ *
+ *   spec_verify_attn        Target-side verify attention.  The gamma+1 chain queries (the last
+ *                           committed token plus gamma drafts), or the N nodes of a token tree,
+ *                           attend over the full GQA KV cache of their sequence.
+ *                           ("Guide to MagicDec", Solution section 2 and Implementation Step 3:
+ *                           one target pass over prefix + drafts; "Speculative Decoding &
+ *                           Medusa", section 4 and "Speculative Decoding in LLM Serving Systems",
+ *                           Tree-based variants: tree attention where a node sees only its
+ *                           ancestors.)
+ *   spec_draft_window_attn  Draft-side single-query attention over a fixed-size ring-buffer
+ *                           window of the last W tokens ("Guide to MagicDec", Solution section 1
+ *                           and Implementation Step 1: bounded circular FIFO draft KV cache).
+ *   spec_sample             The speculative-sampling step over the vocabulary: softmax of target
+ *                           logits P and draft logits Q, left-to-right accept with probability
+ *                           min(1, P(x)/Q(x)), residual resample from norm(max(P - Q, 0)) at the
+ *                           first rejection, bonus token from P_{gamma+1} when all are accepted
+ *                           ("Speculative Decoding & Medusa", section 2; "Speculative Decoding in
+ *                           LLM Serving Systems", Accepting and rejecting); plus greedy chain and
+ *                           greedy longest-accepted-path tree selection.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except the tree parent arrays,
+ *    which are HOST pointers (the tree is small and shared by the batch; it is validated and
+ *    turned into per-node ancestor bitmasks on the host before any launch).
+ *  - Strides are in ELEMENTS.  The innermost dimension of every tensor is contiguous.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t; NULL = the legacy default
+ *    stream).  They allocate no memory, keep no global mutable state and are thread-safe.
+ *    Scratch memory is the caller's `workspace`, at least the size the matching *_workspace()
+ *    query returns, 256-byte aligned.  Two calls that share a workspace must not overlap.
+ *  - Host-side validation runs first and returns a negative status WITHOUT launching anything.
+ *    A launch failure returns SPEC_ERR_CUDA.
+ *  - Data errors that only the device can see (a kv_len or pos out of range, a token id outside
+ *    [0, V)) never trap: the affected sequence's output is zeroed (attention) or its
+ *    out_num_accepted is set to -1 (sampling), and a flag is OR-ed into the 32-bit status word
+ *    at byte 0 of the workspace (SPEC_STATUS_*), which the call resets.  Read it with any
+ *    device-to-host copy once the stream has reached the end of the call.
+ *  - Device-side waits are bounded; a wait that runs out sets SPEC_STATUS_TIMEOUT and the kernel
+ *    returns.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* spec_stream_t; /* same type as cudaStream_t */
+
+/* return codes */
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = -1, /* null pointer, bad size, stride, alignment or tree */
+  SPEC_ERR_UNSUPPORTED = -2, /* a valid combination this build does not implement */
+  SPEC_ERR_WORKSPACE = -3,   /* workspace missing, too small or misaligned */
+  SPEC_ERR_CUDA = -4         /* a CUDA runtime/driver call or kernel launch failed */
+};
+
+/* element types */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+/* flags OR-ed into the device status word (byte 0 of the workspace) */
+enum {
+  SPEC_STATUS_BAD_KV_LEN = 1, /* kv_len[b] < nq or > Lmax: that sequence's output is zero   */
+  SPEC_STATUS_BAD_POS = 2,    /* pos[b] < 1: that sequence's window output is zero           */
+  SPEC_STATUS_BAD_TOKEN = 4,  /* a token id outside [0, V): that row's num_accepted is -1   */
+  SPEC_STATUS_TIMEOUT = 8     /* a bounded device wait ran out; results are not valid        */
+};
+
+/* ------------------------------------------------------------------------------------------
+ * spec_verify_attn
+ *
+ * For every sequence b, query row j in [0, nq) and query head h in [0, Hq):
+ *     o[b, j, h, :] = softmax_t(scale * q[b, j, h, :] . k[b, g, t, :]) @ v[b, g, t, :]
+ * with g = floor(h / (Hq / Hkv)) (contiguous GQA groups) and t over the keys row j sees.  The
+ * cache of sequence b holds kv_len[b] entries, the last nq of which are the new query tokens
+ * (already appended by the caller; Q and K already position-encoded):
+ *   chain (tree_parent == NULL): row j sees keys 0 .. kv_len[b] - nq + j  (causal);
+ *   tree  (tree_parent != NULL): node j sees the context keys [0, kv_len[b] - nq) and the tree
+ *         keys kv_len[b] - nq + m for every m on the path from j to the root (m = j included).
+ *
+ * Layout (elements, innermost contiguous):
+ *   q  [B, nq, Hq, D]   strides q_stride_b, q_stride_t, q_stride_h
+ *   k,v[B, Hkv, Lmax, D] strides kv_stride_b, kv_stride_h; token stride = D
+ *   o  [B, nq, Hq, D]   strides o_stride_b, o_stride_t, o_stride_h
+ *   kv_len [B] int32 device
+ * Types: kv_dtype SPEC_BF16 (q bf16) or SPEC_F32 (q f32); o_dtype SPEC_F32 or SPEC_BF16.
+ * Limits: D in {64, 128}; Hq % Hkv == 0; 1 <= B <= 4096; 1 <= nq; nq * (Hq/Hkv) <= 1024;
+ *   tree: nq <= 64, tree_parent[0] == -1, 0 <= tree_parent[i] < i for i >= 1.
+ *   bf16 K/V: base pointers 16-byte aligned, kv_stride_h and kv_stride_b multiples of 8.
+ * scale == 0 selects 1/sqrt(D).
+ * Accumulation is fp32 (scores, softmax, P.V); bf16 inputs are multiplied exactly.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct spec_attn_args {
+  int32_t B, Hq, Hkv, D, nq;
+  int32_t q_dtype, kv_dtype, o_dtype;
+  const void* q;
+  int64_t q_stride_b, q_stride_t, q_stride_h;
+  const void* k;
+  const void* v;
+  int64_t kv_stride_b, kv_stride_h;
+  int32_t Lmax;
+  int32_t reserved0;
+  const int32_t* kv_len;      /* device [B] */
+  const int32_t* tree_parent; /* HOST [nq], or NULL for chain verify */
+  float scale;
+  int32_t reserved1;
+  void* o;
+  int64_t o_stride_b, o_stride_t, o_stride_h;
+  void* workspace;
+  size_t workspace_bytes;
+} spec_attn_args;
+
+/* Bytes of workspace spec_verify_attn needs for these sizes (host only, pure; reads no
+ * pointer).  Returns 0 if the sizes are invalid. */
+size_t spec_verify_attn_workspace(const spec_attn_args* args);
+int spec_verify_attn(const spec_attn_args* args, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_draft_window_attn
+ *
+ * Single-query draft attention over the last min(pos[b], W) tokens of sequence b, kept in a
+ * ring: token t (0-based) lives in slot t mod W.  pos[b] counts the tokens written including
+ * the current one.  If k_new/v_new are given, the current token's K/V are first written into
+ * slot (pos[b] - 1) mod W (the ring is updated in place).  The visible slots are then
+ * {t mod W : pos[b] - min(pos[b], W) <= t < pos[b]}; since softmax over keys does not depend on
+ * their order, this equals attention over the page's shift-left buffer.
+ *
+ * Layout: q [B, Hq, D] (q_stride_b, q_stride_h); rings [B, Hkv, W, D] (ring_stride_b,
+ * ring_stride_h; token stride D); k_new/v_new [B, Hkv, D] (new_stride_b, new_stride_h) or both
+ * NULL; o [B, Hq, D] (o_stride_b, o_stride_h); pos [B] int32 device.
+ * Types and limits as spec_verify_attn (nq = 1); W >= 1.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct spec_window_args {
+  int32_t B, Hq, Hkv, D, W;
+  int32_t q_dtype, kv_dtype, o_dtype;
+  const void* q;
+  int64_t q_stride_b, q_stride_h;
+  void* k_ring;
+  void* v_ring;
+  int64_t ring_stride_b, ring_stride_h;
+  const int32_t* pos; /* device [B] */
+  const void* k_new;  /* device [B, Hkv, D] or NULL */
+  const void* v_new;
+  int64_t new_stride_b, new_stride_h;
+  float scale;
+  int32_t reserved0;
+  void* o;
+  int64_t o_stride_b, o_stride_h;
+  void* workspace;
+  size_t workspace_bytes;
+} spec_window_args;
+
+size_t spec_draft_window_attn_workspace(const spec_window_args* args);
+int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_sample
+ *
+ * SPEC_SAMPLE_CHAIN (stochastic, temperature 1, n = gamma >= 1):
+ *   P_i = softmax(target_logits[b, i]), Q_i = softmax(draft_logits[b, i]).  For i = 1..gamma
+ *   accept x_i = draft_tokens[b, i-1] iff u_i * Q_i(x_i) < P_i(x_i) (u_i = uniforms[b, i-1]),
+ *   stopping at the first rejection (k accepted).  Then draw y by inverse CDF in token-id order
+ *   with u_{gamma+1} = uniforms[b, gamma] from r = max(P_{k+1} - Q_{k+1}, 0) if k < gamma, else
+ *   r = P_{gamma+1}: y = min{y : sum_{z<=y} r_z > u_{gamma+1} * sum r} (if sum r == 0, r = P_{k+1};
+ *   if no index qualifies through rounding, the largest y with r_y > 0).
+ *   Output: out_tokens[b, 0..k] = x_1..x_k, y; the rest of the row -1; out_num_accepted[b] = k.
+ * SPEC_SAMPLE_CHAIN_GREEDY (n = gamma >= 0): x_i accepted while it equals argmax P_i (ties to the
+ *   smallest id); then the argmax of row k+1 is emitted.  draft_logits and uniforms unused.
+ * SPEC_SAMPLE_TREE_GREEDY (n = N nodes, tree_parent HOST [N]): row i of target_logits holds the
+ *   logits after node i; node i >= 1 is accepted iff its parent is accepted and
+ *   draft_tokens[b, i] (the node's token) equals the argmax of its parent's row; node 0 (the last
+ *   committed token) is accepted.  The deepest accepted node d (ties to the smallest index) is
+ *   chosen: out_tokens = tokens of the path's nodes at depth 1..depth(d), then argmax of row d;
+ *   out_path_nodes (optional) = those node ids; out_num_accepted = depth(d).
+ *
+ * Layout: logits rows are V contiguous fp32; target_logits [B, rows_t, V] with batch stride
+ *   tl_stride_b (rows_t = gamma+1 chain, N tree); draft_logits [B, gamma, V] (dl_stride_b);
+ *   draft_tokens [B, gamma] or [B, N] int32 (tok_stride_b); uniforms [B, gamma+1] fp32 in [0, 1)
+ *   (u_stride_b); out_tokens / out_path_nodes [B, out_cols] int32 (row stride out_cols);
+ *   out_num_accepted [B] int32.
+ * Limits: V % 4 == 0, logits pointers 16-byte aligned and tl/dl strides multiples of 4;
+ *   1 <= B; chain: 1 <= gamma <= 32 (stochastic), 0 <= gamma <= 32 (greedy),
+ *   out_cols >= gamma + 1; tree: 1 <= N <= 64, out_cols >= max depth + 1.
+ * Floating point: exponentials in fp32, every sum above a thread's own few elements in fp64; the
+ * accept ratio uses fp64 exponentials of the two selected logits.
+ * ---------------------------------------------------------------------------------------- */
+enum { SPEC_SAMPLE_CHAIN = 0, SPEC_SAMPLE_CHAIN_GREEDY = 1, SPEC_SAMPLE_TREE_GREEDY = 2 };
+
+typedef struct spec_sample_args {
+  int32_t mode, B, n, V;
+  const float* target_logits;
+  int64_t tl_stride_b;
+  const float* draft_logits;
+  int64_t dl_stride_b;
+  const int32_t* draft_tokens;
+  int64_t tok_stride_b;
+  const int32_t* tree_parent; /* HOST [N] (tree mode) */
+  const float* uniforms;
+  int64_t u_stride_b;
+  int32_t out_cols;
+  int32_t reserved0;
+  int32_t* out_tokens;
+  int32_t* out_num_accepted;
+  int32_t* out_path_nodes; /* tree mode, optional */
+  void* workspace;
+  size_t workspace_bytes;
+} spec_sample_args;
+
+size_t spec_sample_workspace(const spec_sample_args* args);
+int spec_sample(const spec_sample_args* args, spec_stream_t stream);
+
+/* Text for a return code. */
+const char* spec_status_string(int status);
+/* ABI version: bump on any struct or semantic change. */
+int spec_abi_version(void);
+/* sizeof() of the argument structs as compiled into the library, so that a binding can check
+ * its own layout: which = 0 spec_attn_args, 1 spec_window_args, 2 spec_sample_args; else 0. */
+size_t spec_abi_struct_size(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

@@ -1,0 +1,345 @@
+// C ABI of libspecverify: argument validation, workspace sizing, TMA descriptor encoding and
+// kernel launches.  Nothing here allocates memory or keeps mutable state between calls (the
+// driver entry point for tensor-map encoding is looked up once and never changes).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sample_internal.h"
+#include "spec_verify.h"
+
+namespace {
+
+using specv::AttnParams;
+using specv::SampleParams;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tree: parent[0] == -1, 0 <= parent[i] < i.  Fills ancestor masks and depths; returns max depth
+// or -1 if malformed.
+int build_tree(const int32_t* parent, int N, unsigned long long* anc, int8_t* par8, int8_t* depth8) {
+  if (!parent || N < 1 || N > 64) return -1;
+  if (parent[0] != -1) return -1;
+  int depth[64];
+  depth[0] = 0;
+  if (anc) anc[0] = 1ull;
+  if (par8) par8[0] = -1;
+  int maxd = 0;
+  for (int i = 1; i < N; ++i) {
+    const int p = parent[i];
+    if (p < 0 || p >= i) return -1;
+    depth[i] = depth[p] + 1;
+    if (anc) anc[i] = anc[p] | (1ull << i);
+    if (par8) par8[i] = (int8_t)p;
+    if (depth[i] > maxd) maxd = depth[i];
+  }
+  if (depth8)
+    for (int i = 0; i < N; ++i) depth8[i] = (int8_t)depth[i];
+  return maxd;
+}
+
+bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int B, int64_t stride_h,
+                   int64_t stride_b) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)Hkv, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)stride_h * 2, (cuuint64_t)stride_b * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)specv::kKeyTile, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return sms;
+}
+
+// ------------------------------------------------------------------ attention validation
+struct AttnShape {
+  int B, Hq, Hkv, D, nq, Lmax, q_dtype, kv_dtype, o_dtype;
+};
+
+int check_attn_shape(const AttnShape& s) {
+  if (s.B < 1 || s.B > 4096 || s.Hq < 1 || s.Hkv < 1 || s.nq < 1 || s.Lmax < 1) return SPEC_ERR_INVALID_ARG;
+  if (s.Hq % s.Hkv != 0) return SPEC_ERR_INVALID_ARG;
+  if (s.D != 64 && s.D != 128) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)s.nq * (s.Hq / s.Hkv) > 1024) return SPEC_ERR_UNSUPPORTED;
+  if (s.kv_dtype != SPEC_F32 && s.kv_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (s.q_dtype != s.kv_dtype) return SPEC_ERR_UNSUPPORTED;
+  if (s.o_dtype != SPEC_F32 && s.o_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+int check_kv_layout(const void* k, const void* v, int kv_dtype, int64_t sb, int64_t sh) {
+  if (!k || !v) return SPEC_ERR_INVALID_ARG;
+  if (sb < 0 || sh < 0) return SPEC_ERR_INVALID_ARG;
+  if (kv_dtype == SPEC_BF16) {
+    if (!aligned(k, 16) || !aligned(v, 16) || (sb % 8) != 0 || (sh % 8) != 0) return SPEC_ERR_INVALID_ARG;
+  } else {
+    if (!aligned(k, 4) || !aligned(v, 4)) return SPEC_ERR_INVALID_ARG;
+  }
+  return SPEC_OK;
+}
+
+int check_q_layout(const void* q, int dtype, int64_t s0, int64_t s1, int64_t s2) {
+  if (!q || s0 < 0 || s1 < 0 || s2 < 0) return SPEC_ERR_INVALID_ARG;
+  if (dtype == SPEC_BF16 && (!aligned(q, 4) || (s0 % 2) || (s1 % 2) || (s2 % 2))) return SPEC_ERR_INVALID_ARG;
+  if (dtype == SPEC_F32 && !aligned(q, 4)) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+int check_o_layout(const void* o, int dtype, int64_t s0, int64_t s1, int64_t s2) {
+  if (!o || s0 < 0 || s1 < 0 || s2 < 0) return SPEC_ERR_INVALID_ARG;
+  if (!aligned(o, dtype == SPEC_BF16 ? 2 : 4)) return SPEC_ERR_INVALID_ARG;
+  return SPEC_OK;
+}
+
+int check_workspace(void* ws, size_t have, size_t need) {
+  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  if (!ws || have < need || !aligned(ws, 256)) return SPEC_ERR_WORKSPACE;
+  return SPEC_OK;
+}
+
+float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / sqrtf((float)D); }
+
+}  // namespace
+
+extern "C" {
+
+int spec_abi_version(void) { return 1; }
+
+size_t spec_abi_struct_size(int which) {
+  switch (which) {
+    case 0: return sizeof(spec_attn_args);
+    case 1: return sizeof(spec_window_args);
+    case 2: return sizeof(spec_sample_args);
+    default: return 0;
+  }
+}
+
+const char* spec_status_string(int s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case SPEC_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+// ------------------------------------------------------------------ spec_verify_attn
+size_t spec_verify_attn_workspace(const spec_attn_args* a) {
+  if (!a) return 0;
+  AttnShape s{a->B, a->Hq, a->Hkv, a->D, a->nq, a->Lmax, a->q_dtype, a->kv_dtype, a->o_dtype};
+  if (check_attn_shape(s) != SPEC_OK) return 0;
+  return specv::attn_workspace_bytes(a->B * a->Hkv, a->nq * (a->Hq / a->Hkv), a->D);
+}
+
+int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  AttnShape s{a->B, a->Hq, a->Hkv, a->D, a->nq, a->Lmax, a->q_dtype, a->kv_dtype, a->o_dtype};
+  int st = check_attn_shape(s);
+  if (st != SPEC_OK) return st;
+  if (a->Lmax < a->nq) return SPEC_ERR_INVALID_ARG;
+  if ((st = check_q_layout(a->q, a->q_dtype, a->q_stride_b, a->q_stride_t, a->q_stride_h)) != SPEC_OK) return st;
+  if ((st = check_kv_layout(a->k, a->v, a->kv_dtype, a->kv_stride_b, a->kv_stride_h)) != SPEC_OK) return st;
+  if ((st = check_o_layout(a->o, a->o_dtype, a->o_stride_b, a->o_stride_t, a->o_stride_h)) != SPEC_OK) return st;
+  if (!a->kv_len) return SPEC_ERR_INVALID_ARG;
+  if (!isfinite(a->scale)) return SPEC_ERR_INVALID_ARG;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.mask = specv::kMaskChain;
+  if (a->tree_parent) {
+    if (a->nq > 64) return SPEC_ERR_UNSUPPORTED;
+    if (build_tree(a->tree_parent, a->nq, p.anc, nullptr, nullptr) < 0) return SPEC_ERR_INVALID_ARG;
+    p.mask = specv::kMaskTree;
+  }
+  const size_t need = spec_verify_attn_workspace(a);
+  if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
+
+  p.B = a->B; p.Hq = a->Hq; p.Hkv = a->Hkv; p.G = a->Hq / a->Hkv; p.D = a->D; p.nq = a->nq;
+  p.rows = a->nq * p.G;
+  p.Lmax = a->Lmax;
+  p.is_window = 0;
+  p.lens = a->kv_len;
+  p.q = a->q; p.q_sb = a->q_stride_b; p.q_st = a->q_stride_t; p.q_sh = a->q_stride_h;
+  p.k = a->k; p.v = a->v; p.kv_sb = a->kv_stride_b; p.kv_sh = a->kv_stride_h;
+  p.scale_log2 = resolve_scale(a->scale, a->D) * 1.4426950408889634f;
+  p.o = a->o; p.o_sb = a->o_stride_b; p.o_st = a->o_stride_t; p.o_sh = a->o_stride_h;
+  p.o_bf16 = a->o_dtype == SPEC_BF16;
+  specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
+
+  CUtensorMap tmK, tmV;
+  const int bf16 = a->kv_dtype == SPEC_BF16;
+  if (bf16) {
+    if (!encode_kv_map(&tmK, a->k, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b) ||
+        !encode_kv_map(&tmV, a->v, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b))
+      return SPEC_ERR_CUDA;
+  }
+  cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ spec_draft_window_attn
+size_t spec_draft_window_attn_workspace(const spec_window_args* a) {
+  if (!a) return 0;
+  AttnShape s{a->B, a->Hq, a->Hkv, a->D, 1, a->W, a->q_dtype, a->kv_dtype, a->o_dtype};
+  if (check_attn_shape(s) != SPEC_OK) return 0;
+  return specv::attn_workspace_bytes(a->B * a->Hkv, a->Hq / a->Hkv, a->D);
+}
+
+int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  AttnShape s{a->B, a->Hq, a->Hkv, a->D, 1, a->W, a->q_dtype, a->kv_dtype, a->o_dtype};
+  int st = check_attn_shape(s);
+  if (st != SPEC_OK) return st;
+  if ((st = check_q_layout(a->q, a->q_dtype, a->q_stride_b, 0, a->q_stride_h)) != SPEC_OK) return st;
+  if ((st = check_kv_layout(a->k_ring, a->v_ring, a->kv_dtype, a->ring_stride_b, a->ring_stride_h)) != SPEC_OK)
+    return st;
+  if ((st = check_o_layout(a->o, a->o_dtype, a->o_stride_b, 0, a->o_stride_h)) != SPEC_OK) return st;
+  if (!a->pos) return SPEC_ERR_INVALID_ARG;
+  if ((a->k_new == nullptr) != (a->v_new == nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (a->k_new && (a->new_stride_b < 0 || a->new_stride_h < 0)) return SPEC_ERR_INVALID_ARG;
+  if (!isfinite(a->scale)) return SPEC_ERR_INVALID_ARG;
+  const size_t need = spec_draft_window_attn_workspace(a);
+  if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int bf16 = a->kv_dtype == SPEC_BF16;
+  if (a->k_new) {
+    specv::WindowAppend w;
+    w.B = a->B; w.Hkv = a->Hkv; w.D = a->D; w.W = a->W; w.bf16 = bf16;
+    w.pos = a->pos; w.k_ring = a->k_ring; w.v_ring = a->v_ring;
+    w.ring_sb = a->ring_stride_b; w.ring_sh = a->ring_stride_h;
+    w.k_new = a->k_new; w.v_new = a->v_new; w.new_sb = a->new_stride_b; w.new_sh = a->new_stride_h;
+    if (specv::launch_window_append(w, cs) != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B; p.Hq = a->Hq; p.Hkv = a->Hkv; p.G = a->Hq / a->Hkv; p.D = a->D; p.nq = 1;
+  p.rows = p.G;
+  p.mask = specv::kMaskNone;
+  p.Lmax = a->W;
+  p.is_window = 1;
+  p.lens = a->pos;
+  p.q = a->q; p.q_sb = a->q_stride_b; p.q_st = 0; p.q_sh = a->q_stride_h;
+  p.k = a->k_ring; p.v = a->v_ring; p.kv_sb = a->ring_stride_b; p.kv_sh = a->ring_stride_h;
+  p.scale_log2 = resolve_scale(a->scale, a->D) * 1.4426950408889634f;
+  p.o = a->o; p.o_sb = a->o_stride_b; p.o_st = 0; p.o_sh = a->o_stride_h;
+  p.o_bf16 = a->o_dtype == SPEC_BF16;
+  specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
+  CUtensorMap tmK, tmV;
+  if (bf16) {
+    if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b) ||
+        !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b))
+      return SPEC_ERR_CUDA;
+  }
+  cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16, cs);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ spec_sample
+static int sample_rows(const spec_sample_args* a, int* rows_t, int* rows_d) {
+  switch (a->mode) {
+    case SPEC_SAMPLE_CHAIN:
+      if (a->n < 1 || a->n > specv::kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+      *rows_t = a->n + 1; *rows_d = a->n;
+      return SPEC_OK;
+    case SPEC_SAMPLE_CHAIN_GREEDY:
+      if (a->n < 0 || a->n > specv::kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+      *rows_t = a->n + 1; *rows_d = 0;
+      return SPEC_OK;
+    case SPEC_SAMPLE_TREE_GREEDY:
+      if (a->n < 1 || a->n > specv::kMaxTreeNodes) return SPEC_ERR_UNSUPPORTED;
+      *rows_t = a->n; *rows_d = 0;
+      return SPEC_OK;
+    default: return SPEC_ERR_INVALID_ARG;
+  }
+}
+
+size_t spec_sample_workspace(const spec_sample_args* a) {
+  if (!a) return 0;
+  int rt, rd;
+  if (sample_rows(a, &rt, &rd) != SPEC_OK) return 0;
+  if (a->B < 1 || a->V < 1 || a->V > (1 << 20)) return 0;
+  return specv::sample_workspace_bytes(a->mode, a->B, rt, rd, a->V);
+}
+
+int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  int rt, rd;
+  int st = sample_rows(a, &rt, &rd);
+  if (st != SPEC_OK) return st;
+  if (a->B < 1 || a->V < 1) return SPEC_ERR_INVALID_ARG;
+  if (a->V > (1 << 20) || (a->V % 4) != 0) return SPEC_ERR_UNSUPPORTED;
+  if (a->V > specv::kSmallVocab && a->B > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (!a->target_logits || !aligned(a->target_logits, 16) || a->tl_stride_b < 0 || (a->tl_stride_b % 4))
+    return SPEC_ERR_INVALID_ARG;
+  if (!a->out_tokens || !a->out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (a->mode == SPEC_SAMPLE_CHAIN) {
+    if (!a->draft_logits || !aligned(a->draft_logits, 16) || a->dl_stride_b < 0 || (a->dl_stride_b % 4))
+      return SPEC_ERR_INVALID_ARG;
+    if (!a->uniforms || a->u_stride_b < 0) return SPEC_ERR_INVALID_ARG;
+  }
+  if ((a->mode != SPEC_SAMPLE_CHAIN_GREEDY || a->n > 0) && (!a->draft_tokens || a->tok_stride_b < 0))
+    return SPEC_ERR_INVALID_ARG;
+  SampleParams p;
+  memset(&p, 0, sizeof(p));
+  if (a->mode == SPEC_SAMPLE_TREE_GREEDY) {
+    const int maxd = build_tree(a->tree_parent, a->n, nullptr, p.parent, p.depth);
+    if (maxd < 0) return SPEC_ERR_INVALID_ARG;
+    if (a->out_cols < maxd + 1) return SPEC_ERR_INVALID_ARG;
+    p.N = a->n;
+  } else if (a->out_cols < a->n + 1) {
+    return SPEC_ERR_INVALID_ARG;
+  }
+  const size_t need = spec_sample_workspace(a);
+  if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
+  const int sms = num_sms();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+
+  p.mode = a->mode; p.B = a->B; p.V = a->V;
+  p.gamma = a->mode == SPEC_SAMPLE_TREE_GREEDY ? 0 : a->n;
+  p.rows_t = rt; p.rows_d = rd;
+  p.tl = a->target_logits; p.tl_sb = a->tl_stride_b;
+  p.dl = a->draft_logits; p.dl_sb = a->dl_stride_b;
+  p.tok = a->draft_tokens; p.tok_sb = a->tok_stride_b;
+  p.u = a->uniforms; p.u_sb = a->u_stride_b;
+  p.out_cols = a->out_cols; p.out_tok = a->out_tokens; p.out_nacc = a->out_num_accepted;
+  p.out_nodes = a->out_path_nodes;
+  specv::sample_workspace_carve(a->workspace, &p);
+  cudaError_t e = specv::launch_sample(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"

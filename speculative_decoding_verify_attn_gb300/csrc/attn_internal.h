@@ -1,0 +1,68 @@
+// Internal interface between the C ABI (api.cpp) and the attention kernels (attn.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace specv {
+
+// Keys per TMA stage and pipeline depth of the bf16 split-KV kernel.
+constexpr int kKeyTile = 64;
+constexpr int kStages = 3;
+// Query rows one CTA row-group holds (4 warps x 16 rows of mma.sync tiles).
+constexpr int kRowsPerGroup = 64;
+// Upper bound on CTAs along the key axis; the workspace is sized for it.
+constexpr int kMaxGridX = 1024;
+// Minimum keys a CTA takes, so that short total work does not spread over every SM.
+constexpr int kMinKeysPerCta = 256;
+// Key-slice count per row tile is at most 4 (one warp per slice).
+constexpr int kMaxSlices = 4;
+
+enum MaskMode : int { kMaskNone = 0, kMaskChain = 1, kMaskTree = 2 };
+
+// Everything a partial/merge kernel needs; passed by value as a __grid_constant__ parameter.
+struct AttnParams {
+  int B, Hq, Hkv, G, D, nq, rows;  // rows = nq * G query rows per (sequence, kv head)
+  int mask;                        // MaskMode
+  int Lmax;                        // verify: cache capacity; window: W
+  int is_window;                   // lengths come from pos (min(pos, W); pos < 1 invalid)
+  const int32_t* lens;             // kv_len or pos, device [B]
+  const void* q;
+  int64_t q_sb, q_st, q_sh;
+  const void* k;
+  const void* v;
+  int64_t kv_sb, kv_sh;
+  float scale_log2;                // scale * log2(e)
+  void* o;
+  int64_t o_sb, o_st, o_sh;
+  int o_bf16;
+  int grid_x;                      // CTAs along the key axis (same value in partial and merge)
+  float* part_o;                   // [slots][kMaxSlices][rows][D]
+  float2* part_ml;                 // [slots][kMaxSlices][rows]  (m in log2 units, l)
+  uint32_t* status;
+  unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
+};
+
+struct WindowAppend {
+  int B, Hkv, D, W, bf16;
+  const int32_t* pos;
+  void* k_ring;
+  void* v_ring;
+  int64_t ring_sb, ring_sh;
+  const void* k_new;
+  const void* v_new;
+  int64_t new_sb, new_sh;
+};
+
+// Workspace layout for the attention kernels (bytes), for a given number of segments and rows.
+size_t attn_workspace_bytes(int segments, int rows, int D);
+void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p);
+
+// Launch helpers; return a cudaError_t.  tmK/tmV are used by the bf16 path only.
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
+                             cudaStream_t stream);
+cudaError_t launch_window_append(const WindowAppend& a, cudaStream_t stream);
+
+}  // namespace specv

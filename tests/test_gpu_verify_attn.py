@@ -1,0 +1,184 @@
+"""GPU parity: spec_verify_attn (chain and tree) through the C ABI against the CPU oracle.
+
+Sizes the oracle finishes in seconds still span several 64-key tiles, several CTAs per sequence
+and ragged tails; K/V slots past kv_len hold NaN; planted needles make mask leaks visible.  The
+full-size workloads are checked on sampled (sequence, row, head) outputs.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import attn as oa
+from workloads import gen
+from workloads.configs import CONFIGS
+
+from .helpers import assert_attn_close, to_dev, to_np, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verify_attn_gb300 as sv
+    sv.lib()
+    return sv
+
+
+def run_verify(sv, inp, kv_dtype, out_dtype="f32", tree_parent=None):
+    torch = torch_mod()
+    q = to_dev(inp["q"], kv_dtype)
+    k = to_dev(inp["k"], kv_dtype)
+    v = to_dev(inp["v"], kv_dtype)
+    kv_len = to_dev(inp["kv_len"], "i32")
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16 if out_dtype == "bf16" else torch.float32,
+                   device=q.device)
+    ws = torch.empty(sv.spec_verify_attn_workspace(q, k, o), dtype=torch.uint8, device=q.device)
+    sv.spec_verify_attn(q, k, v, kv_len, o, tree_parent=tree_parent, workspace=ws)
+    torch.cuda.synchronize()
+    return to_np(o), sv.read_status(ws)
+
+
+def test_tiny_config_fp32(sv):
+    cfg = CONFIGS["tiny"]
+    kv_len = gen.kv_lengths(cfg.B, *cfg.ctx, cfg.seed)
+    inp = gen.attn_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.nq, kv_len, int(kv_len.max()), "f32", cfg.seed)
+    o, st = run_verify(sv, inp, "f32")
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len)
+    assert st == 0
+    assert_attn_close(o, ref, "f32", what="tiny")
+
+
+@pytest.mark.parametrize("name,B,lens", [
+    ("llama3-8b-layer", 3, [1500, 2113, 777]),
+    ("magicdec-64k", 2, [2600, 2600]),
+    ("llama3-70b-layer", 2, [1900, 1023]),
+])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_chain_bf16_scaled(sv, name, B, lens, out_dtype):
+    cfg = CONFIGS[name]
+    kv_len = np.array(lens, dtype=np.int32)
+    Lmax = int(kv_len.max()) + 37
+    inp = gen.attn_inputs(B, cfg.Hq, cfg.Hkv, cfg.D, cfg.nq, kv_len, Lmax, "bf16", cfg.seed)
+    inp = gen.plant_chain_needles(inp, cfg.nq, "bf16", cfg.seed)
+    o, st = run_verify(sv, inp, "bf16", out_dtype)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len)
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", out_dtype, what=name)
+
+
+def test_tree_bf16_scaled(sv):
+    cfg = CONFIGS["medusa-tree-8k"]
+    parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+    kv_len = np.array([1100, 700], dtype=np.int32)
+    inp = gen.attn_inputs(2, cfg.Hq, cfg.Hkv, cfg.D, cfg.nq, kv_len, 1200, "bf16", cfg.seed)
+    inp = gen.plant_tree_needles(inp, parent, "bf16", cfg.seed)
+    o, st = run_verify(sv, inp, "bf16", tree_parent=parent)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what="tree")
+
+
+def test_chain_shaped_tree_matches_chain_on_gpu(sv):
+    cfg = CONFIGS["llama3-8b-layer"]
+    kv_len = np.array([640, 333], dtype=np.int32)
+    inp = gen.attn_inputs(2, cfg.Hq, cfg.Hkv, cfg.D, cfg.nq, kv_len, 700, "bf16", 7)
+    chain, _ = run_verify(sv, inp, "bf16")
+    tree, _ = run_verify(sv, inp, "bf16", tree_parent=np.arange(-1, cfg.nq - 1))
+    assert np.max(np.abs(chain - tree)) <= 1e-6
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_head_dims_and_group_sizes(sv, D):
+    kv_len = np.array([300, 129, 64], dtype=np.int32)
+    for Hq, Hkv, nq in ((8, 8, 3), (16, 2, 2), (12, 4, 9)):
+        inp = gen.attn_inputs(3, Hq, Hkv, D, nq, kv_len, 320, "bf16", 21 + Hq)
+        o, st = run_verify(sv, inp, "bf16")
+        ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len)
+        assert st == 0
+        assert_attn_close(o, ref, "bf16", what=f"D{D} Hq{Hq} Hkv{Hkv} nq{nq}")
+
+
+def test_fp32_tree_and_d128(sv):
+    parent = np.array([-1, 0, 0, 1, 1, 2, 3, 3])
+    kv_len = np.array([90, 40], dtype=np.int32)
+    inp = gen.attn_inputs(2, 8, 2, 128, len(parent), kv_len, 96, "f32", 33)
+    o, st = run_verify(sv, inp, "f32", tree_parent=parent)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    assert st == 0
+    assert_attn_close(o, ref, "f32", what="fp32 tree")
+
+
+def test_edge_no_context_and_bad_lengths(sv):
+    # kv_len == nq (only the new tokens), and invalid lengths (< nq, > Lmax) -> zeros + status flag
+    nq = 5
+    kv_len = np.array([nq, 200, 3, 999], dtype=np.int32)
+    Lmax = 256
+    safe = np.minimum(np.maximum(kv_len, 0), Lmax)
+    inp = gen.attn_inputs(4, 8, 2, 128, nq, safe, Lmax, "bf16", 44)
+    inp["kv_len"] = kv_len
+    o, st = run_verify(sv, inp, "bf16")
+    assert st & 1, "SPEC_STATUS_BAD_KV_LEN expected"
+    for b in (2, 3):
+        assert np.all(o[b] == 0.0)
+    for b in (0, 1):
+        ref = oa.verify_attn(inp["q"][b:b + 1], inp["k"][b:b + 1], inp["v"][b:b + 1], kv_len[b:b + 1])
+        assert_attn_close(o[b:b + 1], ref, "bf16", what=f"edge b{b}")
+
+
+def test_single_query_single_key(sv):
+    # nq = 1, kv_len = 1: the output is exactly v of the only key (bf16-exact, fp32 output)
+    inp = gen.attn_inputs(1, 4, 1, 64, 1, np.array([1], np.int32), 8, "bf16", 55)
+    o, _ = run_verify(sv, inp, "bf16")
+    assert np.allclose(o[0, 0], np.repeat(inp["v"][0, 0, 0][None], 4, 0), atol=1e-6)
+
+
+def _device_inputs(cfg, seed):
+    """Full-size inputs generated on the device (seeded torch generator)."""
+    torch = torch_mod()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    kv_len = gen.kv_lengths(cfg.B, *cfg.ctx, cfg.seed)
+    Lmax = int(kv_len.max())
+    shape = (cfg.B, cfg.Hkv, Lmax, cfg.D)
+    k = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    for b in range(cfg.B):
+        k[b] = torch.randn(shape[1:], generator=g, device="cuda").to(torch.bfloat16)
+        v[b] = torch.randn(shape[1:], generator=g, device="cuda").to(torch.bfloat16)
+    q = torch.randn((cfg.B, cfg.nq, cfg.Hq, cfg.D), generator=g, device="cuda").to(torch.bfloat16)
+    return q, k, v, kv_len
+
+
+@pytest.mark.parametrize("name", ["magicdec-64k", "llama3-70b-layer", "medusa-tree-8k", "llama3-8b-layer"])
+def test_full_size_sampled_outputs(sv, name):
+    torch = torch_mod()
+    cfg = CONFIGS[name]
+    q, k, v, kv_len = _device_inputs(cfg, cfg.seed)
+    parent = None
+    if cfg.tree_nodes:
+        parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    kvl = to_dev(kv_len, "i32")
+    sv.spec_verify_attn(q, k, v, kvl, o, tree_parent=parent)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(cfg.seed)
+    G = cfg.G
+    worst = 0.0
+    for _ in range(6):
+        b = int(rng.integers(cfg.B))
+        g = int(rng.integers(cfg.Hkv))
+        L = int(kv_len[b])
+        kb = k[b, g, :L].float().cpu().numpy().astype(np.float64)
+        vb = v[b, g, :L].float().cpu().numpy().astype(np.float64)
+        for j in (0, cfg.nq - 1, int(rng.integers(cfg.nq))):
+            h = g * G + int(rng.integers(G))
+            qv = q[b, j, h].float().cpu().numpy()
+            vis = oa.chain_visible(L, cfg.nq, j) if parent is None else oa.tree_visible(L, parent, j)
+            ref = oa.attend(qv, kb[vis], vb[vis], 1.0 / np.sqrt(cfg.D))
+            got = o[b, j, h].cpu().numpy()
+            err = float(np.max(np.abs(got - ref)))
+            rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+            worst = max(worst, err)
+            assert err <= 2e-2 and rel <= 1e-2, (name, b, j, h, err, rel)
+    del k, v
+    torch.cuda.empty_cache()

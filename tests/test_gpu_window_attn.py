@@ -1,0 +1,107 @@
+"""GPU parity: spec_draft_window_attn (ring-buffer draft window) against the CPU oracle."""
+
+import numpy as np
+import pytest
+
+from oracle import attn as oa
+from workloads import gen
+from workloads.configs import CONFIGS
+
+from .helpers import assert_attn_close, to_dev, to_np, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verify_attn_gb300 as sv
+    sv.lib()
+    return sv
+
+
+def _run(sv, q, kr, vr, pos, kn, vn, dtype):
+    torch = torch_mod()
+    o = torch.full(q.shape, float("nan"), dtype=torch.float32, device=q.device)
+    ws = torch.empty(sv.spec_draft_window_attn_workspace(q, kr, o), dtype=torch.uint8, device=q.device)
+    sv.spec_draft_window_attn(q, kr, vr, pos, o, k_new=kn, v_new=vn, workspace=ws)
+    torch.cuda.synchronize()
+    return to_np(o), sv.read_status(ws)
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("f32", 64, 4, 1), ("bf16", 64, 8, 2)])
+def test_window_with_append_many_positions(sv, dtype, D, Hq, Hkv):
+    W = 512
+    pos = np.array([1, 100, 511, 512, 513, 1800, 70000], dtype=np.int32)
+    B = len(pos)
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, pos, dtype, seed=5 + D)
+    q, kr, vr = to_dev(inp["q"], dtype), to_dev(inp["k_ring"], dtype), to_dev(inp["v_ring"], dtype)
+    kn, vn = to_dev(inp["k_new"], dtype), to_dev(inp["v_new"], dtype)
+    o, st = _run(sv, q, kr, vr, to_dev(pos, "i32"), kn, vn, dtype)
+    ref, k_after, v_after = oa.draft_window_attn(inp["q"], inp["k_ring"], inp["v_ring"], pos,
+                                                 inp["k_new"], inp["v_new"])
+    assert st == 0
+    assert_attn_close(o, ref, dtype, what="window")
+    # the append wrote the current token's slot and nothing else
+    kr_np = to_np(kr)
+    for b in range(B):
+        s = (pos[b] - 1) % W
+        assert np.array_equal(kr_np[b, :, s], k_after[b, :, s].astype(np.float32))
+        other = [t for t in oa.window_slots(int(pos[b]), W) if t != s]
+        assert np.array_equal(kr_np[b][:, other], inp["k_ring"][b][:, other])
+
+
+def test_magicdec_draft_round_four_steps(sv):
+    """Four draft steps of a round, each appending one token, on the MagicDec window shape."""
+    cfg = CONFIGS["magicdec-64k"]
+    B, W = 6, cfg.window
+    pos0 = np.array([65536, 65537, 300, 509, 512, 1024], dtype=np.int32)
+    inp = gen.window_inputs(B, cfg.Hq, cfg.Hkv, cfg.D, W, pos0, "bf16", seed=cfg.seed)
+    kr, vr = to_dev(inp["k_ring"], "bf16"), to_dev(inp["v_ring"], "bf16")
+    k_ring, v_ring = inp["k_ring"], inp["v_ring"]
+    r = np.random.default_rng(cfg.seed)
+    for step in range(cfg.draft_steps):
+        pos = pos0 + step
+        q = gen.store(r.standard_normal((B, cfg.Hq, cfg.D)).astype(np.float32), "bf16")
+        kn = gen.store(r.standard_normal((B, cfg.Hkv, cfg.D)).astype(np.float32), "bf16")
+        vn = gen.store(r.standard_normal((B, cfg.Hkv, cfg.D)).astype(np.float32), "bf16")
+        o, st = _run(sv, to_dev(q, "bf16"), kr, vr, to_dev(pos, "i32"), to_dev(kn, "bf16"), to_dev(vn, "bf16"), "bf16")
+        ref, k_ring, v_ring = oa.draft_window_attn(q, k_ring, v_ring, pos, kn, vn)
+        assert st == 0
+        assert_attn_close(o, ref, "bf16", what=f"step {step}")
+
+
+def test_window_without_append_and_bad_pos(sv):
+    W, D, Hq, Hkv = 64, 128, 8, 2
+    pos = np.array([0, 10, 64, 200], dtype=np.int32)
+    inp = gen.window_inputs(4, Hq, Hkv, D, W, np.maximum(pos, 1), "bf16", seed=9)
+    # without an append the current token must already be in its slot: fill slot (pos-1) mod W
+    kr, vr = inp["k_ring"].copy(), inp["v_ring"].copy()
+    for b in range(4):
+        if pos[b] >= 1:
+            kr[b, :, (pos[b] - 1) % W] = inp["k_new"][b]
+            vr[b, :, (pos[b] - 1) % W] = inp["v_new"][b]
+    o, st = _run(sv, to_dev(inp["q"], "bf16"), to_dev(kr, "bf16"), to_dev(vr, "bf16"), to_dev(pos, "i32"),
+                 None, None, "bf16")
+    assert st & 2, "SPEC_STATUS_BAD_POS expected for pos = 0"
+    assert np.all(o[0] == 0.0)
+    ref, _, _ = oa.draft_window_attn(inp["q"][1:], kr[1:], vr[1:], pos[1:])
+    assert_attn_close(o[1:], ref, "bf16", what="no append")
+
+
+def test_window_covering_context_equals_verify(sv):
+    """W >= context: the window call equals single-query chain verify over the same keys."""
+    torch = torch_mod()
+    W, D, Hq, Hkv = 256, 128, 16, 4
+    pos = np.array([256, 97], dtype=np.int32)
+    inp = gen.window_inputs(2, Hq, Hkv, D, W, pos, "bf16", seed=12)
+    kr, vr = inp["k_ring"].copy(), inp["v_ring"].copy()
+    for b in range(2):
+        kr[b, :, pos[b] - 1] = inp["k_new"][b]
+        vr[b, :, pos[b] - 1] = inp["v_new"][b]
+    o_win, _ = _run(sv, to_dev(inp["q"], "bf16"), to_dev(kr, "bf16"), to_dev(vr, "bf16"), to_dev(pos, "i32"),
+                    None, None, "bf16")
+    q4 = to_dev(inp["q"][:, None], "bf16")
+    o_ver = torch.empty(q4.shape, dtype=torch.float32, device=q4.device)
+    sv.spec_verify_attn(q4, to_dev(kr, "bf16"), to_dev(vr, "bf16"), to_dev(pos, "i32"), o_ver)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(o_win - to_np(o_ver)[:, 0])) <= 1e-6
