@@ -43,7 +43,10 @@ def gpu_chain(sv, inp, mode=None):
     return to_np(out), to_np(nacc), sv.read_status(ws)
 
 
-def compare_chain(inp, out, nacc, what, max_near_frac=0.01):
+def compare_chain(inp, out, nacc, what, max_near_frac=0.5):
+    """Bit-exact outside the near-threshold band.  With a 128K vocabulary the band for the final
+    draw (1e-6 * R around any CDF step) is comparable to one token's mass, so a sizeable share of
+    draws falls inside it; those are counted, and how many of them still match is reported."""
     ref_out, ref_k, near = osm.spec_sample_chain(inp["target_logits"], inp["draft_logits"],
                                                  inp["draft_tokens"], inp["uniforms"])
     far = ~near
@@ -51,6 +54,8 @@ def compare_chain(inp, out, nacc, what, max_near_frac=0.01):
     bad_t = np.nonzero(np.any(out != ref_out, axis=1) & far)[0]
     assert len(bad_k) == 0, f"{what}: accepted counts differ at {bad_k[:10]} ({nacc[bad_k[:5]]} vs {ref_k[bad_k[:5]]})"
     assert len(bad_t) == 0, f"{what}: tokens differ at {bad_t[:10]}"
+    near_match = int(np.sum(near & (nacc == ref_k) & np.all(out == ref_out, axis=1)))
+    print(f"{what}: {len(near)} sequences, {int(near.sum())} near-threshold ({near_match} of them match too)")
     assert near.mean() <= max_near_frac, f"{what}: {near.sum()} near-threshold sequences"
     return int(near.sum())
 
