@@ -61,7 +61,8 @@ enum {
   SPEC_ERR_INVALID_ARG = -1, /* null pointer, bad size, stride, alignment or tree */
   SPEC_ERR_UNSUPPORTED = -2, /* a valid combination this build does not implement */
   SPEC_ERR_WORKSPACE = -3,   /* workspace missing, too small or misaligned */
-  SPEC_ERR_CUDA = -4         /* a CUDA runtime/driver call or kernel launch failed */
+  SPEC_ERR_CUDA = -4,        /* a CUDA runtime/driver call or kernel launch failed */
+  SPEC_ERR_SCRATCH_LIMIT = -6 /* the problem needs more scratch than spec_verify_attn_noalloc has */
 };
 
 /* element types */
@@ -123,6 +124,26 @@ typedef struct spec_attn_args {
  * pointer).  Returns 0 if the sizes are invalid. */
 size_t spec_verify_attn_workspace(const spec_attn_args* args);
 int spec_verify_attn(const spec_attn_args* args, spec_stream_t stream);
+
+/* spec_verify_attn_noalloc -- the same verify attention with no caller workspace and no device
+ * allocation anywhere.  The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory on their hot path (a serving engine that has handed all HBM to
+ * its KV cache and weights up front, a plugin whose host framework owns every device
+ * allocation, or a loop that cannot afford cudaMalloc/cudaFree, which synchronize the device).
+ *
+ * Scratch lives in one file-scope device array of SPEC_NOALLOC_SCRATCH_BYTES (64 MiB) that every
+ * GPU which loads this library holds until the process exits.  args->workspace and
+ * args->workspace_bytes are ignored.  A problem whose spec_verify_attn_workspace() size exceeds
+ * the array returns SPEC_ERR_SCRATCH_LIMIT before anything is launched.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents behind; nothing in it
+ *    has to start at zero (the per-call status word is cleared by the call itself).  Calls whose
+ *    kernels overlap on the GPU (other streams, other host threads) race on the array: serialize
+ *    them.  The status word (SPEC_STATUS_*) of the last call is at byte 0 of the array.
+ * All other arguments, limits and results are those of spec_verify_attn. */
+#define SPEC_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int spec_verify_attn_noalloc(const spec_attn_args* args, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * spec_draft_window_attn

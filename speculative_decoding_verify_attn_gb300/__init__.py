@@ -10,3 +10,4 @@ from .binding import (  # noqa: F401
     SpecWindowArgs, lib, read_status, spec_abi_version, spec_draft_window_attn, spec_draft_window_attn_workspace,
     spec_sample, spec_sample_workspace, spec_status_string, spec_verify_attn, spec_verify_attn_workspace,
 )
+from .binding import SPEC_ERR_SCRATCH_LIMIT, spec_verify_attn_noalloc  # noqa: F401,E402

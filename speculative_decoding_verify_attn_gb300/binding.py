@@ -330,3 +330,29 @@ def spec_sample(mode, target_logits, out_tokens, out_num_accepted, *, draft_logi
 def read_status(workspace) -> int:
     """The device status word (first 4 bytes of a workspace) after the stream is synchronized."""
     return int(workspace[:4].view(_torch().int32).item())
+
+
+# ---------------------------------------------------------------------------- no-allocation verify
+SPEC_ERR_SCRATCH_LIMIT = -6
+_noalloc_fn = None
+
+
+def spec_verify_attn_noalloc(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0, stream=None):
+    """spec_verify_attn for callers that cannot allocate device memory: the library uses its own
+    fixed 64 MiB device scratch array instead of a caller workspace, and nothing here allocates
+    (no torch workspace either).  Calls on one device share that array, so calls whose kernels
+    overlap on the GPU must not be issued; the first call on a device must precede any stream
+    capture.  Writes o and returns it."""
+    global _noalloc_fn
+    _check_cuda(q, k, v, kv_len, o)
+    if _noalloc_fn is None:
+        fn = lib().spec_verify_attn_noalloc
+        fn.argtypes = [POINTER(SpecAttnArgs), c_void_p]
+        fn.restype = c_int
+        _noalloc_fn = fn
+    a, keep = verify_attn_args(q, k, v, kv_len, o, tree_parent, scale, None)
+    st = _noalloc_fn(byref(a), _stream_handle(stream))
+    del keep
+    if st != SPEC_OK:
+        raise SpecError(st, "spec_verify_attn_noalloc")
+    return o

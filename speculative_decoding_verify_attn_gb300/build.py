@@ -21,7 +21,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIBNAME = "libspecverify.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
-SOURCES = ["attn.cu", "sample.cu", "api.cpp"]
+SOURCES = ["attn.cu", "sample.cu", "api.cpp", "noalloc.cu"]
 HEADERS = ["common.cuh", "attn_internal.h", "sample_internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -152,6 +152,7 @@ const char* spec_status_string(int s) {
     case SPEC_ERR_UNSUPPORTED: return "unsupported configuration";
     case SPEC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case SPEC_ERR_CUDA: return "CUDA error";
+    case SPEC_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-allocation entry point holds";
     default: return "unknown status";
   }
 }
