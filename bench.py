@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling a small case)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -407,6 +408,9 @@ def run_reference(args, cfg):
 def main():
     args = parse()
     cfg = get_config(args.workload)
+    if args.batch:
+        from workloads.configs import scaled
+        cfg = scaled(cfg, B=args.batch)
     if args.impl == "reference":
         return run_reference(args, cfg)
     import torch
