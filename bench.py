@@ -36,6 +36,7 @@ from workloads.configs import get_config  # noqa: E402
 METRIC = "verify-attn KV GB/s (% HBM peak); spec_sample rounds/s; at 1 GB300"
 DEFAULT_WORKLOAD = "magicdec-64k"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 << 20
 
 
 def parse():
@@ -153,6 +154,7 @@ class ClockSampler:
 def make_inputs(cfg, device, seed):
     """Seeded synthetic inputs generated on the device (torch Philox generator)."""
     import torch
+    from workloads import gen
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     B, Hq, Hkv, D, nq, V, gamma = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.nq, cfg.vocab, cfg.gamma
@@ -160,25 +162,43 @@ def make_inputs(cfg, device, seed):
     kv_len_h = np.random.default_rng([seed, 4]).integers(lo, hi + 1, size=B).astype(np.int32) if lo != hi \
         else np.full(B, lo, np.int32)
     Lmax = int(kv_len_h.max())
-    bf = torch.bfloat16
-    k = torch.empty((B, Hkv, Lmax, D), dtype=bf, device=device)
-    v = torch.empty((B, Hkv, Lmax, D), dtype=bf, device=device)
+    dt = torch.bfloat16 if cfg.kv_dtype == "bf16" else torch.float32
+    k = torch.empty((B, Hkv, Lmax, D), dtype=dt, device=device)
+    v = torch.empty((B, Hkv, Lmax, D), dtype=dt, device=device)
     for b in range(B):
-        k[b] = torch.randn((Hkv, Lmax, D), generator=g, device=device).to(bf)
-        v[b] = torch.randn((Hkv, Lmax, D), generator=g, device=device).to(bf)
+        k[b] = torch.randn((Hkv, Lmax, D), generator=g, device=device).to(dt)
+        v[b] = torch.randn((Hkv, Lmax, D), generator=g, device=device).to(dt)
     inp = dict(k=k, v=v, kv_len_h=kv_len_h, kv_len=torch.from_numpy(kv_len_h).to(device))
-    inp["q"] = torch.randn((B, nq, Hq, D), generator=g, device=device).to(bf)
+    inp["q"] = torch.randn((B, nq, Hq, D), generator=g, device=device).to(dt)
     inp["o"] = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=device)
+    inp["tree"] = None
     W = cfg.window
     if W:
-        inp["k_ring"] = torch.randn((B, Hkv, W, D), generator=g, device=device).to(bf)
-        inp["v_ring"] = torch.randn((B, Hkv, W, D), generator=g, device=device).to(bf)
+        inp["k_ring"] = torch.randn((B, Hkv, W, D), generator=g, device=device).to(dt)
+        inp["v_ring"] = torch.randn((B, Hkv, W, D), generator=g, device=device).to(dt)
         inp["pos0"] = kv_len_h.copy()      # the draft has written as many tokens as the target cache holds
-        inp["dq"] = torch.randn((cfg.draft_steps, B, Hq, D), generator=g, device=device).to(bf)
-        inp["dk"] = torch.randn((cfg.draft_steps, B, Hkv, D), generator=g, device=device).to(bf)
-        inp["dv"] = torch.randn((cfg.draft_steps, B, Hkv, D), generator=g, device=device).to(bf)
+        inp["dq"] = torch.randn((cfg.draft_steps, B, Hq, D), generator=g, device=device).to(dt)
+        inp["dk"] = torch.randn((cfg.draft_steps, B, Hkv, D), generator=g, device=device).to(dt)
+        inp["dv"] = torch.randn((cfg.draft_steps, B, Hkv, D), generator=g, device=device).to(dt)
         inp["dpos"] = torch.from_numpy(np.stack([kv_len_h + s for s in range(cfg.draft_steps)])).to(device)
         inp["do"] = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+    if cfg.tree_nodes:
+        N = cfg.tree_nodes
+        inp["tree"] = gen.random_tree(N, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+        tl = cfg.target_sigma * torch.randn((B, N, V), generator=g, device=device)
+        # each node's first child carries its parent's planted argmax with probability 0.6
+        tok = torch.randint(0, V, (B, N), generator=g, device=device, dtype=torch.int32)
+        first = {}
+        for i in range(1, N):
+            first.setdefault(int(inp["tree"][i]), i)
+        for p_, c_ in first.items():
+            hit = torch.rand((B,), generator=g, device=device) < 0.6
+            tl[hit, p_, tok[hit, c_].long()] = 30.0
+        depth = int(gen_depths(inp["tree"]).max())
+        inp.update(tl=tl.contiguous(), x=tok, out=torch.empty((B, depth + 1), dtype=torch.int32, device=device),
+                   nodes=torch.empty((B, depth + 1), dtype=torch.int32, device=device),
+                   nacc=torch.empty((B,), dtype=torch.int32, device=device))
+        return inp
     z = torch.randn((B, gamma + 1, V), generator=g, device=device)
     tl = cfg.target_sigma * z
     eps = torch.randn((B, gamma, V), generator=g, device=device)
@@ -197,14 +217,25 @@ def make_inputs(cfg, device, seed):
     return inp
 
 
+def gen_depths(parent):
+    d = np.zeros(len(parent), dtype=np.int64)
+    for i in range(1, len(parent)):
+        d[i] = d[int(parent[i])] + 1
+    return d
+
+
 def step_bytes(cfg, inp):
-    kv = int(inp["kv_len_h"].sum()) * cfg.Hkv * cfg.D * 2 * 2
-    qo = cfg.B * cfg.nq * cfg.Hq * cfg.D * (2 + 4)
+    kvb = 2 if cfg.kv_dtype == "bf16" else 4
+    kv = int(inp["kv_len_h"].sum()) * cfg.Hkv * cfg.D * 2 * kvb
+    qo = cfg.B * cfg.nq * cfg.Hq * cfg.D * (kvb + 4)
     win = 0
     if cfg.window:
         valid = np.minimum(inp["pos0"] + 1, cfg.window)   # tokens visible at the first draft step
-        win = int(valid.sum()) * cfg.Hkv * cfg.D * 2 * 2 + cfg.B * cfg.Hq * cfg.D * (2 + 4)
-    samp = cfg.B * (2 * cfg.gamma + 1) * cfg.vocab * 4 + cfg.B * 2 * cfg.vocab * 4
+        win = int(valid.sum()) * cfg.Hkv * cfg.D * 2 * kvb + cfg.B * cfg.Hq * cfg.D * (kvb + 4)
+    if cfg.tree_nodes:
+        samp = cfg.B * cfg.tree_nodes * cfg.vocab * 4
+    else:
+        samp = cfg.B * (2 * cfg.gamma + 1) * cfg.vocab * 4 + cfg.B * 2 * cfg.vocab * 4
     return dict(verify_kv=kv, verify_total=kv + qo, window=win, sample=samp)
 
 
@@ -215,8 +246,9 @@ class Runner:
         import torch
         self.sv, self.cfg, self.inp, self.torch = sv, cfg, inp, torch
         u8 = torch.uint8
+        self.mode = sv.SPEC_SAMPLE_TREE_GREEDY if cfg.tree_nodes else sv.SPEC_SAMPLE_CHAIN
         self.ws_v = torch.empty(sv.spec_verify_attn_workspace(inp["q"], inp["k"], inp["o"]), dtype=u8, device=device)
-        self.ws_s = torch.empty(sv.spec_sample_workspace(sv.SPEC_SAMPLE_CHAIN, inp["tl"]), dtype=u8, device=device)
+        self.ws_s = torch.empty(sv.spec_sample_workspace(self.mode, inp["tl"]), dtype=u8, device=device)
         self.ws_w = None
         if cfg.window:
             self.ws_w = torch.empty(sv.spec_draft_window_attn_workspace(inp["dq"][0], inp["k_ring"], inp["do"]),
@@ -229,12 +261,17 @@ class Runner:
 
     def verify(self):
         i = self.inp
-        self.sv.spec_verify_attn(i["q"], i["k"], i["v"], i["kv_len"], i["o"], workspace=self.ws_v)
+        self.sv.spec_verify_attn(i["q"], i["k"], i["v"], i["kv_len"], i["o"], tree_parent=i["tree"],
+                                 workspace=self.ws_v)
 
     def sample(self):
         i = self.inp
-        self.sv.spec_sample(self.sv.SPEC_SAMPLE_CHAIN, i["tl"], i["out"], i["nacc"], draft_logits=i["dl"],
-                            draft_tokens=i["x"], uniforms=i["u"], workspace=self.ws_s)
+        if self.cfg.tree_nodes:
+            self.sv.spec_sample(self.mode, i["tl"], i["out"], i["nacc"], draft_tokens=i["x"], tree_parent=i["tree"],
+                                out_path_nodes=i["nodes"], workspace=self.ws_s)
+        else:
+            self.sv.spec_sample(self.mode, i["tl"], i["out"], i["nacc"], draft_logits=i["dl"],
+                                draft_tokens=i["x"], uniforms=i["u"], workspace=self.ws_s)
 
     def launches_per_step(self):
         # our kernels: window (append, partial, merge) x draft steps, verify (partial, merge), sample (2)
@@ -256,6 +293,11 @@ def time_steps(runner, K, W, pg, device):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    # working sets that L2 (~126 MB) could hold between steps are flushed by a 512 MB write
+    nb = step_bytes(cfg, runner.inp)
+    flush = None
+    if nb["verify_total"] + nb["sample"] < 4 * L2_BYTES:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     barrier(pg, device)
     torch.cuda.synchronize()
     clocks = ClockSampler(device.index)
@@ -264,6 +306,8 @@ def time_steps(runner, K, W, pg, device):
     start.record(stream)
     for k in range(K):
         e = evs[k]
+        if flush is not None:
+            flush.fill_(k & 0xFF)
         e[0].record(stream)
         for s in range(cfg.draft_steps if cfg.window else 0):
             runner.draft(s)
@@ -278,10 +322,13 @@ def time_steps(runner, K, W, pg, device):
     barrier(pg, device)
     ck = clocks.stop()
     total_ms = start.elapsed_time(end)
+    if flush is not None:   # exclude the flushes: sum of the steps themselves
+        total_ms = float(sum(e[0].elapsed_time(e[3]) for e in evs))
     win = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     ver = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     smp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
-    return dict(total_ms=total_ms, wall_s=wall, window_ms=win, verify_ms=ver, sample_ms=smp, clocks=ck)
+    return dict(total_ms=total_ms, wall_s=wall, window_ms=win, verify_ms=ver, sample_ms=smp, clocks=ck,
+                l2_flush=flush is not None)
 
 
 def time_e2e(runner, K, W, device):
@@ -292,7 +339,7 @@ def time_e2e(runner, K, W, device):
     B, nq = cfg.B, cfg.nq
     host = {}
     for name in ("q", "tl", "dl", "x", "u", "dq", "dk", "dv"):
-        if name in inp:
+        if inp.get(name) is not None:
             host[name] = inp[name].cpu().pin_memory()
     L = inp["kv_len_h"]
     newk = inp["k"].new_empty((B, cfg.Hkv, nq, cfg.D)).cpu().pin_memory()
@@ -300,7 +347,7 @@ def time_e2e(runner, K, W, device):
     for b in range(B):
         newk[b] = inp["k"][b, :, L[b] - nq:L[b]].cpu()
         newv[b] = inp["v"][b, :, L[b] - nq:L[b]].cpu()
-    out_h = torch.empty((B, nq), dtype=torch.int32).pin_memory()
+    out_h = torch.empty(tuple(inp["out"].shape), dtype=torch.int32).pin_memory()
     nacc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + 2 * newk.numel() * newk.element_size()
     d2h = out_h.numel() * 4 + nacc_h.numel() * 4
@@ -343,6 +390,9 @@ def oracle_sample_run(cfg, seed, budget_s=12.0):
     from workloads import gen
     r = np.random.default_rng(seed)
     L = int(cfg.ctx[1])
+    parent = None
+    if cfg.tree_nodes:
+        parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
     nbytes = 0
     t_attn = 0.0
     segs = 0
@@ -351,17 +401,22 @@ def oracle_sample_run(cfg, seed, budget_s=12.0):
         k = gen.store(r.standard_normal((1, 1, L, cfg.D)).astype(np.float32), cfg.kv_dtype)
         v = gen.store(r.standard_normal((1, 1, L, cfg.D)).astype(np.float32), cfg.kv_dtype)
         t0 = time.perf_counter()
-        oa.verify_attn(q, k, v, np.array([L]))
+        oa.verify_attn(q, k, v, np.array([L]), tree_parent=parent)
         t_attn += time.perf_counter() - t0
         nbytes += L * cfg.D * 2 * cfg.kv_bytes
         segs += 1
     t_s = 0.0
     rounds = 0
     while t_s < budget_s * 0.4 and rounds < 64:
-        s = gen.chain_sample_inputs(1, cfg.gamma, cfg.vocab, int(r.integers(1 << 30)), cfg.target_sigma,
-                                    cfg.draft_noise_sigma, cfg.draft_corr)
-        t0 = time.perf_counter()
-        osm.spec_sample_chain(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"])
+        if parent is not None:
+            s = gen.tree_sample_inputs(1, parent, cfg.vocab, int(r.integers(1 << 30)))
+            t0 = time.perf_counter()
+            osm.tree_greedy(s["target_logits"], s["node_tokens"], parent)
+        else:
+            s = gen.chain_sample_inputs(1, cfg.gamma, cfg.vocab, int(r.integers(1 << 30)), cfg.target_sigma,
+                                        cfg.draft_noise_sigma, cfg.draft_corr)
+            t0 = time.perf_counter()
+            osm.spec_sample_chain(s["target_logits"], s["draft_logits"], s["draft_tokens"], s["uniforms"])
         t_s += time.perf_counter() - t0
         rounds += 1
     return dict(kv_gbs=nbytes / t_attn / 1e9, rounds_per_s=rounds / t_s, segments=segs, rounds=rounds,
@@ -452,13 +507,15 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.kv_dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.B, "q_heads": cfg.Hq, "kv_heads": cfg.Hkv,
                    "head_dim": cfg.D, "context": list(cfg.ctx), "gamma": cfg.gamma, "window": cfg.window,
                    "draft_steps": cfg.draft_steps, "vocab": cfg.vocab, "kv_dtype": cfg.kv_dtype,
                    "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2: the 8.6 GB verify cache streamed each step evicts L2; "
-                         "draft steps 2-4 of a round re-read the 67 MB ring (may be L2-resident)"},
+                   "l2": ("L2 flushed (512 MB write) before every timed step; flush time excluded" if t["l2_flush"] else
+                          f"inputs larger than L2: the {nb['verify_kv'] / 1e9:.2f} GB verify cache streamed each step "
+                          "evicts L2" + ("; draft steps 2-4 of a round re-read the ring (may be L2-resident)"
+                                         if cfg.window else ""))},
         "hbm_frac_verify": value / world / peak,
         "spec_sample_rounds_per_s": world * cfg.B / (smp_ms * 1e-3),
         "tokens_verified_per_s": world * cfg.B * cfg.nq / (ver_ms * 1e-3),

@@ -11,9 +11,9 @@
 // read from HBM once.
 //
 // bf16 K/V: TMA (cp.async.bulk.tensor, 128-byte swizzle, no multicast) fills a 3-stage ring of
-// 64-key K and V tiles guarded by mbarriers; one producer warp issues the copies, four consumer
-// warps run QK^T and PV with mma.sync m16n8k16 (fp32 accumulate) and an fp32 online softmax in
-// the log2 domain.  fp32 K/V: a plain CUDA-core kernel (one warp per query row).
+// 128-key K and V tiles guarded by mbarriers; one producer warp issues the copies, eight consumer
+// warps (row tiles x key slices of each tile) run QK^T and PV with mma.sync m16n8k16 (fp32
+// accumulate) and an fp32 online softmax in the log2 domain.  fp32 K/V: a plain CUDA-core kernel (one warp per query row).
 //
 // Masks: chain row j sees keys 0 .. len - nq + j; tree node j sees the context [0, len - nq)
 // and the tree keys whose node is on its root path (bitmask); window: every valid ring slot.
@@ -128,8 +128,9 @@ __device__ __forceinline__ bool walker_next(const AttnParams& p, Walker& w, int&
   return true;
 }
 
-__device__ __forceinline__ int slices_for_rows(int rows_here) {
-  return rows_here <= 16 ? 4 : (rows_here <= 32 ? 2 : 1);
+// key slices per row tile for row groups of `rows_per_group` rows: kConsumerWarps / 16-row tiles
+static inline int slices_for_rows(int rows_per_group) {
+  return rows_per_group <= 16 ? kConsumerWarps : (rows_per_group <= 32 ? kConsumerWarps / 2 : kConsumerWarps / 4);
 }
 
 // Visibility of key index kk (absolute in the segment) for query position j.
@@ -146,7 +147,7 @@ __device__ __forceinline__ bool key_visible(int kk, int ke, int tail_start, int 
 // ------------------------------------------------------------------ bf16 partial kernel
 
 template <int D, int MASK, int NKS>
-__device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint64_t* full, uint64_t* empty,
+__device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw, uint64_t* full, uint64_t* empty,
                               int warp, int lane, int row0, int rows_here, volatile int* s_abort) {
   constexpr int KT = kKeyTile;
   constexpr int KS = KT / NKS;     // keys of each tile this warp handles
@@ -167,29 +168,21 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint64_t* fu
   uint32_t phase = 0;
   int b, g, kb, ke, len;
   while (walker_next(p, w, b, g, kb, ke, len)) {
-    // ---- this warp's 16 query rows of (b, g) as mma.sync A fragments, straight from global
-    // (Q is tiny and L2-resident; padding rows are zero)
-    uint32_t qf[KSTEPS][4];
-    {
-      const uint32_t* q_lo = nullptr;
-      const uint32_t* q_hi = nullptr;
-      if (r_lo < rows_here) {
-        const int rr = row0 + r_lo;
-        q_lo = reinterpret_cast<const uint32_t*>(qbase + b * p.q_sb + (rr / p.G) * p.q_st + (g * p.G + rr % p.G) * p.q_sh);
+    // ---- this warp's 16 query rows of (b, g) into its own swizzled shared-memory region
+    // (padding rows are zero); A fragments are read back with ldmatrix per k-step pair
+    __syncwarp();
+    for (int idx = lane; idx < 16 * (D / 8); idx += 32) {
+      const int r = idx / (D / 8), c = idx % (D / 8);
+      const int rr = rt * 16 + r;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (rr < rows_here) {
+        const int ro = row0 + rr;
+        val = *reinterpret_cast<const uint4*>(qbase + b * p.q_sb + (ro / p.G) * p.q_st + (g * p.G + ro % p.G) * p.q_sh +
+                                              c * 8);
       }
-      if (r_hi < rows_here) {
-        const int rr = row0 + r_hi;
-        q_hi = reinterpret_cast<const uint32_t*>(qbase + b * p.q_sb + (rr / p.G) * p.q_st + (g * p.G + rr % p.G) * p.q_sh);
-      }
-      const int cw = lane & 3;  // 32-bit word (2 bf16) within each 8-element group
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        qf[kk][0] = q_lo ? __ldg(q_lo + kk * 8 + cw) : 0u;
-        qf[kk][1] = q_hi ? __ldg(q_hi + kk * 8 + cw) : 0u;
-        qf[kk][2] = q_lo ? __ldg(q_lo + kk * 8 + 4 + cw) : 0u;
-        qf[kk][3] = q_hi ? __ldg(q_hi + kk * 8 + 4 + cw) : 0u;
-      }
+      *reinterpret_cast<uint4*>(sQw + r * (D * 2) + ((c ^ (r & 7)) << 4)) = val;
     }
+    __syncwarp();
     float o[DT][4];
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
@@ -206,17 +199,26 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint64_t* fu
       const uint8_t* sV = sK + TILE;
       float s[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        const int r = ks * KS + nt * 8 + (lane & 7);
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS; kk += 2) {
-          const int d0 = kk * 16 + (lane >> 3) * 8;
-          const int c = (d0 & 63) >> 3;
+      for (int kk = 0; kk < KSTEPS; kk += 2) {
+        uint32_t qa[4], qb[4];
+        {
+          const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int c0 = kk * 2 + (lane >> 4);
+          ldmatrix_x4(smem_u32(sQw + r * (D * 2) + ((c0 ^ (r & 7)) << 4)), qa[0], qa[1], qa[2], qa[3]);
+          const int c1 = c0 + 2;
+          ldmatrix_x4(smem_u32(sQw + r * (D * 2) + ((c1 ^ (r & 7)) << 4)), qb[0], qb[1], qb[2], qb[3]);
+        }
+        const int d0 = kk * 16 + (lane >> 3) * 8;
+        const int c = (d0 & 63) >> 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int r = ks * KS + nt * 8 + (lane & 7);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(smem_u32(sK + (d0 >> 6) * (KT * 128) + r * 128 + ((c ^ (r & 7)) << 4)), b0, b1, b2, b3);
-          mma_bf16_16816(s[nt], qf[kk], b0, b1);
-          mma_bf16_16816(s[nt], qf[kk + 1], b2, b3);
+          mma_bf16_16816(s[nt], qa, b0, b1);
+          mma_bf16_16816(s[nt], qb, b2, b3);
         }
       }
       const bool tail_tile = key0 + KT > ke;
@@ -317,8 +319,8 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint64_t* fu
   }
 }
 
-template <int D, int MASK>
-__global__ void __launch_bounds__(160, 1)
+template <int D, int MASK, int NKS>
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ AttnParams p) {
   constexpr int TILE = kKeyTile * D * 2;
@@ -327,23 +329,24 @@ __global__ void __launch_bounds__(160, 1)
   __shared__ int s_abort;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* stages = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* sQ = stages + kStages * 2 * TILE;  // kConsumerWarps regions of 16 rows x D bf16
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.y * kRowsPerGroup;
-  const int rows_here = min(kRowsPerGroup, p.rows - row0);
+  const int row0 = blockIdx.y * p.rows_per_group;
+  const int rows_here = min(p.rows_per_group, p.rows - row0);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);
+      mbar_init(&empty[i], kConsumerWarps);
     }
     s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == 4) {
+  if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues every TMA copy of this CTA's walk
     Walker w;
     walker_init(p, blockIdx.x, w);
@@ -386,10 +389,7 @@ __global__ void __launch_bounds__(160, 1)
     }
     return;
   }
-  const int nks = slices_for_rows(rows_here);
-  if (nks == 1) consumer_loop<D, MASK, 1>(p, stages, full, empty, warp, lane, row0, rows_here, &s_abort);
-  else if (nks == 2) consumer_loop<D, MASK, 2>(p, stages, full, empty, warp, lane, row0, rows_here, &s_abort);
-  else consumer_loop<D, MASK, 4>(p, stages, full, empty, warp, lane, row0, rows_here, &s_abort);
+  consumer_loop<D, MASK, NKS>(p, stages, sQ + warp * (16 * D * 2), full, empty, warp, lane, row0, rows_here, &s_abort);
 }
 
 // ------------------------------------------------------------------ fp32 partial kernel
@@ -397,8 +397,8 @@ template <int D, int MASK>
 __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.y * kRowsPerGroup;
-  const int rows_here = min(kRowsPerGroup, p.rows - row0);
+  const int row0 = blockIdx.y * p.rows_per_group;
+  const int rows_here = min(p.rows_per_group, p.rows - row0);
   const float* qb = reinterpret_cast<const float*>(p.q);
   const float* kb_ = reinterpret_cast<const float*>(p.k);
   const float* vb_ = reinterpret_cast<const float*>(p.v);
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
 // ------------------------------------------------------------------ merge kernel
 // grid (segments, ceil(rows / 4)); one warp per query row of a segment.
 template <int D>
-__global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p, int fp32_path) {
+__global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -463,8 +463,7 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
     const int64_t per = keys_per_cta(p, total);
     const int64_t start = cum_b + (int64_t)g * len;
     const int c0 = (int)(start / per), c1 = (int)((start + len - 1) / per);
-    const int rg_rows = min(kRowsPerGroup, p.rows - (r / kRowsPerGroup) * kRowsPerGroup);
-    const int nks = fp32_path ? 1 : slices_for_rows(rg_rows);
+    const int nks = p.nks;
     float M = neg_inf();
     for (int c = c0; c <= c1; ++c)
       for (int ks = 0; ks < nks; ++ks) M = fmaxf(M, p.part_ml[((int64_t)(s + c) * kMaxSlices + ks) * p.rows + r].x);
@@ -545,15 +544,25 @@ void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p
   (void)D;
 }
 
-template <int D, int MASK>
+template <int D, int MASK, int NKS>
 static cudaError_t launch_bf16(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, dim3 grid,
                                cudaStream_t stream) {
-  const size_t smem = 1024 + kStages * 2 * (size_t)(kKeyTile * D * 2);
-  auto kern = attn_partial_bf16<D, MASK>;
+  const size_t smem = 1024 + kStages * 2 * (size_t)(kKeyTile * D * 2) + (size_t)kConsumerWarps * 16 * D * 2;
+  auto kern = attn_partial_bf16<D, MASK, NKS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 160, smem, stream>>>(*tmK, *tmV, p);
+  kern<<<grid, (kConsumerWarps + 1) * 32, smem, stream>>>(*tmK, *tmV, p);
   return cudaGetLastError();
+}
+
+template <int D, int MASK>
+static cudaError_t launch_bf16_nks(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, dim3 grid,
+                                   cudaStream_t stream) {
+  switch (p.nks) {
+    case kConsumerWarps / 4: return launch_bf16<D, MASK, kConsumerWarps / 4>(p, tmK, tmV, grid, stream);
+    case kConsumerWarps / 2: return launch_bf16<D, MASK, kConsumerWarps / 2>(p, tmK, tmV, grid, stream);
+    default: return launch_bf16<D, MASK, kConsumerWarps>(p, tmK, tmV, grid, stream);
+  }
 }
 
 template <int D, int MASK>
@@ -567,9 +576,9 @@ static cudaError_t launch_partial(const AttnParams& p, const CUtensorMap* tmK, c
                                   dim3 grid, cudaStream_t stream) {
   if (kv_bf16) {
     switch (p.mask) {
-      case kMaskNone: return launch_bf16<D, kMaskNone>(p, tmK, tmV, grid, stream);
-      case kMaskChain: return launch_bf16<D, kMaskChain>(p, tmK, tmV, grid, stream);
-      default: return launch_bf16<D, kMaskTree>(p, tmK, tmV, grid, stream);
+      case kMaskNone: return launch_bf16_nks<D, kMaskNone>(p, tmK, tmV, grid, stream);
+      case kMaskChain: return launch_bf16_nks<D, kMaskChain>(p, tmK, tmV, grid, stream);
+      default: return launch_bf16_nks<D, kMaskTree>(p, tmK, tmV, grid, stream);
     }
   }
   switch (p.mask) {
@@ -587,19 +596,22 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // bf16: one 160-thread CTA per SM (3-stage ring, up to ~113 KB shared); fp32: 4 per SM.
-  const int per_sm = kv_bf16 ? 1 : 4;
+  // bf16: one 288-thread CTA per SM (a 3-stage ring of 64 KB K+V stages); fp32: 2 per SM.
+  const int per_sm = kv_bf16 ? 1 : 2;
   p.grid_x = sms * per_sm < kMaxGridX ? sms * per_sm : kMaxGridX;
   e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
+  // row groups of equal size (a multiple of 16), so one key-slice count serves the launch
   const int row_groups = (p.rows + kRowsPerGroup - 1) / kRowsPerGroup;
+  p.rows_per_group = ((p.rows + row_groups - 1) / row_groups + 15) / 16 * 16;
+  p.nks = kv_bf16 ? slices_for_rows(p.rows_per_group) : 1;
   dim3 grid(p.grid_x, row_groups);
   e = (p.D == 64) ? launch_partial<64>(p, tmK, tmV, kv_bf16, grid, stream)
                   : launch_partial<128>(p, tmK, tmV, kv_bf16, grid, stream);
   if (e != cudaSuccess) return e;
   dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
-  if (p.D == 64) attn_merge<64><<<mgrid, 128, 0, stream>>>(p, kv_bf16 ? 0 : 1);
-  else attn_merge<128><<<mgrid, 128, 0, stream>>>(p, kv_bf16 ? 0 : 1);
+  if (p.D == 64) attn_merge<64><<<mgrid, 128, 0, stream>>>(p);
+  else attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -8,17 +8,20 @@
 
 namespace specv {
 
-// Keys per TMA stage and pipeline depth of the bf16 split-KV kernel.
-constexpr int kKeyTile = 64;
+// Keys per TMA stage and pipeline depth of the bf16 split-KV kernel (3 x 64 KB for D = 128).
+constexpr int kKeyTile = 128;
 constexpr int kStages = 3;
-// Query rows one CTA row-group holds (4 warps x 16 rows of mma.sync tiles).
+// Consumer warps per CTA (two per SM sub-partition) plus one TMA producer warp.
+constexpr int kConsumerWarps = 8;
+// Query rows one CTA row-group holds (up to 4 row tiles of 16 for mma.sync).
 constexpr int kRowsPerGroup = 64;
-// Upper bound on CTAs along the key axis; the workspace is sized for it.
-constexpr int kMaxGridX = 1024;
+// Upper bound on CTAs along the key axis (two per SM on a 160-SM part); the workspace is sized
+// for it and launches never exceed it.
+constexpr int kMaxGridX = 320;
 // Minimum keys a CTA takes, so that short total work does not spread over every SM.
 constexpr int kMinKeysPerCta = 256;
-// Key-slice count per row tile is at most 4 (one warp per slice).
-constexpr int kMaxSlices = 4;
+// Key slices per row tile: consumer warps / row tiles, at most 8.
+constexpr int kMaxSlices = 8;
 
 enum MaskMode : int { kMaskNone = 0, kMaskChain = 1, kMaskTree = 2 };
 
@@ -39,6 +42,8 @@ struct AttnParams {
   int64_t o_sb, o_st, o_sh;
   int o_bf16;
   int grid_x;                      // CTAs along the key axis (same value in partial and merge)
+  int rows_per_group;              // query rows per CTA row group (blockIdx.y), <= kRowsPerGroup
+  int nks;                         // key slices per row tile (bf16 path), same for every row group
   float* part_o;                   // [slots][kMaxSlices][rows][D]
   float2* part_ml;                 // [slots][kMaxSlices][rows]  (m in log2 units, l)
   uint32_t* status;

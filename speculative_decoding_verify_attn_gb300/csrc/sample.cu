@@ -3,11 +3,12 @@
 // Large vocabularies (V > kSmallVocab), stochastic chain:
 //   K1 sample_stats     grid (chunks, rows, B): every target and draft row is split into
 //                       vocabulary chunks; each CTA reads its chunk once with 128-bit loads and
-//                       writes the chunk max M_c and S_c = sum exp(x - M_c) (fp32 exponentials,
-//                       compensated fp32 per thread, fp64 across threads).
+//                       writes the chunk max M_c and S_c = sum exp(x - M_c) (fp32 exp2f of the
+//                       scaled difference, compensated fp32 per thread, fp64 across threads).
 //   K2 sample_residual  grid (chunks, B): every CTA of a sequence merges the row statistics
 //                       (Z = sum_c S_c exp(M_c - M), fp64), takes the accept decisions for all
-//                       gamma drafts (fp64 exponentials of the two selected logits), and sums the
+//                       gamma drafts at once (one lane per draft, fp64 exponentials of the two
+//                       selected logits), and sums the
 //                       residual max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its chunk.  The last
 //                       CTA of the sequence to finish (atomic ticket, no spinning) finds the chunk
 //                       where the cumulative residual passes u * R, re-scans that one chunk and
@@ -40,11 +41,17 @@ struct Kahan {
   __device__ __forceinline__ double value() const { return (double)s - (double)c; }
 };
 
+// exp(x - M) in fp32 through exp2f (2 ulp); x - M <= 0 is formed first so that the dominant
+// terms (x near M) carry only the rounding of the final product
+__device__ __forceinline__ float exp_shift(float x, float M) {
+  return exp2f(__fmul_rn(__fsub_rn(x, M), kLog2e));
+}
+
 // residual element: max(P(z) - Q(z), 0), or P(z) when there is no draft row
 __device__ __forceinline__ float resid(float t, float d, float Mt, float iZt, float Md, float iZd, bool has_d) {
-  const float pt = __fmul_rn(expf(__fsub_rn(t, Mt)), iZt);
+  const float pt = __fmul_rn(exp_shift(t, Mt), iZt);
   if (!has_d) return pt;
-  const float qd = __fmul_rn(expf(__fsub_rn(d, Md)), iZd);
+  const float qd = __fmul_rn(exp_shift(d, Md), iZd);
   return fmaxf(__fsub_rn(pt, qd), 0.f);
 }
 
@@ -120,21 +127,26 @@ __device__ __forceinline__ const float* drow(const SampleParams& p, int b, int i
   return p.dl + (int64_t)b * p.dl_sb + (int64_t)i * p.V;
 }
 
-// k = number of leading drafts passing u_i * Q_i(x_i) < P_i(x_i); -1 if a token id is invalid.
+// k = number of leading drafts passing u_i * Q_i(x_i) < P_i(x_i), or -1 if a token id is invalid.
 // sM / sZ hold the row max and normaliser: target row i at i, draft row i at rows_t + i.
-__device__ int chain_decide(const SampleParams& p, int b, const float* sM, const double* sZ) {
-  for (int i = 0; i < p.gamma; ++i) {
+// Whole warp: lane i takes draft i (gamma <= 32); the first failing lane is found with a ballot.
+// P_i(x_i) and Q_i(x_i) use fp64 exponentials of the two selected logits.  Every lane returns k.
+__device__ int chain_decide_warp(const SampleParams& p, int b, const float* sM, const double* sZ) {
+  const int i = threadIdx.x & 31;
+  bool bad = false, acc = true;
+  if (i < p.gamma) {
     const int x = p.tok[(int64_t)b * p.tok_sb + i];
-    if (x < 0 || x >= p.V) return -1;
+    bad = x < 0 || x >= p.V;
+    if (!bad) {
+      const double pt = exp((double)trow(p, b, i)[x] - (double)sM[i]) / sZ[i];
+      const double qd = exp((double)drow(p, b, i)[x] - (double)sM[p.rows_t + i]) / sZ[p.rows_t + i];
+      const double uu = (double)p.u[(int64_t)b * p.u_sb + i];
+      acc = uu * qd < pt;
+    }
   }
-  for (int i = 0; i < p.gamma; ++i) {
-    const int x = p.tok[(int64_t)b * p.tok_sb + i];
-    const double pt = exp((double)trow(p, b, i)[x] - (double)sM[i]) / sZ[i];
-    const double qd = exp((double)drow(p, b, i)[x] - (double)sM[p.rows_t + i]) / sZ[p.rows_t + i];
-    const double uu = (double)p.u[(int64_t)b * p.u_sb + i];
-    if (!(uu * qd < pt)) return i;
-  }
-  return p.gamma;
+  if (__any_sync(0xffffffffu, bad)) return -1;
+  const unsigned rej = __ballot_sync(0xffffffffu, i < p.gamma && !acc);
+  return rej ? __ffs(rej) - 1 : p.gamma;
 }
 
 __device__ void write_chain_out(const SampleParams& p, int b, int k, int y) {
@@ -213,7 +225,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_cons
     const float M = block_max(m, redf);
     Kahan k;
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) k.add(expf(__fsub_rn(x[e], M)));
+    for (int e = 0; e < EPT; ++e) k.add(exp_shift(x[e], M));
     const double S = block_sum_d(k.value(), redd);
     if (tid == 0) {
       p.st_m[o] = M;
@@ -295,8 +307,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_residual(const __grid_c
     if (lane == 0) { sM[r] = m; sZ[r] = z; }
   }
   __syncthreads();
-  // 2. accept decisions
-  if (tid == 0) s_k = chain_decide(p, b, sM, sZ);
+  // 2. accept decisions (one warp, one lane per draft)
+  if (warp == 0) {
+    const int kk = chain_decide_warp(p, b, sM, sZ);
+    if (lane == 0) s_k = kk;
+  }
   __syncthreads();
   const int k = s_k;
   if (k < 0) {
@@ -488,7 +503,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_small(const __grid_cons
       for (int e = e0; e < e1; ++e) m = fmaxf(m, row[e]);
       m = warp_max(m);
       Kahan ks;
-      for (int e = e0; e < e1; ++e) ks.add(expf(__fsub_rn(row[e], m)));
+      for (int e = e0; e < e1; ++e) ks.add(exp_shift(row[e], m));
       const double z = warp_sum_d(ks.value());
       if (lane == 0) { sM[r] = m; sZ[r] = z; }
     }
@@ -511,9 +526,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_small(const __grid_cons
     write_chain_out(p, b, k, k >= 0 ? a[k] : -1);
     return;
   }
-  int k = 0;
-  if (lane == 0) k = chain_decide(p, b, sM, sZ);
-  k = __shfl_sync(0xffffffffu, k, 0);
+  const int k = chain_decide_warp(p, b, sM, sZ);
   if (k < 0) {
     if (lane == 0) write_chain_out(p, b, -1, -1);
     return;
