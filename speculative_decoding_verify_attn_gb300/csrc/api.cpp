@@ -111,7 +111,7 @@ int check_kv_layout(const void* k, const void* v, int kv_dtype, int64_t sb, int6
 
 int check_q_layout(const void* q, int dtype, int64_t s0, int64_t s1, int64_t s2) {
   if (!q || s0 < 0 || s1 < 0 || s2 < 0) return SPEC_ERR_INVALID_ARG;
-  if (dtype == SPEC_BF16 && (!aligned(q, 4) || (s0 % 2) || (s1 % 2) || (s2 % 2))) return SPEC_ERR_INVALID_ARG;
+  if (dtype == SPEC_BF16 && (!aligned(q, 16) || (s0 % 8) || (s1 % 8) || (s2 % 8))) return SPEC_ERR_INVALID_ARG;
   if (dtype == SPEC_F32 && !aligned(q, 4)) return SPEC_ERR_INVALID_ARG;
   return SPEC_OK;
 }

@@ -23,125 +23,15 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "attn_common.cuh"
 #include "attn_internal.h"
 #include "common.cuh"
 
 namespace specv {
 
-// ------------------------------------------------------------------ segment bookkeeping
-__device__ __forceinline__ int seg_len(const AttnParams& p, int b) {
-  int L = __ldg(p.lens + b);
-  if (p.is_window) return L >= 1 ? min(L, p.Lmax) : 0;
-  return (L >= p.nq && L <= p.Lmax) ? L : 0;
-}
-
-// Whole-warp: total keys over all segments, and the exclusive prefix (in keys) of sequence
-// `b_query` (pass -1 to skip).
-__device__ void warp_scan_lengths(const AttnParams& p, int b_query, int64_t& total, int64_t& cum_at) {
-  const int lane = threadIdx.x & 31;
-  int64_t run = 0;
-  cum_at = 0;
-  for (int b0 = 0; b0 < p.B; b0 += 32) {
-    const int b = b0 + lane;
-    const int64_t len = (b < p.B) ? (int64_t)seg_len(p, b) * p.Hkv : 0;
-    int64_t x = len;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    const int64_t excl = run + x - len;
-    if (b_query >= b0 && b_query < b0 + 32) cum_at = __shfl_sync(0xffffffffu, excl, b_query - b0);
-    run += __shfl_sync(0xffffffffu, x, 31);
-  }
-  total = run;
-}
-
-__device__ __forceinline__ int64_t keys_per_cta(const AttnParams& p, int64_t total) {
-  int64_t per = (total + p.grid_x - 1) / p.grid_x;
-  return per < kMinKeysPerCta ? (int64_t)kMinKeysPerCta : per;
-}
-
-// Walks the parts of a CTA's global key range.  Every lane of a warp holds the same state.
-struct Walker {
-  int b, g, len, key;
-  int64_t gpos, gend;
-};
-
-// Whole-warp: position the walker at the start of CTA `cta`'s range.
-__device__ void walker_init(const AttnParams& p, int cta, Walker& w) {
-  int64_t total, dummy;
-  warp_scan_lengths(p, -1, total, dummy);
-  const int64_t per = keys_per_cta(p, total);
-  const int64_t begin = min(total, (int64_t)cta * per);
-  w.gpos = begin;
-  w.gend = min(total, begin + per);
-  w.b = 0; w.g = 0; w.len = 0; w.key = 0;
-  if (w.gpos >= w.gend) return;
-  // find the sequence whose key block contains `begin`
-  const int lane = threadIdx.x & 31;
-  int64_t run = 0;
-  int found_b = -1;
-  int64_t found_cum = 0;
-  for (int b0 = 0; b0 < p.B && found_b < 0; b0 += 32) {
-    const int b = b0 + lane;
-    const int64_t len = (b < p.B) ? (int64_t)seg_len(p, b) * p.Hkv : 0;
-    int64_t x = len;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    const int64_t excl = run + x - len;
-    const bool hit = len > 0 && begin >= excl && begin < excl + len;
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    if (m) {
-      const int src = __ffs(m) - 1;
-      found_b = b0 + src;
-      found_cum = __shfl_sync(0xffffffffu, excl, src);
-    }
-    run += __shfl_sync(0xffffffffu, x, 31);
-  }
-  w.b = found_b;
-  w.len = seg_len(p, found_b);
-  const int64_t rel = begin - found_cum;
-  w.g = (int)(rel / w.len);
-  w.key = (int)(rel % w.len);
-}
-
-__device__ __forceinline__ bool walker_next(const AttnParams& p, Walker& w, int& b, int& g, int& kb, int& ke,
-                                            int& len) {
-  if (w.gpos >= w.gend) return false;
-  const int64_t avail = w.gend - w.gpos;
-  const int take = (int)min((int64_t)(w.len - w.key), avail);
-  b = w.b; g = w.g; kb = w.key; ke = w.key + take; len = w.len;
-  w.gpos += take;
-  w.key += take;
-  if (w.key == w.len) {
-    w.key = 0;
-    if (++w.g == p.Hkv) {
-      w.g = 0;
-      do { ++w.b; } while (w.b < p.B && seg_len(p, w.b) == 0);
-      w.len = (w.b < p.B) ? seg_len(p, w.b) : 0;
-    }
-  }
-  return true;
-}
-
 // key slices per row tile for row groups of `rows_per_group` rows: kConsumerWarps / 16-row tiles
 static inline int slices_for_rows(int rows_per_group) {
   return rows_per_group <= 16 ? kConsumerWarps : (rows_per_group <= 32 ? kConsumerWarps / 2 : kConsumerWarps / 4);
-}
-
-// Visibility of key index kk (absolute in the segment) for query position j.
-template <int MASK>
-__device__ __forceinline__ bool key_visible(int kk, int ke, int tail_start, int j, unsigned long long anc) {
-  bool vis = kk < ke;
-  if (MASK != kMaskNone && kk >= tail_start) {
-    const int m = kk - tail_start;
-    vis = vis && (MASK == kMaskChain ? (m <= j) : (((anc >> m) & 1ull) != 0ull));
-  }
-  return vis;
 }
 
 // ------------------------------------------------------------------ bf16 partial kernel
@@ -601,6 +491,19 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   p.grid_x = sms * per_sm < kMaxGridX ? sms * per_sm : kMaxGridX;
   e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
+  dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
+  if (kv_bf16 && p.D == 128 && p.rows > 32) {
+    // dense query blocks: tcgen05 tiles of 128 rows, one CTA per SM (range x row group)
+    p.tc_groups = (p.rows + 127) / 128;
+    p.rows_per_group = (p.rows + p.tc_groups - 1) / p.tc_groups;
+    p.nks = 1;
+    p.grid_x = sms / p.tc_groups > 0 ? sms / p.tc_groups : 1;
+    if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
+    e = launch_partial_tc(p, tmK, tmV, stream);
+    if (e != cudaSuccess) return e;
+    attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   // row groups of equal size (a multiple of 16), so one key-slice count serves the launch
   const int row_groups = (p.rows + kRowsPerGroup - 1) / kRowsPerGroup;
   p.rows_per_group = ((p.rows + row_groups - 1) / row_groups + 15) / 16 * 16;
@@ -609,7 +512,6 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   e = (p.D == 64) ? launch_partial<64>(p, tmK, tmV, kv_bf16, grid, stream)
                   : launch_partial<128>(p, tmK, tmV, kv_bf16, grid, stream);
   if (e != cudaSuccess) return e;
-  dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
   if (p.D == 64) attn_merge<64><<<mgrid, 128, 0, stream>>>(p);
   else attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
   return cudaGetLastError();

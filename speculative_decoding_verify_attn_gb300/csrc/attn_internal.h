@@ -44,6 +44,7 @@ struct AttnParams {
   int grid_x;                      // CTAs along the key axis (same value in partial and merge)
   int rows_per_group;              // query rows per CTA row group (blockIdx.y), <= kRowsPerGroup
   int nks;                         // key slices per row tile (bf16 path), same for every row group
+  int tc_groups;                   // tensor-core path: row groups per key range (CTA = range x group)
   float* part_o;                   // [slots][kMaxSlices][rows][D]
   float2* part_ml;                 // [slots][kMaxSlices][rows]  (m in log2 units, l)
   uint32_t* status;
@@ -69,5 +70,10 @@ void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
                              cudaStream_t stream);
 cudaError_t launch_window_append(const WindowAppend& a, cudaStream_t stream);
+
+// tcgen05 partial kernel (attn_tc.cu): D = 128, bf16, up to 128 query rows per row group.
+cudaError_t launch_partial_tc(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                              cudaStream_t stream);
+size_t attn_tc_smem_bytes();
 
 }  // namespace specv

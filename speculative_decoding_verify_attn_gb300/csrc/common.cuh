@@ -22,6 +22,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// 2^x with the hardware approximation instruction (PTX ex2.approx.ftz.f32; relative error about
+// 2^-22, subnormal results flushed to zero).  Used where the result is rounded to bf16 anyway.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
