@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling a small case)")
+    ap.add_argument("--no-graphs", action="store_true", help="issue every call eagerly instead of graph replays")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -278,16 +279,58 @@ class Runner:
         return (3 * self.cfg.draft_steps if self.cfg.window else 0) + 2 + 2
 
 
-def time_steps(runner, K, W, pg, device):
+class GraphOps:
+    """Each op of a step (the draft-window calls, verify, sample) captured once into a CUDA graph
+    through the public binding and replayed, so that host launch overhead stays out of the device
+    timings.  Per-op CUDA events are recorded between replays, outside the graphs."""
+
+    def __init__(self, runner, stream):
+        import torch
+        self.g = {}
+        cfg = runner.cfg
+        ops = {"verify": runner.verify, "sample": runner.sample}
+        if cfg.window:
+            ops["draft"] = lambda: [runner.draft(s) for s in range(cfg.draft_steps)]
+        with torch.cuda.stream(stream):
+            for name, fn in ops.items():
+                fn()                       # eager first call (module load, attributes)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                    fn()
+                self.g[name] = g
+        torch.cuda.synchronize()
+
+    def draft(self):
+        if "draft" in self.g:
+            self.g["draft"].replay()
+
+    def verify(self):
+        self.g["verify"].replay()
+
+    def sample(self):
+        self.g["sample"].replay()
+
+
+def time_steps(runner, K, W, pg, device, use_graphs=True):
     """K timed steps bracketed by barrier + synchronize; per-op CUDA events on the launching stream."""
     import torch
     cfg = runner.cfg
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=device) if use_graphs else torch.cuda.current_stream()
+    if use_graphs:
+        gops = GraphOps(runner, stream)
+        do_draft, do_verify, do_sample = gops.draft, gops.verify, gops.sample
+    else:
+        def do_draft():
+            for s in range(cfg.draft_steps if cfg.window else 0):
+                runner.draft(s)
+        do_verify, do_sample = runner.verify, runner.sample
+    ctx = torch.cuda.stream(stream)
+    ctx.__enter__()
     for _ in range(W):
-        for s in range(cfg.draft_steps if cfg.window else 0):
-            runner.draft(s)
-        runner.verify()
-        runner.sample()
+        do_draft()
+        do_verify()
+        do_sample()
     torch.cuda.synchronize()
     n_ev = 4
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
@@ -309,16 +352,16 @@ def time_steps(runner, K, W, pg, device):
         if flush is not None:
             flush.fill_(k & 0xFF)
         e[0].record(stream)
-        for s in range(cfg.draft_steps if cfg.window else 0):
-            runner.draft(s)
+        do_draft()
         e[1].record(stream)
-        runner.verify()
+        do_verify()
         e[2].record(stream)
-        runner.sample()
+        do_sample()
         e[3].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
+    ctx.__exit__(None, None, None)
     barrier(pg, device)
     ck = clocks.stop()
     total_ms = start.elapsed_time(end)
@@ -328,7 +371,7 @@ def time_steps(runner, K, W, pg, device):
     ver = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     smp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     return dict(total_ms=total_ms, wall_s=wall, window_ms=win, verify_ms=ver, sample_ms=smp, clocks=ck,
-                l2_flush=flush is not None)
+                l2_flush=flush is not None, graphs=use_graphs)
 
 
 def time_e2e(runner, K, W, device):
@@ -482,7 +525,7 @@ def main():
     inp = make_inputs(cfg, device, seed=cfg.seed + 7919 * rank)
     runner = Runner(sv, cfg, inp, device)
     nb = step_bytes(cfg, inp)
-    t = time_steps(runner, args.steps, args.warmup, pg, device)
+    t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs)
     total_ms = max_over_ranks(pg, t["total_ms"], device)
     ver_ms = max_over_ranks(pg, t["verify_ms"], device)
     smp_ms = max_over_ranks(pg, t["sample_ms"], device)
@@ -512,6 +555,8 @@ def main():
                    "head_dim": cfg.D, "context": list(cfg.ctx), "gamma": cfg.gamma, "window": cfg.window,
                    "draft_steps": cfg.draft_steps, "vocab": cfg.vocab, "kv_dtype": cfg.kv_dtype,
                    "parallelism": f"replicas x{world}",
+                   "launch": "one CUDA graph per op (captured through the binding), replayed" if t["graphs"]
+                             else "eager calls through the binding",
                    "l2": ("L2 flushed (512 MB write) before every timed step; flush time excluded" if t["l2_flush"] else
                           f"inputs larger than L2: the {nb['verify_kv'] / 1e9:.2f} GB verify cache streamed each step "
                           "evicts L2" + ("; draft steps 2-4 of a round re-read the ring (may be L2-resident)"

@@ -1,25 +1,25 @@
 // The speculative-sampling step over the vocabulary, and greedy chain / tree selection.
 //
-// Large vocabularies (V > kSmallVocab), stochastic chain:
+// Large vocabularies (V > kSmallVocab):
 //   K1 sample_stats     grid (chunks, rows, B): every target and draft row is split into
 //                       vocabulary chunks; each CTA reads its chunk once with 128-bit loads and
 //                       writes the chunk max M_c and S_c = sum exp(x - M_c) (fp32 exp2f of the
-//                       scaled difference, compensated fp32 per thread, fp64 across threads).
-//   K2 sample_residual  grid (chunks, B): every CTA of a sequence merges the row statistics
-//                       (Z = sum_c S_c exp(M_c - M), fp64), takes the accept decisions for all
-//                       gamma drafts at once (one lane per draft, fp64 exponentials of the two
-//                       selected logits), and sums the
-//                       residual max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its chunk.  The last
-//                       CTA of the sequence to finish (atomic ticket, no spinning) finds the chunk
-//                       where the cumulative residual passes u * R, re-scans that one chunk and
-//                       writes the emitted tokens.
-// Greedy modes: K1 computes chunk argmaxes (ties to the smallest id), K2 merges them per row and
-// applies the chain or tree acceptance rule.
+//                       scaled difference, compensated fp32 per thread, float-float across the
+//                       warp, fp64 across warps) -- or, in greedy modes, the chunk argmax.  The last
+//                       CTA of a sequence to finish (atomic ticket, no spinning) merges its rows'
+//                       statistics (fp64) and takes every accept decision at once (one lane per
+//                       draft, fp64 exponentials of the two selected logits); greedy modes finish
+//                       there (argmax merge + chain or tree rule).
+//   K2 sample_residual  grid (chunks, B), stochastic chain only: each CTA sums the residual
+//                       max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its chunk; the last CTA of
+//                       the sequence finds the chunk where the cumulative residual passes u * R,
+//                       re-scans that one chunk and writes the emitted tokens.
 // Small vocabularies: one warp per sequence runs the whole step (the 16-token chi-square
 // workload runs 10^6 sequences at once).
 //
-// Every sum that decides a token is reproducible: per-thread compensated fp32 sums in a fixed
-// element order, fp64 above that, no floating-point atomics.
+// Every sum that decides a token is reproducible: fixed element orders, compensated fp32 per
+// thread (Kahan), float-float (Knuth's TwoSum) inside a warp, fp64 above that, no floating-point
+// atomics.
 #include <cuda_runtime.h>
 #include <limits.h>
 
@@ -27,8 +27,6 @@
 #include "sample_internal.h"
 
 namespace specv {
-
-constexpr int kMaxChunks = 512;
 
 struct Kahan {
   float s = 0.f, c = 0.f;
@@ -98,25 +96,38 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     argmax_combine(v, i, v2, i2);
   }
 }
-// exclusive prefix (fp64) over the block's threads in thread order; also returns the total
-__device__ double block_exclusive_scan_d(double v, double* red, double& total) {
+// Float-float (unevaluated sum hi + lo) addition: Knuth's TwoSum on the high parts, then the low
+// parts folded in and renormalised.  About 44 significant bits with fp32 operations only, so warp
+// reductions avoid the fp64 pipe.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float v = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, v)), __fsub_rn(b.hi, v));
+  const float t = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s, t);
+  return FF{hi, __fsub_rn(t, __fsub_rn(hi, s))};
+}
+// Block sum of per-thread float-float values: warps reduce in float-float, then thread 0 adds the
+// warp results in fp64 in warp order.  The result is valid in thread 0.
+__device__ double block_sum_ff(FF v, FF* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double x = v;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+  for (int o = 16; o > 0; o >>= 1) {
+    FF w;
+    w.hi = __shfl_down_sync(0xffffffffu, v.hi, o);
+    w.lo = __shfl_down_sync(0xffffffffu, v.lo, o);
+    if (lane < o) v = ff_add(v, w);
   }
   __syncthreads();
-  if (lane == 31) red[warp] = x;
+  if (lane == 0) red[warp] = v;
   __syncthreads();
-  double before = 0.0, tot = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) before += red[w];
-    tot += red[w];
-  }
-  total = tot;
-  return before + x - v;
+  double t = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += (double)red[w].hi + (double)red[w].lo;
+  return t;
 }
 
 // ------------------------------------------------------------------ shared decision logic
@@ -138,10 +149,13 @@ __device__ int chain_decide_warp(const SampleParams& p, int b, const float* sM, 
     const int x = p.tok[(int64_t)b * p.tok_sb + i];
     bad = x < 0 || x >= p.V;
     if (!bad) {
-      const double pt = exp((double)trow(p, b, i)[x] - (double)sM[i]) / sZ[i];
-      const double qd = exp((double)drow(p, b, i)[x] - (double)sM[p.rows_t + i]) / sZ[p.rows_t + i];
+      // u Q(x) < P(x)  <=>  u < P(x) / Q(x) = exp((t_x - M_t) - (d_x - M_d)) * Z_d / Z_t
+      // (the differences are exact in fp64; one fp64 exponential per draft)
+      const double dt = (double)trow(p, b, i)[x] - (double)sM[i];
+      const double dd = (double)drow(p, b, i)[x] - (double)sM[p.rows_t + i];
+      const double ratio = exp(dt - dd) * (sZ[p.rows_t + i] / sZ[i]);
       const double uu = (double)p.u[(int64_t)b * p.u_sb + i];
-      acc = uu * qd < pt;
+      acc = uu < ratio;
     }
   }
   if (__any_sync(0xffffffffu, bad)) return -1;
@@ -200,277 +214,347 @@ __device__ void tree_select_write(const SampleParams& p, int b, const int* a) {
 }
 
 // ------------------------------------------------------------------ large-V kernels
-template <int EPT, bool GREEDY>
+constexpr int kWarps = kSampleThreads / 32;
+
+// Statistics kernel, warp-granular and persistent: global warp w takes the items w, w + W, ...
+// (W warps in the grid), an item being kStatChunk = 1024 logits of one row, (b, row, item) in
+// row-major order.  Lane l reads elements 4l..4l+3 of each 128-element slab (coalesced 512-byte
+// warp loads).  Reductions are warp shuffles only -- no block barriers -- and the next item's
+// loads are in flight while the current one is reduced.  Per item: the max and the compensated
+// sum of exp(x - max) (float-float across lanes), or the argmax in greedy modes.
+template <bool GREEDY>
 __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_constant__ SampleParams p) {
-  __shared__ float redf[32];
-  __shared__ double redd[32];
-  __shared__ int redi[32];
-  const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  constexpr int PER = kStatChunk / 128;  // float4 loads per lane per item
+  const int lane = threadIdx.x & 31;
   const int rows = p.rows_t + p.rows_d;
-  const float* row = (r < p.rows_t) ? trow(p, b, r) : drow(p, b, r - p.rows_t);
-  const int base = c * p.chunk;
-  float x[EPT];
+  const int per_seq = rows * p.schunks;
+  const int items = p.B * per_seq;
+  const int W = gridDim.x * kWarps;
+  auto src_of = [&](int it, int& base) -> const float* {
+    const int b = it / per_seq;
+    const int rem = it - b * per_seq;
+    const int r = rem / p.schunks;
+    base = (rem - r * p.schunks) * kStatChunk;
+    return (r < p.rows_t) ? trow(p, b, r) : drow(p, b, r - p.rows_t);
+  };
+  auto load = [&](int it, float4 (&v)[PER]) {
+    int base;
+    const float* row = src_of(it, base);
 #pragma unroll
-  for (int i = 0; i < EPT / 4; ++i) {
-    const int idx = base + (i * kSampleThreads + tid) * 4;
-    float4 v = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
-    if (idx < p.V) v = __ldcs(reinterpret_cast<const float4*>(row + idx));
-    x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-  }
-  const int64_t o = ((int64_t)b * rows + r) * p.nchunks + c;
-  if (!GREEDY) {
-    float m = neg_inf();
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) m = fmaxf(m, x[e]);
-    const float M = block_max(m, redf);
-    Kahan k;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) k.add(exp_shift(x[e], M));
-    const double S = block_sum_d(k.value(), redd);
-    if (tid == 0) {
-      p.st_m[o] = M;
-      p.st_s[o] = S;
+    for (int i = 0; i < PER; ++i) {
+      const int idx = base + i * 128 + lane * 4;
+      v[i] = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
+      if (idx < p.V) v[i] = __ldcs(reinterpret_cast<const float4*>(row + idx));
     }
-  } else {
-    float bv = neg_inf();
-    int bi = INT_MAX;
+  };
+  int it = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (it >= items) return;
+  float4 x[PER], xn[PER];
+  load(it, x);
+  for (; it < items; it += W) {
+    if (it + W < items) load(it + W, xn);
+    if (!GREEDY) {
+      float m = neg_inf();
 #pragma unroll
-    for (int i = 0; i < EPT / 4; ++i)
+      for (int i = 0; i < PER; ++i) m = fmaxf(m, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
+      m = warp_max(m);
+      Kahan k;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int idx = base + (i * kSampleThreads + tid) * 4 + j;
-        if (idx < p.V && x[4 * i + j] > bv) { bv = x[4 * i + j]; bi = idx; }
+      for (int i = 0; i < PER; ++i) {
+        k.add(exp_shift(x[i].x, m)); k.add(exp_shift(x[i].y, m));
+        k.add(exp_shift(x[i].z, m)); k.add(exp_shift(x[i].w, m));
       }
-    warp_argmax(bv, bi);
-    const int lane = tid & 31, warp = tid >> 5;
-    __syncthreads();
-    if (lane == 0) { redf[warp] = bv; redi[warp] = bi; }
-    __syncthreads();
-    if (tid == 0) {
-      float v = redf[0];
-      int i0 = redi[0];
-      for (int w = 1; w < kSampleThreads / 32; ++w) argmax_combine(v, i0, redf[w], redi[w]);
-      p.st_m[o] = v;
-      p.st_arg[o] = i0;
-    }
-  }
-  if (c == 0 && r == 0 && tid == 0) {
-    p.ticket[b] = 0;
-    if (b == 0) *p.status = 0u;
-  }
-}
-
-// Residual values of this thread's EPT contiguous elements of chunk `c`, and their compensated
-// sum / last positive index.  Called identically by the chunk pass and by the final re-scan.
-template <int EPT>
-__device__ __forceinline__ void chunk_thread_residual(const float* tr, const float* dr, int start, int V, float Mt,
-                                                      float iZt, float Md, float iZd, bool has_d, float (&r)[EPT]) {
+      FF v{k.s, -k.c};
 #pragma unroll
-  for (int i = 0; i < EPT / 4; ++i) {
-    const int idx = start + 4 * i;
-    if (idx < V) {
-      const float4 tv = *reinterpret_cast<const float4*>(tr + idx);
-      float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (has_d) dv = *reinterpret_cast<const float4*>(dr + idx);
-      r[4 * i] = resid(tv.x, dv.x, Mt, iZt, Md, iZd, has_d);
-      r[4 * i + 1] = resid(tv.y, dv.y, Mt, iZt, Md, iZd, has_d);
-      r[4 * i + 2] = resid(tv.z, dv.z, Mt, iZt, Md, iZd, has_d);
-      r[4 * i + 3] = resid(tv.w, dv.w, Mt, iZt, Md, iZd, has_d);
+      for (int o = 16; o > 0; o >>= 1) {
+        FF w;
+        w.hi = __shfl_down_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_down_sync(0xffffffffu, v.lo, o);
+        if (lane < o) v = ff_add(v, w);
+      }
+      if (lane == 0) {
+        p.st_m[it] = m;
+        p.st_s[it] = (double)v.hi + (double)v.lo;
+      }
     } else {
-      r[4 * i] = r[4 * i + 1] = r[4 * i + 2] = r[4 * i + 3] = 0.f;
+      int base;
+      src_of(it, base);
+      float bv = neg_inf();
+      int bi = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int idx = base + i * 128 + lane * 4;
+        const float e[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (idx + j < p.V && e[j] > bv) { bv = e[j]; bi = idx + j; }
+      }
+      warp_argmax(bv, bi);
+      if (lane == 0) {
+        p.st_m[it] = bv;
+        p.st_arg[it] = bi;
+      }
     }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = xn[i];
   }
 }
 
-template <int EPT>
-__global__ void __launch_bounds__(kSampleThreads) sample_residual(const __grid_constant__ SampleParams p) {
+// One CTA per sequence: merges the chunk statistics of its rows and finishes the sequence --
+// accept decisions and the residual row's statistics (stochastic chain), or the argmax merge and
+// the greedy chain / tree rule.
+template <bool GREEDY>
+__global__ void __launch_bounds__(kSampleThreads) sample_finalize(const __grid_constant__ SampleParams p) {
   __shared__ float sM[2 * kMaxGamma + 1];
   __shared__ double sZ[2 * kMaxGamma + 1];
-  __shared__ double redd[32];
-  __shared__ int redi[32];
-  __shared__ double s_tot[kMaxChunks];
-  __shared__ int s_k, s_last, s_cstar, s_thread, s_y;
-  __shared__ double s_acc, s_R;
-  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
+  __shared__ int sa[kMaxTreeNodes > kMaxGamma + 1 ? kMaxTreeNodes : kMaxGamma + 1];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = p.rows_t + p.rows_d;
+  if (!GREEDY) {
+    for (int rr = warp; rr < rows; rr += kWarps) {
+      const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
+      float m = neg_inf();
+      for (int cc = lane; cc < p.schunks; cc += 32) m = fmaxf(m, p.st_m[oo + cc]);
+      m = warp_max(m);
+      // item weights exp(M_c - M) in fp32 (exp2f, 2 ulp; M_c - M is exact or far below 0 where
+      // the weight is negligible), products and sums in fp64 in a fixed order
+      double z = 0.0;
+      for (int cc = lane; cc < p.schunks; cc += 32) z += p.st_s[oo + cc] * (double)exp_shift(p.st_m[oo + cc], m);
+      z = warp_sum_d(z);
+      if (lane == 0) { sM[rr] = m; sZ[rr] = z; }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int k = chain_decide_warp(p, b, sM, sZ);
+      if (lane == 0) {
+        SeqInfo si;
+        si.k = k;
+        si.pad = 0;
+        si.Mt = 0.f; si.Md = 0.f; si.Zt = 1.0; si.Zd = 1.0;
+        if (k >= 0) { si.Mt = sM[k]; si.Zt = sZ[k]; }
+        if (k >= 0 && k < p.gamma) { si.Md = sM[p.rows_t + k]; si.Zd = sZ[p.rows_t + k]; }
+        p.seq[b] = si;
+        if (k < 0) write_chain_out(p, b, -1, -1);
+      }
+    }
+  } else {
+    for (int rr = warp; rr < rows; rr += kWarps) {
+      const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
+      float v = neg_inf();
+      int i = INT_MAX;
+      for (int cc = lane; cc < p.schunks; cc += 32) argmax_combine(v, i, p.st_m[oo + cc], p.st_arg[oo + cc]);
+      warp_argmax(v, i);
+      if (lane == 0) sa[rr] = i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      if (p.mode == SPEC_SAMPLE_TREE_GREEDY) {
+        tree_select_write(p, b, sa);
+      } else {
+        int k = p.gamma;
+        for (int i = 0; i < p.gamma; ++i) {
+          const int xi = p.tok[(int64_t)b * p.tok_sb + i];
+          if (xi < 0 || xi >= p.V) { k = -1; break; }
+        }
+        if (k >= 0)
+          for (int i = 0; i < p.gamma; ++i)
+            if (p.tok[(int64_t)b * p.tok_sb + i] != sa[i]) { k = i; break; }
+        write_chain_out(p, b, k, k >= 0 ? sa[k] : -1);
+      }
+    }
+  }
+}
 
-  // 1. row statistics (max, normaliser) of every target and draft row of this sequence
-  for (int r = warp; r < rows; r += kSampleThreads / 32) {
-    const int64_t o = ((int64_t)b * rows + r) * p.nchunks;
-    float m = neg_inf();
-    for (int cc = lane; cc < p.nchunks; cc += 32) m = fmaxf(m, p.st_m[o + cc]);
-    m = warp_max(m);
-    double z = 0.0;
-    for (int cc = lane; cc < p.nchunks; cc += 32) z += p.st_s[o + cc] * exp((double)p.st_m[o + cc] - (double)m);
-    z = warp_sum_d(z);
-    if (lane == 0) { sM[r] = m; sZ[r] = z; }
+// Residual of four consecutive elements starting at idx (idx < V, V % 4 == 0).
+__device__ __forceinline__ float4 resid4(const float* tr, const float* dr, int idx, float Mt, float iZt, float Md,
+                                         float iZd, bool has_d) {
+  const float4 tv = __ldcs(reinterpret_cast<const float4*>(tr + idx));
+  float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (has_d) dv = __ldcs(reinterpret_cast<const float4*>(dr + idx));
+  return make_float4(resid(tv.x, dv.x, Mt, iZt, Md, iZd, has_d), resid(tv.y, dv.y, Mt, iZt, Md, iZd, has_d),
+                     resid(tv.z, dv.z, Mt, iZt, Md, iZd, has_d), resid(tv.w, dv.w, Mt, iZt, Md, iZd, has_d));
+}
+
+// Residual mass of one warp slice of a chunk: warp w of the chunk covers 32 * EPT elements in
+// slabs of 128 (lane l takes elements 4l..4l+3 of each slab).  Returns the warp's sum (valid in
+// lane 0, float-float reduced) and the last index with positive residual (all lanes).
+template <int EPT>
+__device__ __forceinline__ double warp_slice_residual(const float* tr, const float* dr, int start, int V, float Mt,
+                                                      float iZt, float Md, float iZd, bool has_d, int& last) {
+  const int lane = threadIdx.x & 31;
+  Kahan ks;
+  last = -1;
+#pragma unroll
+  for (int i = 0; i < EPT / 4; ++i) {
+    const int idx = start + i * 128 + lane * 4;
+    if (idx < V) {
+      const float4 r = resid4(tr, dr, idx, Mt, iZt, Md, iZd, has_d);
+      ks.add(r.x); ks.add(r.y); ks.add(r.z); ks.add(r.w);
+      last = r.w > 0.f ? idx + 3 : (r.z > 0.f ? idx + 2 : (r.y > 0.f ? idx + 1 : (r.x > 0.f ? idx : last)));
+    }
   }
-  __syncthreads();
-  // 2. accept decisions (one warp, one lane per draft)
-  if (warp == 0) {
-    const int kk = chain_decide_warp(p, b, sM, sZ);
-    if (lane == 0) s_k = kk;
+  FF v{ks.s, -ks.c};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF w;
+    w.hi = __shfl_down_sync(0xffffffffu, v.hi, o);
+    w.lo = __shfl_down_sync(0xffffffffu, v.lo, o);
+    if (lane < o) v = ff_add(v, w);
   }
-  __syncthreads();
-  const int k = s_k;
-  if (k < 0) {
-    if (c == 0 && tid == 0) write_chain_out(p, b, -1, -1);
-    return;
-  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  return (double)v.hi + (double)v.lo;
+}
+
+// Residual pass (stochastic chain): grid (chunks, B).  Each warp sums its slice of the chunk; the
+// last CTA of the sequence walks the slice sums in token order to the slice where the cumulative
+// residual passes u * R and re-scans that slice (1024 elements for 8192-element chunks) with one
+// warp, slab by slab, with an fp64 warp scan.
+template <int EPT>
+__global__ void __launch_bounds__(kSampleThreads, 4) sample_residual(const __grid_constant__ SampleParams p) {
+  __shared__ int s_last;
+  __shared__ int s_y;
+  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slice = 32 * EPT;                 // elements per warp slice
+  const int nslices = p.nchunks * kWarps;
+  double* wsum = p.res_sum + (int64_t)b * nslices;
+  int32_t* wlast = p.res_last + (int64_t)b * nslices;
+
+  const int k = __ldcg(&p.seq[b].k);
+  if (k < 0) return;  // invalid token: the statistics pass already wrote the row
   bool has_d = k < p.gamma;
   const float* tr = trow(p, b, k);
   const float* dr = has_d ? drow(p, b, k) : tr;
-  const float Mt = sM[k];
-  const float iZt = (float)(1.0 / sZ[k]);
-  const float Md = has_d ? sM[p.rows_t + k] : 0.f;
-  const float iZd = has_d ? (float)(1.0 / sZ[p.rows_t + k]) : 0.f;
+  const float Mt = __ldcg(&p.seq[b].Mt);
+  const float iZt = (float)(1.0 / __ldcg(&p.seq[b].Zt));
+  const float Md = has_d ? __ldcg(&p.seq[b].Md) : 0.f;
+  const float iZd = has_d ? (float)(1.0 / __ldcg(&p.seq[b].Zd)) : 0.f;
 
-  // 3. residual mass of this chunk
   {
-    float r[EPT];
-    const int start = c * p.chunk + tid * EPT;
-    chunk_thread_residual<EPT>(tr, dr, start, p.V, Mt, iZt, Md, iZd, has_d, r);
-    Kahan ks;
-    int last = -1;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      ks.add(r[e]);
-      if (r[e] > 0.f) last = start + e;
+    int last;
+    const double ws = warp_slice_residual<EPT>(tr, dr, c * p.chunk + warp * slice, p.V, Mt, iZt, Md, iZd, has_d, last);
+    if (lane == 0) {
+      wsum[c * kWarps + warp] = ws;
+      wlast[c * kWarps + warp] = last;
     }
-    const double tot = block_sum_d(ks.value(), redd);
-    const int lst = block_max_i(last, redi);
+    __syncthreads();
     if (tid == 0) {
-      p.res_sum[(int64_t)b * p.nchunks + c] = tot;
-      p.res_last[(int64_t)b * p.nchunks + c] = lst;
       __threadfence();
-      const int t = atomicAdd(&p.ticket[b], 1);
+      const int t = atomicAdd(&p.ticket_b[b], 1);
       s_last = (t == p.nchunks - 1);
     }
     __syncthreads();
     if (!s_last) return;
   }
   __threadfence();
+  if (warp != 0) return;
 
-  // 4. last CTA of the sequence: locate u * R in the cumulative residual and emit
-  for (int cc = tid; cc < p.nchunks; cc += kSampleThreads)
-    s_tot[cc] = __ldcg(p.res_sum + (int64_t)b * p.nchunks + cc);
-  __syncthreads();
-  if (tid == 0) {
-    double R = 0.0;
-    for (int cc = 0; cc < p.nchunks; ++cc) R += s_tot[cc];
-    s_R = R;
-  }
-  __syncthreads();
-  int fallback_last = -1;
-  if (s_R == 0.0) {
-    // residual identically zero: draw from P_{k+1} itself
+  // ---- last CTA, warp 0.  Lane l owns the consecutive slices [l * per, (l + 1) * per); an fp64
+  // exclusive scan over the lanes' sums gives every slice's prefix in token order, and R.
+  const int per = (nslices + 31) / 32;
+  auto scan_slices = [&](double& pre, double& total) {
+    double lsum = 0.0;
+    for (int j = 0; j < per; ++j) {
+      const int sl = lane * per + j;
+      if (sl < nslices) lsum += __ldcg(wsum + sl);
+    }
+    double incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    pre = incl - lsum;
+    total = __shfl_sync(0xffffffffu, incl, 31);
+  };
+  double pre, R;
+  scan_slices(pre, R);
+  if (R == 0.0) {
+    // residual identically zero: draw from P_{k+1} itself (recompute every slice with P)
     has_d = false;
-    for (int cc = 0; cc < p.nchunks; ++cc) {
-      float r[EPT];
-      const int start = cc * p.chunk + tid * EPT;
-      chunk_thread_residual<EPT>(tr, tr, start, p.V, Mt, iZt, 0.f, 0.f, false, r);
-      Kahan ks;
-      int last = -1;
+    for (int sl = 0; sl < nslices; ++sl) {
+      int last;
+      const double ws = warp_slice_residual<EPT>(tr, tr, (sl / kWarps) * p.chunk + (sl % kWarps) * slice, p.V, Mt,
+                                                 iZt, 0.f, 0.f, false, last);
+      if (lane == 0) { wsum[sl] = ws; wlast[sl] = last; }
+    }
+    __syncwarp();
+    __threadfence_block();
+    scan_slices(pre, R);
+  }
+  const double thr = (double)p.u[(int64_t)b * p.u_sb + p.gamma] * R;
+  // the first slice whose cumulative sum passes thr: each lane checks its own slices
+  int my_sl = -1;
+  double my_acc = 0.0;
+  {
+    double run = pre;
+    for (int j = 0; j < per; ++j) {
+      const int sl = lane * per + j;
+      if (sl >= nslices) break;
+      const double ws = __ldcg(wsum + sl);
+      if (run + ws > thr) { my_sl = sl; my_acc = run; break; }
+      run += ws;
+    }
+  }
+  const unsigned found = __ballot_sync(0xffffffffu, my_sl >= 0);
+  int sstar = -1;
+  double acc = 0.0;
+  if (found) {
+    const int src = __ffs(found) - 1;
+    sstar = __shfl_sync(0xffffffffu, my_sl, src);
+    acc = __shfl_sync(0xffffffffu, my_acc, src);
+  }
+  int y = -1;
+  if (sstar >= 0) {
+    const int start = (sstar / kWarps) * p.chunk + (sstar % kWarps) * slice;
+    // the whole slice first (all loads in flight together), then the slab-by-slab scan
+    float4 rs[EPT / 4];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        ks.add(r[e]);
-        if (r[e] > 0.f) last = start + e;
-      }
-      const double tot = block_sum_d(ks.value(), redd);
-      const int lst = block_max_i(last, redi);
-      if (tid == 0) s_tot[cc] = tot;
-      fallback_last = max(fallback_last, lst);
+    for (int i = 0; i < EPT / 4; ++i) {
+      const int idx = start + i * 128 + lane * 4;
+      rs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < p.V) rs[i] = resid4(tr, dr, idx, Mt, iZt, Md, iZd, has_d);
     }
-    __syncthreads();
-    if (tid == 0) {
-      double R = 0.0;
-      for (int cc = 0; cc < p.nchunks; ++cc) R += s_tot[cc];
-      s_R = R;
-    }
-    __syncthreads();
-  }
-  const double thr = (double)p.u[(int64_t)b * p.u_sb + p.gamma] * s_R;
-  if (tid == 0) {
-    double acc = 0.0;
-    int cs = -1;
-    for (int cc = 0; cc < p.nchunks; ++cc) {
-      if (acc + s_tot[cc] > thr) { cs = cc; break; }
-      acc += s_tot[cc];
-    }
-    s_cstar = cs;
-    s_acc = acc;
-    s_thread = INT_MAX;
-    s_y = -1;
-  }
-  __syncthreads();
-  const int cs = s_cstar;
-  if (cs >= 0) {
-    float r[EPT];
-    const int start = cs * p.chunk + tid * EPT;
-    chunk_thread_residual<EPT>(tr, dr, start, p.V, Mt, iZt, Md, iZd, has_d, r);
-    Kahan ks;
+    double base = acc;
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) ks.add(r[e]);
-    double total;
-    const double excl = block_exclusive_scan_d(ks.value(), redd, total);
-    const double before = s_acc + excl;
-    if (before + ks.value() > thr) atomicMin(&s_thread, tid);
-    __syncthreads();
-    if (tid == s_thread) {
-      Kahan run;
-      int y = -1, lastpos = -1;
-      for (int e = 0; e < EPT; ++e) {
-        run.add(r[e]);
-        if (r[e] > 0.f) lastpos = start + e;
-        if (before + run.value() > thr) { y = start + e; break; }
+    for (int i = 0; i < EPT / 4; ++i) {
+      if (y >= 0) break;
+      const int idx = start + i * 128 + lane * 4;
+      const float4 r = rs[i];
+      const double lsum = ((double)r.x + (double)r.y) + ((double)r.z + (double)r.w);
+      double incl = lsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
       }
-      s_y = (y >= 0) ? y : lastpos;
+      const unsigned hit = __ballot_sync(0xffffffffu, base + incl > thr);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        if (lane == src) {
+          const double run0 = base + incl - lsum;
+          const double run1 = run0 + (double)r.x, run2 = run1 + (double)r.y, run3 = run2 + (double)r.z;
+          const double run4 = run3 + (double)r.w;
+          int yy = run1 > thr ? idx : (run2 > thr ? idx + 1 : (run3 > thr ? idx + 2 : (run4 > thr ? idx + 3 : -1)));
+          if (yy < 0) yy = r.w > 0.f ? idx + 3 : (r.z > 0.f ? idx + 2 : (r.y > 0.f ? idx + 1 : idx));
+          s_y = yy;
+        }
+        __syncwarp();
+        y = s_y;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
+    if (y < 0) y = __ldcg(wlast + sstar);  // rounding left the threshold at the slice end
   }
-  if (tid == 0) {
-    int y = s_y;
-    if (y < 0) {
-      // no index passed the threshold through rounding: the largest index with positive mass
-      int lst = -1;
-      if (s_R != 0.0 && fallback_last < 0)
-        for (int cc = 0; cc < p.nchunks; ++cc) lst = max(lst, __ldcg(p.res_last + (int64_t)b * p.nchunks + cc));
-      else lst = fallback_last;
-      y = lst;
-    }
-    write_chain_out(p, b, k, y);
+  if (y < 0) {
+    // no slice passed the threshold through rounding: the largest index with positive mass
+    int lst = -1;
+    for (int i = lane; i < nslices; i += 32) lst = max(lst, __ldcg(wlast + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lst = max(lst, __shfl_xor_sync(0xffffffffu, lst, o));
+    y = lst;
   }
-}
-
-// greedy: merge chunk argmaxes per row, then the chain or tree rule.  grid (B), 256 threads.
-__global__ void __launch_bounds__(kSampleThreads) sample_greedy_decide(const __grid_constant__ SampleParams p) {
-  __shared__ int a[kMaxTreeNodes > kMaxGamma + 1 ? kMaxTreeNodes : kMaxGamma + 1];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = p.rows_t;
-  for (int r = warp; r < rows; r += kSampleThreads / 32) {
-    const int64_t o = ((int64_t)b * rows + r) * p.nchunks;
-    float v = neg_inf();
-    int i = INT_MAX;
-    for (int cc = lane; cc < p.nchunks; cc += 32) argmax_combine(v, i, p.st_m[o + cc], p.st_arg[o + cc]);
-    warp_argmax(v, i);
-    if (lane == 0) a[r] = i;
-  }
-  __syncthreads();
-  if (tid != 0) return;
-  if (p.mode == SPEC_SAMPLE_TREE_GREEDY) {
-    tree_select_write(p, b, a);
-    return;
-  }
-  int k = p.gamma;
-  for (int i = 0; i < p.gamma; ++i) {
-    const int x = p.tok[(int64_t)b * p.tok_sb + i];
-    if (x < 0 || x >= p.V) { k = -1; break; }
-  }
-  if (k >= 0)
-    for (int i = 0; i < p.gamma; ++i)
-      if (p.tok[(int64_t)b * p.tok_sb + i] != a[i]) { k = i; break; }
-  write_chain_out(p, b, k, k >= 0 ? a[k] : -1);
+  if (lane == 0) write_chain_out(p, b, k, y);
 }
 
 // ------------------------------------------------------------------ small-V kernel
@@ -597,53 +681,73 @@ static int pick_chunk(int V, int rows_total, int B, int num_sms) {
   return 2048;
 }
 
+static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
 size_t sample_workspace_bytes(int mode, int B, int rows_t, int rows_d, int V) {
   (void)mode;
   const size_t nch = (size_t)(V + kMinChunk - 1) / kMinChunk;
+  const size_t sch = (size_t)(V + kStatChunk - 1) / kStatChunk;
   const size_t rows = (size_t)rows_t + rows_d;
-  size_t bytes = 256;
-  bytes += (B * rows * nch * sizeof(float) + 255) / 256 * 256;    // st_m
-  bytes += (B * rows * nch * sizeof(double) + 255) / 256 * 256;   // st_s / st_arg
-  bytes += (B * nch * sizeof(double) + 255) / 256 * 256;          // res_sum
-  bytes += (B * nch * sizeof(int32_t) + 255) / 256 * 256;         // res_last
-  bytes += ((size_t)B * sizeof(int32_t) + 255) / 256 * 256;       // ticket
+  size_t bytes = 256;                                        // status
+  bytes += round256(2 * (size_t)B * sizeof(int32_t));        // tickets (zeroed per call)
+  bytes += round256((size_t)B * sizeof(SeqInfo));            // accept decisions
+  bytes += round256(B * rows * sch * sizeof(float));         // st_m
+  bytes += round256(B * rows * sch * sizeof(double));        // st_s / st_arg
+  bytes += round256(B * nch * 8 * sizeof(double));           // res_sum (per warp slice)
+  bytes += round256(B * nch * 8 * sizeof(int32_t));          // res_last
   return bytes;
 }
 
 void sample_workspace_carve(void* ws, SampleParams* p) {
   const size_t nch = (size_t)(p->V + kMinChunk - 1) / kMinChunk;
+  const size_t sch = (size_t)(p->V + kStatChunk - 1) / kStatChunk;
   const size_t rows = (size_t)p->rows_t + p->rows_d;
   const size_t B = (size_t)p->B;
   uint8_t* q = reinterpret_cast<uint8_t*>(ws);
   p->status = reinterpret_cast<uint32_t*>(q);
   q += 256;
+  p->ticket_a = reinterpret_cast<int32_t*>(q);
+  p->ticket_b = p->ticket_a + B;
+  q += round256(2 * B * sizeof(int32_t));
+  p->seq = reinterpret_cast<SeqInfo*>(q);
+  q += round256(B * sizeof(SeqInfo));
   p->st_m = reinterpret_cast<float*>(q);
-  q += (B * rows * nch * sizeof(float) + 255) / 256 * 256;
+  q += round256(B * rows * sch * sizeof(float));
   p->st_s = reinterpret_cast<double*>(q);
   p->st_arg = reinterpret_cast<int32_t*>(q);
-  q += (B * rows * nch * sizeof(double) + 255) / 256 * 256;
+  q += round256(B * rows * sch * sizeof(double));
   p->res_sum = reinterpret_cast<double*>(q);
-  q += (B * nch * sizeof(double) + 255) / 256 * 256;
+  q += round256(B * nch * 8 * sizeof(double));
   p->res_last = reinterpret_cast<int32_t*>(q);
-  q += (B * nch * sizeof(int32_t) + 255) / 256 * 256;
-  p->ticket = reinterpret_cast<int32_t*>(q);
 }
 
 template <int EPT>
 static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const int rows = p.rows_t + p.rows_d;
-  dim3 g1(p.nchunks, rows, p.B);
+  // status word and both ticket arrays start at zero for this call
+  cudaError_t e = cudaMemsetAsync(p.status, 0, 256 + 2 * (size_t)p.B * sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
+  const int items = p.schunks * rows * p.B;
+  // persistent statistics grid: as many CTAs as fit on the GPU at once (warp-granular items)
+  int per_sm = 1;
+  if (p.mode == SPEC_SAMPLE_CHAIN)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_stats<false>, kSampleThreads, 0);
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_stats<true>, kSampleThreads, 0);
+  if (per_sm < 1) per_sm = 1;
+  const int need = (items + kWarps - 1) / kWarps;
+  const int g1 = need < per_sm * p.num_sms ? need : per_sm * p.num_sms;
   if (p.mode == SPEC_SAMPLE_CHAIN) {
-    sample_stats<EPT, false><<<g1, kSampleThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    sample_stats<false><<<g1, kSampleThreads, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    sample_finalize<false><<<p.B, kSampleThreads, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     dim3 g2(p.nchunks, p.B);
     sample_residual<EPT><<<g2, kSampleThreads, 0, stream>>>(p);
   } else {
-    sample_stats<EPT, true><<<g1, kSampleThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    sample_greedy_decide<<<p.B, kSampleThreads, 0, stream>>>(p);
+    sample_stats<true><<<g1, kSampleThreads, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    sample_finalize<true><<<p.B, kSampleThreads, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
@@ -656,8 +760,10 @@ cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream) {
     sample_small<<<(p.B + per_block - 1) / per_block, kSampleThreads, 0, stream>>>(p);
     return cudaGetLastError();
   }
+  p.num_sms = num_sms;
   p.chunk = pick_chunk(p.V, p.rows_t + p.rows_d, p.B, num_sms);
   p.nchunks = (p.V + p.chunk - 1) / p.chunk;
+  p.schunks = (p.V + kStatChunk - 1) / kStatChunk;
   switch (p.chunk) {
     case 8192: return launch_large<32>(p, stream);
     case 4096: return launch_large<16>(p, stream);
