@@ -275,8 +275,52 @@ class Runner:
                                 draft_tokens=i["x"], uniforms=i["u"], workspace=self.ws_s)
 
     def launches_per_step(self):
-        # our kernels: window (append, partial, merge) x draft steps, verify (partial, merge), sample (2)
-        return (3 * self.cfg.draft_steps if self.cfg.window else 0) + 2 + 2
+        """Our kernels per step by the library's launch rules (status/ticket memsets are not
+        counted); used only when the captured graphs cannot be inspected.  Verify: partial + merge.
+        Window: see below.  Sampling: one warp-per-sequence kernel for V <= 2048, else statistics +
+        finalize, plus the residual pass for the chain."""
+        import torch
+        cfg = self.cfg
+        win = 0
+        if cfg.window:
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            S, seg_tiles = cfg.B * cfg.Hkv, -(-cfg.window // 128)
+            spc, even = -(-S // sms), -(-S * seg_tiles // sms)
+            if cfg.kv_dtype == "bf16" and cfg.D == 128 and cfg.G > 32:
+                per_call = 3                     # append + tensor-core partial + merge
+            elif cfg.kv_dtype == "bf16" and cfg.G <= 64 and spc * seg_tiles <= max(2 * even, 16):
+                per_call = 1                     # whole segments per CTA: partial writes o itself
+            else:
+                per_call = 2                     # partial + merge (append fused into the merge)
+            win = cfg.draft_steps * per_call
+        if cfg.vocab <= 2048:
+            samp = 1
+        else:
+            samp = 2 if cfg.tree_nodes else 3
+        return win + 2 + samp
+
+
+def count_kernel_nodes(graph):
+    """Kernel nodes in a captured CUDA graph (driver API on the raw cudaGraph_t), or None."""
+    import ctypes
+    try:
+        raw = ctypes.c_void_p(graph.raw_cuda_graph())
+        cu = ctypes.CDLL("libcuda.so.1")
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(raw, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * max(1, n.value))()
+        if cu.cuGraphGetNodes(raw, nodes, ctypes.byref(n)) != 0:
+            return None
+        kernels = 0
+        for i in range(n.value):
+            t = ctypes.c_int(-1)
+            if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0:
+                return None
+            kernels += int(t.value == 0)   # CU_GRAPH_NODE_TYPE_KERNEL
+        return kernels
+    except Exception:
+        return None
 
 
 class GraphOps:
@@ -287,6 +331,7 @@ class GraphOps:
     def __init__(self, runner, stream):
         import torch
         self.g = {}
+        self.kernels_per_step = 0          # kernel nodes over the captured ops, None if not countable
         cfg = runner.cfg
         ops = {"verify": runner.verify, "sample": runner.sample}
         if cfg.window:
@@ -295,9 +340,17 @@ class GraphOps:
             for name, fn in ops.items():
                 fn()                       # eager first call (module load, attributes)
                 stream.synchronize()
-                g = torch.cuda.CUDAGraph()
+                try:
+                    g, kept = torch.cuda.CUDAGraph(keep_graph=True), True
+                except TypeError:
+                    g, kept = torch.cuda.CUDAGraph(), False
                 with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
                     fn()
+                k = count_kernel_nodes(g) if kept else None
+                self.kernels_per_step = None if (k is None or self.kernels_per_step is None) \
+                    else self.kernels_per_step + k
+                if kept:
+                    g.instantiate()
                 self.g[name] = g
         torch.cuda.synchronize()
 
@@ -371,7 +424,8 @@ def time_steps(runner, K, W, pg, device, use_graphs=True):
     ver = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     smp = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
     return dict(total_ms=total_ms, wall_s=wall, window_ms=win, verify_ms=ver, sample_ms=smp, clocks=ck,
-                l2_flush=flush is not None, graphs=use_graphs)
+                l2_flush=flush is not None, graphs=use_graphs,
+                kernels_per_step=gops.kernels_per_step if use_graphs else None)
 
 
 def time_e2e(runner, K, W, device):
@@ -570,7 +624,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
                      "peak_source": peak_kind},
-        "gpu_launches": runner.launches_per_step() * args.steps,
+        "gpu_launches": (t["kernels_per_step"] if t["kernels_per_step"] is not None
+                         else runner.launches_per_step()) * args.steps,
+        "gpu_launches_source": "kernel nodes of the captured step graphs" if t["kernels_per_step"] is not None
+                               else "launch rule of the library",
         "clocks": t["clocks"],
         "wall_s_timed": t["wall_s"],
         "e2e": e2e,

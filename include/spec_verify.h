@@ -150,8 +150,10 @@ int spec_verify_attn_noalloc(const spec_attn_args* args, spec_stream_t stream);
  *
  * Single-query draft attention over the last min(pos[b], W) tokens of sequence b, kept in a
  * ring: token t (0-based) lives in slot t mod W.  pos[b] counts the tokens written including
- * the current one.  If k_new/v_new are given, the current token's K/V are first written into
- * slot (pos[b] - 1) mod W (the ring is updated in place).  The visible slots are then
+ * the current one.  If k_new/v_new are given, the current token's K/V take slot (pos[b] - 1)
+ * mod W: the attention uses them in place of that slot's old contents, and the ring is updated
+ * in place (the slot holds k_new/v_new once the call's work on the stream has completed);
+ * k_new/v_new must not overlap the rings.  The visible slots are
  * {t mod W : pos[b] - min(pos[b], W) <= t < pos[b]}; since softmax over keys does not depend on
  * their order, this equals attention over the page's shift-left buffer.
  *

@@ -197,6 +197,7 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   p.scale_log2 = resolve_scale(a->scale, a->D) * 1.4426950408889634f;
   p.o = a->o; p.o_sb = a->o_stride_b; p.o_st = a->o_stride_t; p.o_sh = a->o_stride_h;
   p.o_bf16 = a->o_dtype == SPEC_BF16;
+  p.kv_bf16 = a->kv_dtype == SPEC_BF16;
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
 
   CUtensorMap tmK, tmV;
@@ -237,14 +238,6 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int bf16 = a->kv_dtype == SPEC_BF16;
-  if (a->k_new) {
-    specv::WindowAppend w;
-    w.B = a->B; w.Hkv = a->Hkv; w.D = a->D; w.W = a->W; w.bf16 = bf16;
-    w.pos = a->pos; w.k_ring = a->k_ring; w.v_ring = a->v_ring;
-    w.ring_sb = a->ring_stride_b; w.ring_sh = a->ring_stride_h;
-    w.k_new = a->k_new; w.v_new = a->v_new; w.new_sb = a->new_stride_b; w.new_sh = a->new_stride_h;
-    if (specv::launch_window_append(w, cs) != cudaSuccess) return SPEC_ERR_CUDA;
-  }
   AttnParams p;
   memset(&p, 0, sizeof(p));
   p.B = a->B; p.Hq = a->Hq; p.Hkv = a->Hkv; p.G = a->Hq / a->Hkv; p.D = a->D; p.nq = 1;
@@ -258,6 +251,10 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   p.scale_log2 = resolve_scale(a->scale, a->D) * 1.4426950408889634f;
   p.o = a->o; p.o_sb = a->o_stride_b; p.o_st = 0; p.o_sh = a->o_stride_h;
   p.o_bf16 = a->o_dtype == SPEC_BF16;
+  p.kv_bf16 = bf16;
+  p.has_new = a->k_new != nullptr;
+  p.k_new = a->k_new; p.v_new = a->v_new;
+  p.new_sb = a->new_stride_b; p.new_sh = a->new_stride_h;
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
   CUtensorMap tmK, tmV;
   if (bf16) {

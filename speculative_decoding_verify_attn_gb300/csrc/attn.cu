@@ -1,8 +1,9 @@
 // Split-KV ("flash-decode") attention for speculative verify and for the draft ring window.
 //
-// Work decomposition (one launch, balanced over the whole batch): the key ranges of all
-// (sequence b, kv head g) segments are laid end to end, total = Hkv * sum_b len_b keys, and CTA c
-// takes the global range [c*T, (c+1)*T), T = max(ceil(total / grid_x), kMinKeysPerCta).  A CTA
+// Work decomposition (one launch, balanced over the whole batch): the 128-key tiles of all
+// (sequence b, kv head g) segments are laid end to end, total = Hkv * sum_b ceil(len_b / 128)
+// tiles, and CTA c takes the global tile range [c*T, (c+1)*T), T = max(ceil(total / grid_x),
+// kMinTilesPerCta), so no tile is split between two CTAs.  A CTA
 // walks the segments its range touches; for each piece ("part") it produces the un-normalised
 // flash-attention partial (m, l, o) of every query row of that segment, stored at slot s + c
 // (s = b*Hkv + g; along the monotone walk s + c is unique, so S + grid_x slots suffice).  The
@@ -19,6 +20,9 @@
 // and the tree keys whose node is on its root path (bitmask); window: every valid ring slot.
 // Cache slots at or beyond len are never trusted: their scores are masked by select, and the
 // matching V rows are zeroed before P.V, so NaN garbage there cannot leak into the output.
+// Window with a new key: ring slot (pos - 1) mod W is about to be overwritten, so the partial
+// kernels treat it like a slot past the end, and the merge kernel adds the new key's score and
+// value to the softmax and then stores the key into the slot (after every partial has read it).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -36,9 +40,171 @@ static inline int slices_for_rows(int rows_per_group) {
 
 // ------------------------------------------------------------------ bf16 partial kernel
 
+// Named barrier 1 over the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+// Same barrier, returning the OR of `pred` over every consumer thread, so that all consumer warps
+// take the same decision.
+__device__ __forceinline__ int consumers_sync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\tselp.b32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r;
+}
+
+// Column swizzle of the fp32 combine buffers (rows of CW floats): 8-float groups XOR-ed by row, so
+// the float2 fragment stores of 8 rows spread over the banks.
+template <int CW>
+__device__ __forceinline__ int combine_col(int row, int col) {
+  return col ^ (((row & 7) << 3) & (CW - 8));
+}
+
+// Direct mode, end of a segment (the CTA owns all of it): the NKS warps of each 16-row tile hold
+// flash partials (m, l, o) of disjoint key slices of the same rows.  They are combined through
+// shared memory (each warp's Q staging region, free once the segment's tiles are consumed) in
+// NPASS column passes: every warp stores its o columns, then warp ks combines rows ks, ks + NKS,
+// ... of its tile in fixed slice order, adds the window's new key, normalises and writes the
+// output row.  Returns nonzero if the CTA must stop (a wait timed out in any warp).
+template <int D, int NKS, int NPASS>
+__device__ __forceinline__ int combine_part(const AttnParams& p, float (&o)[D / 8][4], float m_lo, float m_hi,
+                                            float l_lo, float l_hi, float* regions, float2* sML, int warp,
+                                            int lane, int rt, int ks, int row0, int rows_here, int b, int g,
+                                            int len, int bad, volatile int* s_abort) {
+  constexpr int DT = D / 8, CW = D / NPASS, EPL = CW / 32, RPW = 16 / NKS;
+  constexpr int REGION = 8 * D;  // floats in one warp's region (16 rows x D bf16)
+  const int q = lane >> 2, t = lane & 3;
+  const int rows_tile = min(16, rows_here - rt * 16);
+  if (t == 0) {
+    sML[warp * 16 + q] = make_float2(m_lo, l_lo);
+    sML[warp * 16 + q + 8] = make_float2(m_hi, l_hi);
+  }
+  const bool add_new = p.has_new && len > 0;
+  // direct mode: score of the new key for each row this warp combines
+  float s_new[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) s_new[i] = neg_inf();
+  if (add_new) {
+    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + b * p.new_sb + g * p.new_sh;
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int rr = ks + i * NKS;
+      if (rr < rows_tile) {
+        const int ro = row0 + rt * 16 + rr;
+        const __nv_bfloat16* qr = qb + b * p.q_sb + (ro / p.G) * p.q_st + (g * p.G + ro % p.G) * p.q_sh;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < D / 32; ++e)
+          dot = fmaf(__bfloat162float(qr[lane + 32 * e]), __bfloat162float(kn[lane + 32 * e]), dot);
+        s_new[i] = warp_sum(dot) * p.scale_log2;
+      }
+    }
+  }
+  float* mine = regions + warp * REGION;
+  int stop = 0;
+#pragma unroll
+  for (int h = 0; h < NPASS; ++h) {
+    // ---- this warp's o columns [h * CW, (h + 1) * CW) into its region
+#pragma unroll
+    for (int dt = h * (DT / NPASS); dt < (h + 1) * (DT / NPASS); ++dt) {
+      const int col = dt * 8 + 2 * t - h * CW;
+      if (q < rows_tile)
+        *reinterpret_cast<float2*>(mine + q * CW + combine_col<CW>(q, col)) = make_float2(o[dt][0], o[dt][1]);
+      if (NPASS == 2 && q + 8 < rows_tile)
+        *reinterpret_cast<float2*>(mine + (q + 8) * CW + combine_col<CW>(q + 8, col)) =
+            make_float2(o[dt][2], o[dt][3]);
+    }
+    consumers_sync();
+    if (h == 0) {
+      if (add_new && warp == 0) {
+        // every warp is past this segment's tiles: store the new key into its ring slot
+        const int slot = (__ldg(p.lens + b) - 1) % p.Lmax;
+        const int64_t src = (int64_t)b * p.new_sb + (int64_t)g * p.new_sh;
+        const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * D;
+        const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src;
+        const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + src;
+        __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.k)) + dst;
+        __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.v)) + dst;
+#pragma unroll
+        for (int e = 0; e < D / 32; ++e) {
+          kr[lane + 32 * e] = kn[lane + 32 * e];
+          vr[lane + 32 * e] = vn[lane + 32 * e];
+        }
+      }
+      if (len == 0 && warp == 0 && lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
+    }
+    // ---- combine the rows this warp owns (slice weights relative to the row maximum, the new
+    // key included; recomputed per pass to keep registers free)
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int rr = ks + i * NKS;
+      if (rr >= rows_tile) continue;
+      float M = s_new[i];
+#pragma unroll
+      for (int k = 0; k < NKS; ++k) M = fmaxf(M, sML[(rt * NKS + k) * 16 + rr].x);
+      const int c0 = lane * EPL;
+      float acc[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+      float L = 0.f;
+#pragma unroll
+      for (int k = 0; k < NKS; ++k) {
+        const float2 ml = sML[(rt * NKS + k) * 16 + rr];
+        const float wk = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
+        L = fmaf(wk, ml.y, L);
+        const float* src = regions + (rt * NKS + k) * REGION + rr * CW + combine_col<CW>(rr, c0);
+        float v[EPL];
+        if constexpr (EPL == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        } else if constexpr (EPL == 2) {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          v[0] = x.x; v[1] = x.y;
+        } else {
+          v[0] = *src;
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, v[e], acc[e]);
+      }
+      const int ro = row0 + rt * 16 + rr;
+      const int col = h * CW + c0;
+      {
+        const int j = ro / p.G, head = g * p.G + ro % p.G;
+        const int64_t off = (int64_t)b * p.o_sb + (int64_t)j * p.o_st + (int64_t)head * p.o_sh + col;
+        if (add_new) {
+          const float w_new = exp2f(s_new[i] - M);
+          L += w_new;
+          const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + b * p.new_sb + g * p.new_sh;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w_new, __bfloat162float(vn[col + e]), acc[e]);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        if (p.o_bf16) {
+          __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o) + off;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+        } else {
+          float* of = reinterpret_cast<float*>(p.o) + off;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) of[e] = acc[e] * inv;
+        }
+      }
+    }
+    // regions are reused by the next pass or the next part's Q staging
+    if (h + 1 < NPASS) consumers_sync();
+    else stop = consumers_sync_or(bad | *s_abort);
+  }
+  return stop;
+}
+
 template <int D, int MASK, int NKS>
-__device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw, uint64_t* full, uint64_t* empty,
-                              int warp, int lane, int row0, int rows_here, volatile int* s_abort) {
+__device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQ, float2* sML, uint64_t* full,
+                              uint64_t* empty, int warp, int lane, int row0, int rows_here, volatile int* s_abort) {
   constexpr int KT = kKeyTile;
   constexpr int KS = KT / NKS;     // keys of each tile this warp handles
   constexpr int NT = KS / 8;       // score n-tiles
@@ -51,6 +217,9 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
   const unsigned long long anc_lo = (MASK == kMaskTree) ? p.anc[j_lo] : 0ull;
   const unsigned long long anc_hi = (MASK == kMaskTree) ? p.anc[j_hi] : 0ull;
   const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  uint8_t* sQw = sQ + warp * (16 * D * 2);
+  // column passes of the slice combine: one when every row tile has at most 8 rows
+  const int npass = (NKS == kConsumerWarps && min(16, rows_here) <= 8) ? 1 : 2;
 
   Walker w;
   walker_init(p, blockIdx.x, w);
@@ -78,12 +247,16 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
     for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
     const int tail_start = len - p.nq;
+    // window with a new key: the ring slot being replaced (verify masks have none)
+    const int skip = (MASK == kMaskNone && p.has_new) ? (__ldg(p.lens + b) - 1) % p.Lmax : -1;
 
+    int bad = 0;
     for (int key0 = kb; key0 < ke; key0 += KT) {
       if (!mbar_wait_bounded(&full[stage], phase, s_abort)) {
         *s_abort = 1;
-        atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
-        return;
+        if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+        bad = 1;
+        break;
       }
       const uint8_t* sK = stages + stage * 2 * TILE;
       const uint8_t* sV = sK + TILE;
@@ -111,7 +284,8 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
           mma_bf16_16816(s[nt], qb, b2, b3);
         }
       }
-      const bool tail_tile = key0 + KT > ke;
+      const bool skip_tile = MASK == kMaskNone && (unsigned)(skip - key0) < (unsigned)KT;
+      const bool tail_tile = key0 + KT > ke || skip_tile;
       const bool needs_mask = tail_tile || (MASK != kMaskNone && key0 + KT > tail_start);
       float mx_lo = neg_inf(), mx_hi = neg_inf();
 #pragma unroll
@@ -123,7 +297,7 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
             const int kk = key0 + ks * KS + nt * 8 + 2 * (lane & 3) + (e & 1);
             const bool vis = (e < 2) ? key_visible<MASK>(kk, ke, tail_start, j_lo, anc_lo)
                                      : key_visible<MASK>(kk, ke, tail_start, j_hi, anc_hi);
-            if (!vis) x = neg_inf();
+            if (!vis || (MASK == kMaskNone && kk == skip)) x = neg_inf();
           }
           s[nt][e] = x;
         }
@@ -174,8 +348,9 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
           uint32_t v0, v1, v2, v3;
           ldmatrix_x4_trans(smem_u32(sV + (d0 >> 6) * (KT * 128) + r * 128 + ((c ^ (r & 7)) << 4)), v0, v1, v2, v3);
           if (tail_tile) {
-            const uint32_t m0 = (kf < ke ? 0x0000ffffu : 0u) | (kf + 1 < ke ? 0xffff0000u : 0u);
-            const uint32_t m1 = (kf + 8 < ke ? 0x0000ffffu : 0u) | (kf + 9 < ke ? 0xffff0000u : 0u);
+            auto ok = [&](int k) { return k < ke && (MASK != kMaskNone || k != skip); };
+            const uint32_t m0 = (ok(kf) ? 0x0000ffffu : 0u) | (ok(kf + 1) ? 0xffff0000u : 0u);
+            const uint32_t m1 = (ok(kf + 8) ? 0x0000ffffu : 0u) | (ok(kf + 9) ? 0xffff0000u : 0u);
             v0 &= m0; v1 &= m1; v2 &= m0; v3 &= m1;
           }
           mma_bf16_16816(o[dn], a, v0, v1);
@@ -190,8 +365,27 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQw
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    if constexpr (MASK == kMaskNone) {
+      if (p.direct) {
+        float* regions = reinterpret_cast<float*>(sQ);
+        int stop;
+        if constexpr (NKS == kConsumerWarps) {
+          stop = npass == 1 ? combine_part<D, NKS, 1>(p, o, m_lo, m_hi, l_lo, l_hi, regions, sML, warp, lane, rt, ks,
+                                                      row0, rows_here, b, g, len, bad, s_abort)
+                            : combine_part<D, NKS, 2>(p, o, m_lo, m_hi, l_lo, l_hi, regions, sML, warp, lane, rt, ks,
+                                                      row0, rows_here, b, g, len, bad, s_abort);
+        } else {
+          stop = combine_part<D, NKS, 2>(p, o, m_lo, m_hi, l_lo, l_hi, regions, sML, warp, lane, rt, ks, row0,
+                                         rows_here, b, g, len, bad, s_abort);
+        }
+        if (stop) return;
+        continue;
+      }
+    }
+    if (bad) return;
+    // split mode: one (m, l, o) record per (part, key slice, row) for the merge kernel
     const int64_t slot = (int64_t)(b * p.Hkv + g) + blockIdx.x;
-    const int64_t rec_base = (slot * kMaxSlices + ks) * p.rows + row0;
+    const int64_t rec_base = (slot * NKS + ks) * p.rows + row0;
     if (r_lo < rows_here) {
       const int64_t rec = rec_base + r_lo;
       if ((lane & 3) == 0) p.part_ml[rec] = make_float2(m_lo, l_lo);
@@ -216,6 +410,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   constexpr int TILE = kKeyTile * D * 2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * kStages];
+  __shared__ float2 sML[kConsumerWarps * 16];  // (m, l) of every consumer warp's 16 rows
   __shared__ int s_abort;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* stages = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -279,7 +474,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     }
     return;
   }
-  consumer_loop<D, MASK, NKS>(p, stages, sQ + warp * (16 * D * 2), full, empty, warp, lane, row0, rows_here, &s_abort);
+  consumer_loop<D, MASK, NKS>(p, stages, sQ, sML, full, empty, warp, lane, row0, rows_here, &s_abort);
 }
 
 // ------------------------------------------------------------------ fp32 partial kernel
@@ -297,6 +492,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
   int b, g, kb, ke, len;
   while (walker_next(p, w, b, g, kb, ke, len)) {
     const int tail_start = len - p.nq;
+    const int skip = p.has_new ? (__ldg(p.lens + b) - 1) % p.Lmax : -1;
     const float* kseg = kb_ + b * p.kv_sb + g * p.kv_sh;
     const float* vseg = vb_ + b * p.kv_sb + g * p.kv_sh;
     for (int r = warp; r < rows_here; r += 4) {
@@ -310,7 +506,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
       }
       float m = neg_inf(), l = 0.f;
       for (int kk = kb; kk < ke; ++kk) {
-        if (!key_visible<MASK>(kk, ke, tail_start, j, anc)) continue;
+        if (!key_visible<MASK>(kk, ke, tail_start, j, anc) || kk == skip) continue;
         const float* kp = kseg + (int64_t)kk * D;
         float dot = 0.f;
 #pragma unroll
@@ -325,7 +521,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
         m = mn;
       }
       const int64_t slot = (int64_t)(b * p.Hkv + g) + blockIdx.x;
-      const int64_t rec = (slot * kMaxSlices + 0) * p.rows + rr;
+      const int64_t rec = slot * p.rows + rr;
       if (lane == 0) p.part_ml[rec] = make_float2(m, l);
 #pragma unroll
       for (int i = 0; i < PER; ++i) p.part_o[rec * D + lane + 32 * i] = acc[i];
@@ -334,7 +530,29 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ merge kernel
-// grid (segments, ceil(rows / 4)); one warp per query row of a segment.
+// Element `i` of a row of q, k_new or v_new as fp32.
+__device__ __forceinline__ float load_elem(const void* base, int64_t off, int bf16) {
+  return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[off])
+              : reinterpret_cast<const float*>(base)[off];
+}
+
+// Vector of PER consecutive fp32 values (PER = 2 or 4), one 8- or 16-byte load.
+template <int PER>
+__device__ __forceinline__ void load_vec(const float* src, float (&v)[PER]) {
+  if constexpr (PER == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    v[0] = t.x; v[1] = t.y;
+  }
+}
+
+// grid (segments, ceil(rows / 4)); one warp per query row of a segment, lane l owning head-dim
+// elements [l * D/32, (l + 1) * D/32).  The records of a row (parts x key slices) are read
+// lane-parallel: lane i fetches record i's (m, l), and the weighted sum of the o vectors issues
+// its loads independently of one another, so the merge costs a few memory latencies, not one
+// per record.
 template <int D>
 __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
   constexpr int PER = D / 32;
@@ -344,80 +562,135 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
   if (r >= p.rows) return;
   const int b = s / p.Hkv, g = s % p.Hkv;
   int64_t total, cum_b;
-  warp_scan_lengths(p, b, total, cum_b);
+  warp_scan_tiles(p, b, total, cum_b);
   const int len = seg_len(p, b);
+  const int j = r / p.G, h = g * p.G + r % p.G;
+  const int e0 = lane * PER;
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   if (len > 0) {
-    const int64_t per = keys_per_cta(p, total);
-    const int64_t start = cum_b + (int64_t)g * len;
-    const int c0 = (int)(start / per), c1 = (int)((start + len - 1) / per);
+    const int ntiles = seg_tiles(len);
+    const int64_t per = tiles_per_cta(p, total);
+    const int64_t start = cum_b + (int64_t)g * ntiles;
+    const int c0 = (int)(start / per), c1 = (int)((start + ntiles - 1) / per);
     const int nks = p.nks;
+    const int nrec = (c1 - c0 + 1) * nks;  // per CTA that took part of the segment: one per key slice
+    auto rec_of = [&](int i) -> int64_t { return ((int64_t)(s + c0 + i / nks) * nks + i % nks) * p.rows + r; };
     float M = neg_inf();
-    for (int c = c0; c <= c1; ++c)
-      for (int ks = 0; ks < nks; ++ks) M = fmaxf(M, p.part_ml[((int64_t)(s + c) * kMaxSlices + ks) * p.rows + r].x);
+    for (int i = lane; i < nrec; i += 32) M = fmaxf(M, p.part_ml[rec_of(i)].x);
+    M = warp_max(M);
+    // the window's new key: score q . k_new (log2 units), weight 1 relative to itself
+    float s_new = neg_inf(), kn[PER], vn[PER];
+    if (p.has_new) {
+      const int64_t qo = (int64_t)b * p.q_sb + (int64_t)j * p.q_st + (int64_t)h * p.q_sh + e0;
+      const int64_t no = (int64_t)b * p.new_sb + (int64_t)g * p.new_sh + e0;
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        kn[i] = load_elem(p.k_new, no + i, p.kv_bf16);
+        vn[i] = load_elem(p.v_new, no + i, p.kv_bf16);
+        dot = fmaf(load_elem(p.q, qo + i, p.kv_bf16), kn[i], dot);
+      }
+      s_new = warp_sum(dot) * p.scale_log2;
+      M = fmaxf(M, s_new);
+    }
     float L = 0.f;
     if (M != neg_inf()) {
-      for (int c = c0; c <= c1; ++c) {
-        for (int ks = 0; ks < nks; ++ks) {
-          const int64_t rec = ((int64_t)(s + c) * kMaxSlices + ks) * p.rows + r;
-          const float2 ml = p.part_ml[rec];
-          if (ml.x == neg_inf()) continue;
-          const float wgt = exp2f(ml.x - M);
-          L = fmaf(wgt, ml.y, L);
-          const float* po = p.part_o + rec * D;
-#pragma unroll
-          for (int i = 0; i < PER; ++i) acc[i] = fmaf(wgt, po[lane + 32 * i], acc[i]);
+      for (int i0 = 0; i0 < nrec; i0 += 32) {
+        float wgt = 0.f, lw = 0.f;
+        if (i0 + lane < nrec) {
+          const float2 ml = p.part_ml[rec_of(i0 + lane)];
+          wgt = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
+          lw = wgt * ml.y;
         }
+        L += warp_sum(lw);
+        const int n = min(32, nrec - i0);
+#pragma unroll 4
+        for (int t = 0; t < n; ++t) {
+          const float wt = __shfl_sync(0xffffffffu, wgt, t);
+          float v[PER];
+          load_vec<PER>(p.part_o + rec_of(i0 + t) * D + e0, v);
+#pragma unroll
+          for (int i = 0; i < PER; ++i) acc[i] = fmaf(wt, v[i], acc[i]);
+        }
+      }
+      if (p.has_new) {
+        const float wgt = exp2f(s_new - M);
+        L += wgt;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = fmaf(wgt, vn[i], acc[i]);
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] *= inv;
+    if (p.has_new && r == 0) {
+      // every partial kernel has finished reading the ring (stream order): store the new key
+      const int slot = (__ldg(p.lens + b) - 1) % p.Lmax;
+      const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * D + e0;
+      if (p.kv_bf16) {
+        __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.k)) + dst;
+        __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.v)) + dst;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          kr[i] = __float2bfloat16_rn(kn[i]);  // exact: the value came from bf16
+          vr[i] = __float2bfloat16_rn(vn[i]);
+        }
+      } else {
+        float* kr = reinterpret_cast<float*>(const_cast<void*>(p.k)) + dst;
+        float* vr = reinterpret_cast<float*>(const_cast<void*>(p.v)) + dst;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          kr[i] = kn[i];
+          vr[i] = vn[i];
+        }
+      }
+    }
   } else if (lane == 0 && g == 0 && r == 0) {
     atomicOr(p.status, p.is_window ? (uint32_t)SPEC_STATUS_BAD_POS : (uint32_t)SPEC_STATUS_BAD_KV_LEN);
   }
-  const int j = r / p.G, h = g * p.G + r % p.G;
-  const int64_t off = (int64_t)b * p.o_sb + (int64_t)j * p.o_st + (int64_t)h * p.o_sh;
+  const int64_t off = (int64_t)b * p.o_sb + (int64_t)j * p.o_st + (int64_t)h * p.o_sh + e0;
   if (p.o_bf16) {
     __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o) + off;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) ob[lane + 32 * i] = __float2bfloat16_rn(acc[i]);
+    for (int i = 0; i < PER; ++i) ob[i] = __float2bfloat16_rn(acc[i]);
   } else {
     float* of = reinterpret_cast<float*>(p.o) + off;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) of[lane + 32 * i] = acc[i];
+    for (int i = 0; i < PER; ++i) of[i] = acc[i];
   }
 }
 
 // ------------------------------------------------------------------ ring append
-__global__ void window_append_kernel(const WindowAppend a) {
-  const int b = blockIdx.x / a.Hkv, g = blockIdx.x % a.Hkv;
-  const int pos = a.pos[b];
+// Separate append, used ahead of the tensor-core partial kernel (which has no replaced-slot mask):
+// one CTA per (sequence, kv head) stores k_new / v_new into ring slot (pos - 1) mod W.
+__global__ void window_append_kernel(const __grid_constant__ AttnParams p) {
+  const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
+  const int pos = p.lens[b];
   if (pos < 1) return;
-  const int slot = (pos - 1) % a.W;
-  const int64_t dst = (int64_t)b * a.ring_sb + (int64_t)g * a.ring_sh + (int64_t)slot * a.D;
-  const int64_t src = (int64_t)b * a.new_sb + (int64_t)g * a.new_sh;
-  if (a.bf16) {
-    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(a.k_new) + src;
-    const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(a.v_new) + src;
-    __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(a.k_ring) + dst;
-    __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(a.v_ring) + dst;
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) { kr[d] = kn[d]; vr[d] = vn[d]; }
+  const int slot = (pos - 1) % p.Lmax;
+  const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * p.D;
+  const int64_t src = (int64_t)b * p.new_sb + (int64_t)g * p.new_sh;
+  if (p.kv_bf16) {
+    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src;
+    const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + src;
+    __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.k)) + dst;
+    __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.v)) + dst;
+    for (int d = threadIdx.x; d < p.D; d += blockDim.x) { kr[d] = kn[d]; vr[d] = vn[d]; }
   } else {
-    const float* kn = reinterpret_cast<const float*>(a.k_new) + src;
-    const float* vn = reinterpret_cast<const float*>(a.v_new) + src;
-    float* kr = reinterpret_cast<float*>(a.k_ring) + dst;
-    float* vr = reinterpret_cast<float*>(a.v_ring) + dst;
-    for (int d = threadIdx.x; d < a.D; d += blockDim.x) { kr[d] = kn[d]; vr[d] = vn[d]; }
+    const float* kn = reinterpret_cast<const float*>(p.k_new) + src;
+    const float* vn = reinterpret_cast<const float*>(p.v_new) + src;
+    float* kr = reinterpret_cast<float*>(const_cast<void*>(p.k)) + dst;
+    float* vr = reinterpret_cast<float*>(const_cast<void*>(p.v)) + dst;
+    for (int d = threadIdx.x; d < p.D; d += blockDim.x) { kr[d] = kn[d]; vr[d] = vn[d]; }
   }
 }
 
 // ------------------------------------------------------------------ host side
 size_t attn_workspace_bytes(int segments, int rows, int D) {
   const size_t slots = (size_t)segments + kMaxGridX;
-  const size_t recs = slots * kMaxSlices * (size_t)rows;
+  const size_t recs = slots * kConsumerWarps * (size_t)rows;  // up to kConsumerWarps key slices
   size_t bytes = 256;                                   // status word + padding
   bytes += (recs * sizeof(float2) + 255) / 256 * 256;   // (m, l)
   bytes += recs * (size_t)D * sizeof(float);            // unnormalised o
@@ -426,7 +699,7 @@ size_t attn_workspace_bytes(int segments, int rows, int D) {
 
 void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p) {
   const size_t slots = (size_t)segments + kMaxGridX;
-  const size_t recs = slots * kMaxSlices * (size_t)rows;
+  const size_t recs = slots * kConsumerWarps * (size_t)rows;
   uint8_t* base = reinterpret_cast<uint8_t*>(ws);
   p->status = reinterpret_cast<uint32_t*>(base);
   p->part_ml = reinterpret_cast<float2*>(base + 256);
@@ -449,7 +722,10 @@ template <int D, int MASK>
 static cudaError_t launch_bf16_nks(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, dim3 grid,
                                    cudaStream_t stream) {
   switch (p.nks) {
-    case kConsumerWarps / 4: return launch_bf16<D, MASK, kConsumerWarps / 4>(p, tmK, tmV, grid, stream);
+    case kConsumerWarps / 4:
+      // D = 128 row groups above 32 rows take the tensor-core kernel
+      if constexpr (D == 128) return cudaErrorInvalidValue;
+      else return launch_bf16<D, MASK, kConsumerWarps / 4>(p, tmK, tmV, grid, stream);
     case kConsumerWarps / 2: return launch_bf16<D, MASK, kConsumerWarps / 2>(p, tmK, tmV, grid, stream);
     default: return launch_bf16<D, MASK, kConsumerWarps>(p, tmK, tmV, grid, stream);
   }
@@ -494,6 +770,11 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
   if (kv_bf16 && p.D == 128 && p.rows > 32) {
     // dense query blocks: tcgen05 tiles of 128 rows, one CTA per SM (range x row group)
+    if (p.has_new) {
+      window_append_kernel<<<p.B * p.Hkv, 128, 0, stream>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      p.has_new = 0;
+    }
     p.tc_groups = (p.rows + 127) / 128;
     p.rows_per_group = (p.rows + p.tc_groups - 1) / p.tc_groups;
     p.nks = 1;
@@ -508,17 +789,26 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   const int row_groups = (p.rows + kRowsPerGroup - 1) / kRowsPerGroup;
   p.rows_per_group = ((p.rows + row_groups - 1) / row_groups + 15) / 16 * 16;
   p.nks = kv_bf16 ? slices_for_rows(p.rows_per_group) : 1;
+  if (kv_bf16 && p.is_window && row_groups == 1) {
+    // short segments (a ring of W keys): whole segments per CTA, no merge pass, as long as that
+    // does not put many more tiles on a CTA than the even split would
+    const int64_t S = (int64_t)p.B * p.Hkv;
+    const int64_t spc = (S + sms - 1) / sms;
+    const int64_t seg_tiles = (p.Lmax + kKeyTile - 1) / kKeyTile;
+    const int64_t even = (S * seg_tiles + sms - 1) / sms;
+    if (spc * seg_tiles <= (2 * even > 16 ? 2 * even : 16)) {
+      p.direct = 1;
+      p.segs_per_cta = (int)spc;
+      p.grid_x = (int)((S + spc - 1) / spc);
+    }
+  }
   dim3 grid(p.grid_x, row_groups);
   e = (p.D == 64) ? launch_partial<64>(p, tmK, tmV, kv_bf16, grid, stream)
                   : launch_partial<128>(p, tmK, tmV, kv_bf16, grid, stream);
   if (e != cudaSuccess) return e;
+  if (p.direct) return cudaSuccess;
   if (p.D == 64) attn_merge<64><<<mgrid, 128, 0, stream>>>(p);
   else attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_window_append(const WindowAppend& a, cudaStream_t stream) {
-  window_append_kernel<<<a.B * a.Hkv, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -18,10 +18,8 @@ constexpr int kRowsPerGroup = 64;
 // Upper bound on CTAs along the key axis (two per SM on a 160-SM part); the workspace is sized
 // for it and launches never exceed it.
 constexpr int kMaxGridX = 320;
-// Minimum keys a CTA takes, so that short total work does not spread over every SM.
-constexpr int kMinKeysPerCta = 256;
-// Key slices per row tile: consumer warps / row tiles, at most 8.
-constexpr int kMaxSlices = 8;
+// Minimum 128-key tiles a CTA takes, so that short total work does not spread over every SM.
+constexpr int kMinTilesPerCta = 2;
 
 enum MaskMode : int { kMaskNone = 0, kMaskChain = 1, kMaskTree = 2 };
 
@@ -44,22 +42,21 @@ struct AttnParams {
   int grid_x;                      // CTAs along the key axis (same value in partial and merge)
   int rows_per_group;              // query rows per CTA row group (blockIdx.y), <= kRowsPerGroup
   int nks;                         // key slices per row tile (bf16 path), same for every row group
+  int direct;                      // bf16 path: each CTA owns whole segments and writes o itself
+  int segs_per_cta;                // direct mode: segments per CTA
   int tc_groups;                   // tensor-core path: row groups per key range (CTA = range x group)
-  float* part_o;                   // [slots][kMaxSlices][rows][D]
-  float2* part_ml;                 // [slots][kMaxSlices][rows]  (m in log2 units, l)
+  float* part_o;                   // [slots][nks][rows][D]  (slot = segment + CTA index)
+  float2* part_ml;                 // [slots][nks][rows]  (m in log2 units, l)
   uint32_t* status;
-  unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
-};
-
-struct WindowAppend {
-  int B, Hkv, D, W, bf16;
-  const int32_t* pos;
-  void* k_ring;
-  void* v_ring;
-  int64_t ring_sb, ring_sh;
+  // window with a fused ring append: the partial kernels mask ring slot (pos - 1) mod W (about
+  // to be overwritten) and the merge kernel adds the new key (k_new, v_new) to the softmax and
+  // stores it into that slot.  has_new = 0: no append.
+  int has_new;
+  int kv_bf16;                     // q, k_new, v_new element type (same as the cache)
   const void* k_new;
   const void* v_new;
   int64_t new_sb, new_sh;
+  unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
 };
 
 // Workspace layout for the attention kernels (bytes), for a given number of segments and rows.
@@ -69,7 +66,6 @@ void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p
 // Launch helpers; return a cudaError_t.  tmK/tmV are used by the bf16 path only.
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
                              cudaStream_t stream);
-cudaError_t launch_window_append(const WindowAppend& a, cudaStream_t stream);
 
 // tcgen05 partial kernel (attn_tc.cu): D = 128, bf16, up to 128 query rows per row group.
 cudaError_t launch_partial_tc(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,

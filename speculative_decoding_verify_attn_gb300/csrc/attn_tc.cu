@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::fence_after();
       {
         const int64_t slot = (int64_t)(cb * p.Hkv + cg) + cta;
-        const int64_t rec = (slot * kMaxSlices) * p.rows + rr;
+        const int64_t rec = slot * p.rows + rr;
         uint32_t u[32];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {

@@ -28,8 +28,11 @@ def _run(sv, q, kr, vr, pos, kn, vn, dtype):
     return to_np(o), sv.read_status(ws)
 
 
-@pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("f32", 64, 4, 1), ("bf16", 64, 8, 2)])
+@pytest.mark.parametrize("dtype,D,Hq,Hkv", [("bf16", 128, 32, 8), ("f32", 64, 4, 1), ("bf16", 64, 8, 2),
+                                            ("bf16", 128, 24, 1), ("bf16", 128, 64, 1), ("f32", 128, 8, 8)])
 def test_window_with_append_many_positions(sv, dtype, D, Hq, Hkv):
+    """Group sizes 4..64 cover every partial kernel: mma.sync with 8, 4 and 2 key slices per
+    tile, the fp32 kernel, and the tensor-core kernel (64 rows, separate append)."""
     W = 512
     pos = np.array([1, 100, 511, 512, 513, 1800, 70000], dtype=np.int32)
     B = len(pos)
@@ -42,12 +45,14 @@ def test_window_with_append_many_positions(sv, dtype, D, Hq, Hkv):
     assert st == 0
     assert_attn_close(o, ref, dtype, what="window")
     # the append wrote the current token's slot and nothing else
-    kr_np = to_np(kr)
+    kr_np, vr_np = to_np(kr), to_np(vr)
     for b in range(B):
         s = (pos[b] - 1) % W
         assert np.array_equal(kr_np[b, :, s], k_after[b, :, s].astype(np.float32))
+        assert np.array_equal(vr_np[b, :, s], v_after[b, :, s].astype(np.float32))
         other = [t for t in oa.window_slots(int(pos[b]), W) if t != s]
         assert np.array_equal(kr_np[b][:, other], inp["k_ring"][b][:, other])
+        assert np.array_equal(vr_np[b][:, other], inp["v_ring"][b][:, other])
 
 
 def test_magicdec_draft_round_four_steps(sv):
@@ -105,3 +110,27 @@ def test_window_covering_context_equals_verify(sv):
     sv.spec_verify_attn(q4, to_dev(kr, "bf16"), to_dev(vr, "bf16"), to_dev(pos, "i32"), o_ver)
     torch.cuda.synchronize()
     assert np.max(np.abs(o_win - to_np(o_ver)[:, 0])) <= 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_window_long_ring_split_over_ctas(sv, dtype):
+    """A ring far longer than a CTA's share (W = 6000, one kv head) is split over many CTAs and
+    merged; the new key then enters through the merge.  pos = 0 marks a bad sequence."""
+    W, D, Hq, Hkv = 6000, 128, 4, 1
+    pos = np.array([9001, 0, 4321], dtype=np.int32)
+    inp = gen.window_inputs(3, Hq, Hkv, D, W, np.maximum(pos, 1), dtype, seed=21)
+    q, kr, vr = to_dev(inp["q"], dtype), to_dev(inp["k_ring"], dtype), to_dev(inp["v_ring"], dtype)
+    kn, vn = to_dev(inp["k_new"], dtype), to_dev(inp["v_new"], dtype)
+    o, st = _run(sv, q, kr, vr, to_dev(pos, "i32"), kn, vn, dtype)
+    assert st & 2, "SPEC_STATUS_BAD_POS expected for pos = 0"
+    assert np.all(o[1] == 0.0)
+    keep = [0, 2]
+    ref, k_after, _ = oa.draft_window_attn(inp["q"][keep], inp["k_ring"][keep], inp["v_ring"][keep], pos[keep],
+                                           inp["k_new"][keep], inp["v_new"][keep])
+    assert_attn_close(o[keep], ref, dtype, what="long ring")
+    kr_np = to_np(kr)
+    for i, b in enumerate(keep):
+        s = (pos[b] - 1) % W
+        assert np.array_equal(kr_np[b, :, s], k_after[i, :, s].astype(np.float32))
+    # the bad sequence's ring is untouched
+    assert np.array_equal(kr_np[1], inp["k_ring"][1].astype(np.float32), equal_nan=True)
