@@ -777,7 +777,7 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
     }
     p.tc_groups = (p.rows + 127) / 128;
     p.rows_per_group = (p.rows + p.tc_groups - 1) / p.tc_groups;
-    p.nks = 1;
+    p.nks = kTcSlices;
     p.grid_x = sms / p.tc_groups > 0 ? sms / p.tc_groups : 1;
     if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
     e = launch_partial_tc(p, tmK, tmV, stream);

@@ -67,7 +67,9 @@ void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
                              cudaStream_t stream);
 
-// tcgen05 partial kernel (attn_tc.cu): D = 128, bf16, up to 128 query rows per row group.
+// tcgen05 partial kernel (attn_tc.cu): D = 128, bf16, up to 128 query rows per row group; two
+// softmax warpgroups on alternate tiles, so each part leaves kTcSlices records.
+constexpr int kTcSlices = 2;
 cudaError_t launch_partial_tc(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
                               cudaStream_t stream);
 size_t attn_tc_smem_bytes();
