@@ -1,25 +1,25 @@
 // The speculative-sampling step over the vocabulary, and greedy chain / tree selection.
 //
 // Large vocabularies (V > kSmallVocab):
-//   K1 sample_stats     grid (chunks, rows, B): every target and draft row is split into
-//                       vocabulary chunks; each CTA reads its chunk once with 128-bit loads and
-//                       writes the chunk max M_c and S_c = sum exp(x - M_c) (fp32 exp2f of the
-//                       scaled difference, compensated fp32 per thread, float-float across the
-//                       warp, fp64 across warps) -- or, in greedy modes, the chunk argmax.  The last
-//                       CTA of a sequence to finish (atomic ticket, no spinning) merges its rows'
-//                       statistics (fp64) and takes every accept decision at once (one lane per
-//                       draft, fp64 exponentials of the two selected logits); greedy modes finish
-//                       there (argmax merge + chain or tree rule).
-//   K2 sample_residual  grid (chunks, B), stochastic chain only: each CTA sums the residual
-//                       max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its chunk; the last CTA of
-//                       the sequence finds the chunk where the cumulative residual passes u * R,
-//                       re-scans that one chunk and writes the emitted tokens.
+//   sample_stats         persistent, warp-granular: every target and draft row is cut into items of
+//                        1024 logits; per item the max M_c and S_c = sum exp(x - M_c) (fp32 exp2f of
+//                        the scaled difference, compensated fp32 per lane, float-float across the
+//                        warp) -- or, in greedy modes, the item argmax.
+//   sample_chain_finish  stochastic chain: one thread-block cluster per sequence.  Every CTA of the
+//                        cluster merges the sequence's item statistics (fp64) and takes the accept
+//                        decisions (one lane per draft); then CTA c computes the residual
+//                        max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its share of the vocabulary
+//                        in 512-element slabs, the CTAs exchange their residual masses through
+//                        distributed shared memory, and the CTA whose share holds u * R finds its
+//                        slab and re-scans it for the emitted token.
+//   sample_finalize      greedy modes: argmax merge and the chain or tree rule, one CTA per sequence.
 // Small vocabularies: one warp per sequence runs the whole step (the 16-token chi-square
 // workload runs 10^6 sequences at once).
 //
 // Every sum that decides a token is reproducible: fixed element orders, compensated fp32 per
 // thread (Kahan), float-float (Knuth's TwoSum) inside a warp, fp64 above that, no floating-point
 // atomics.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <limits.h>
 
@@ -110,6 +110,50 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
   const float hi = __fadd_rn(s, t);
   return FF{hi, __fsub_rn(t, __fsub_rn(hi, s))};
 }
+__device__ __forceinline__ FF ff_neg(FF a) { return FF{-a.hi, -a.lo}; }
+// a * b for float-float a and float b: the exact product of the high parts (FMA) plus the low
+// part's product, renormalised
+__device__ __forceinline__ FF ff_mul_f(FF a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  const float e = __fmaf_rn(a.hi, b, -p);
+  const float t = __fmaf_rn(a.lo, b, e);
+  const float hi = __fadd_rn(p, t);
+  return FF{hi, __fsub_rn(t, __fsub_rn(hi, p))};
+}
+// a > b (the sign of the float-float difference)
+__device__ __forceinline__ bool ff_gt(FF a, FF b) {
+  const FF d = ff_add(a, ff_neg(b));
+  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+__device__ __forceinline__ FF shfl_ff(FF v, int src) {
+  return FF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ FF shfl_up_ff(FF v, int o) {
+  return FF{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+// Warp sum of float-float values, in a fixed tree order; every lane returns lane 0's result.
+__device__ __forceinline__ FF warp_sum_ff(FF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    FF w;
+    w.hi = __shfl_down_sync(0xffffffffu, v.hi, o);
+    w.lo = __shfl_down_sync(0xffffffffu, v.lo, o);
+    if (lane < o) v = ff_add(v, w);
+  }
+  return shfl_ff(v, 0);
+}
+// Inclusive warp scan of float-float values in lane order.
+__device__ __forceinline__ FF warp_scan_ff(FF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const FF t = shfl_up_ff(v, o);
+    if (lane >= o) v = ff_add(t, v);
+  }
+  return v;
+}
+
 // Block sum of per-thread float-float values: warps reduce in float-float, then thread 0 adds the
 // warp results in fp64 in warp order.  The result is valid in thread 0.
 __device__ double block_sum_ff(FF v, FF* red) {
@@ -142,20 +186,56 @@ __device__ __forceinline__ const float* drow(const SampleParams& p, int b, int i
 // sM / sZ hold the row max and normaliser: target row i at i, draft row i at rows_t + i.
 // Whole warp: lane i takes draft i (gamma <= 32); the first failing lane is found with a ballot.
 // P_i(x_i) and Q_i(x_i) use fp64 exponentials of the two selected logits.  Every lane returns k.
-__device__ int chain_decide_warp(const SampleParams& p, int b, const float* sM, const double* sZ) {
+__device__ int chain_decide_warp(const SampleParams& p, int b, const float* sM, const double* sZ,
+                                 bool use_sel = false) {
   const int i = threadIdx.x & 31;
   bool bad = false, acc = true;
   if (i < p.gamma) {
     const int x = p.tok[(int64_t)b * p.tok_sb + i];
+    // recorded logits are loaded alongside the token (their slots do not depend on it)
+    const int rows = p.rows_t + p.rows_d;
+    const float tsel = use_sel ? __ldcg(p.sel + (int64_t)b * rows + i) : 0.f;
+    const float dsel = use_sel ? __ldcg(p.sel + (int64_t)b * rows + p.rows_t + i) : 0.f;
     bad = x < 0 || x >= p.V;
     if (!bad) {
       // u Q(x) < P(x)  <=>  u < P(x) / Q(x) = exp((t_x - M_t) - (d_x - M_d)) * Z_d / Z_t
       // (the differences are exact in fp64; one fp64 exponential per draft)
-      const double dt = (double)trow(p, b, i)[x] - (double)sM[i];
-      const double dd = (double)drow(p, b, i)[x] - (double)sM[p.rows_t + i];
+      const float tx = use_sel ? tsel : trow(p, b, i)[x];
+      const float dx = use_sel ? dsel : drow(p, b, i)[x];
+      const double dt = (double)tx - (double)sM[i];
+      const double dd = (double)dx - (double)sM[p.rows_t + i];
       const double ratio = exp(dt - dd) * (sZ[p.rows_t + i] / sZ[i]);
       const double uu = (double)p.u[(int64_t)b * p.u_sb + i];
       acc = uu < ratio;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) return -1;
+  const unsigned rej = __ballot_sync(0xffffffffu, i < p.gamma && !acc);
+  return rej ? __ffs(rej) - 1 : p.gamma;
+}
+
+// The same decisions from float-float row normalisers and the logits the statistics pass
+// recorded, in fp32 arithmetic only: the exponent (t_x - M_t) - (d_x - M_d) is formed exactly as a
+// float-float, and the ratio exp(e) * Z_d / Z_t carries a relative error of a few 1e-7, far inside
+// the 1e-6 band around each threshold.  u = 0 accepts (P(x) > 0 for every token).
+__device__ int chain_decide_warp_ff(const SampleParams& p, int b, const float* sM, const FF* sZ) {
+  const int i = threadIdx.x & 31;
+  bool bad = false, acc = true;
+  if (i < p.gamma) {
+    const int rows = p.rows_t + p.rows_d;
+    const int x = p.tok[(int64_t)b * p.tok_sb + i];
+    const float tx = __ldcg(p.sel + (int64_t)b * rows + i);
+    const float dx = __ldcg(p.sel + (int64_t)b * rows + p.rows_t + i);
+    const float uu = p.u[(int64_t)b * p.u_sb + i];
+    bad = x < 0 || x >= p.V;
+    if (!bad) {
+      const FF dt = ff_add(FF{tx, 0.f}, FF{-sM[i], 0.f});
+      const FF dd = ff_add(FF{dx, 0.f}, FF{-sM[p.rows_t + i], 0.f});
+      const FF e = ff_add(dt, ff_neg(dd));
+      const FF zt = sZ[i], zd = sZ[p.rows_t + i];
+      const float zr = __fdiv_rn(zd.hi, zt.hi) * (1.f + (__fdiv_rn(zd.lo, zd.hi) - __fdiv_rn(zt.lo, zt.hi)));
+      const float ratio = expf(e.hi) * (1.f + e.lo) * zr;
+      acc = uu == 0.f || uu < ratio;
     }
   }
   if (__any_sync(0xffffffffu, bad)) return -1;
@@ -274,7 +354,26 @@ __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_cons
       }
       if (lane == 0) {
         p.st_m[it] = m;
-        p.st_s[it] = (double)v.hi + (double)v.lo;
+        p.st_s[it] = make_float2(v.hi, v.lo);
+      }
+      // the draft token of this row, if it falls in this item: record its logit for the accept test
+      if (p.mode == SPEC_SAMPLE_CHAIN) {
+        int base;
+        src_of(it, base);
+        const int b = it / per_seq;
+        const int r = (it - b * per_seq) / p.schunks;
+        const int ti = r < p.rows_t ? r : r - p.rows_t;
+        if (ti < p.gamma) {
+          const int off = __ldg(p.tok + (int64_t)b * p.tok_sb + ti) - base;
+          if ((unsigned)off < (unsigned)kStatChunk && lane == ((off & 127) >> 2)) {
+            const int q = off >> 7, j = off & 3;
+            float val = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+              if (i == q) val = j == 0 ? x[i].x : (j == 1 ? x[i].y : (j == 2 ? x[i].z : x[i].w));
+            p.sel[(int64_t)b * rows + r] = val;
+          }
+        }
       }
     } else {
       int base;
@@ -300,98 +399,91 @@ __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_cons
   }
 }
 
-// One CTA per sequence: merges the chunk statistics of its rows and finishes the sequence --
-// accept decisions and the residual row's statistics (stochastic chain), or the argmax merge and
-// the greedy chain / tree rule.
-template <bool GREEDY>
+// Greedy modes, one CTA per sequence: merges the item argmaxes of its rows and applies the greedy
+// chain or tree rule.
 __global__ void __launch_bounds__(kSampleThreads) sample_finalize(const __grid_constant__ SampleParams p) {
-  __shared__ float sM[2 * kMaxGamma + 1];
-  __shared__ double sZ[2 * kMaxGamma + 1];
   __shared__ int sa[kMaxTreeNodes > kMaxGamma + 1 ? kMaxTreeNodes : kMaxGamma + 1];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = p.rows_t + p.rows_d;
-  if (!GREEDY) {
-    for (int rr = warp; rr < rows; rr += kWarps) {
-      const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
-      float m = neg_inf();
-      for (int cc = lane; cc < p.schunks; cc += 32) m = fmaxf(m, p.st_m[oo + cc]);
-      m = warp_max(m);
-      // item weights exp(M_c - M) in fp32 (exp2f, 2 ulp; M_c - M is exact or far below 0 where
-      // the weight is negligible), products and sums in fp64 in a fixed order
-      double z = 0.0;
-      for (int cc = lane; cc < p.schunks; cc += 32) z += p.st_s[oo + cc] * (double)exp_shift(p.st_m[oo + cc], m);
-      z = warp_sum_d(z);
-      if (lane == 0) { sM[rr] = m; sZ[rr] = z; }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const int k = chain_decide_warp(p, b, sM, sZ);
-      if (lane == 0) {
-        SeqInfo si;
-        si.k = k;
-        si.pad = 0;
-        si.Mt = 0.f; si.Md = 0.f; si.Zt = 1.0; si.Zd = 1.0;
-        if (k >= 0) { si.Mt = sM[k]; si.Zt = sZ[k]; }
-        if (k >= 0 && k < p.gamma) { si.Md = sM[p.rows_t + k]; si.Zd = sZ[p.rows_t + k]; }
-        p.seq[b] = si;
-        if (k < 0) write_chain_out(p, b, -1, -1);
+  for (int rr = warp; rr < rows; rr += kWarps) {
+    const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
+    float v = neg_inf();
+    int i = INT_MAX;
+    for (int cc = lane; cc < p.schunks; cc += 32) argmax_combine(v, i, p.st_m[oo + cc], p.st_arg[oo + cc]);
+    warp_argmax(v, i);
+    if (lane == 0) sa[rr] = i;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (p.mode == SPEC_SAMPLE_TREE_GREEDY) {
+      tree_select_write(p, b, sa);
+    } else {
+      int k = p.gamma;
+      for (int i = 0; i < p.gamma; ++i) {
+        const int xi = p.tok[(int64_t)b * p.tok_sb + i];
+        if (xi < 0 || xi >= p.V) { k = -1; break; }
       }
-    }
-  } else {
-    for (int rr = warp; rr < rows; rr += kWarps) {
-      const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
-      float v = neg_inf();
-      int i = INT_MAX;
-      for (int cc = lane; cc < p.schunks; cc += 32) argmax_combine(v, i, p.st_m[oo + cc], p.st_arg[oo + cc]);
-      warp_argmax(v, i);
-      if (lane == 0) sa[rr] = i;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      if (p.mode == SPEC_SAMPLE_TREE_GREEDY) {
-        tree_select_write(p, b, sa);
-      } else {
-        int k = p.gamma;
-        for (int i = 0; i < p.gamma; ++i) {
-          const int xi = p.tok[(int64_t)b * p.tok_sb + i];
-          if (xi < 0 || xi >= p.V) { k = -1; break; }
-        }
-        if (k >= 0)
-          for (int i = 0; i < p.gamma; ++i)
-            if (p.tok[(int64_t)b * p.tok_sb + i] != sa[i]) { k = i; break; }
-        write_chain_out(p, b, k, k >= 0 ? sa[k] : -1);
-      }
+      if (k >= 0)
+        for (int i = 0; i < p.gamma; ++i)
+          if (p.tok[(int64_t)b * p.tok_sb + i] != sa[i]) { k = i; break; }
+      write_chain_out(p, b, k, k >= 0 ? sa[k] : -1);
     }
   }
 }
 
-// Residual of four consecutive elements starting at idx (idx < V, V % 4 == 0).
-__device__ __forceinline__ float4 resid4(const float* tr, const float* dr, int idx, float Mt, float iZt, float Md,
-                                         float iZd, bool has_d) {
-  const float4 tv = __ldcs(reinterpret_cast<const float4*>(tr + idx));
-  float4 dv = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (has_d) dv = __ldcs(reinterpret_cast<const float4*>(dr + idx));
-  return make_float4(resid(tv.x, dv.x, Mt, iZt, Md, iZd, has_d), resid(tv.y, dv.y, Mt, iZt, Md, iZd, has_d),
-                     resid(tv.z, dv.z, Mt, iZt, Md, iZd, has_d), resid(tv.w, dv.w, Mt, iZt, Md, iZd, has_d));
-}
+// ------------------------------------------------------------------ stochastic chain finish
+constexpr int kFinThreads = 512;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kSlab = 512;  // residual slab: lane l takes elements 4l..4l+3 of each 128-element quarter
 
-// Residual mass of one warp slice of a chunk: warp w of the chunk covers 32 * EPT elements in
-// slabs of 128 (lane l takes elements 4l..4l+3 of each slab).  Returns the warp's sum (valid in
-// lane 0, float-float reduced) and the last index with positive residual (all lanes).
-template <int EPT>
-__device__ __forceinline__ double warp_slice_residual(const float* tr, const float* dr, int start, int V, float Mt,
-                                                      float iZt, float Md, float iZd, bool has_d, int& last) {
+// This lane's 16 logits of target and draft row in the slab starting at `base` (0 past V).
+struct SlabData {
+  float4 tv[4], dv[4];
+};
+__device__ __forceinline__ void slab_load(const float* tr, const float* dr, int base, int V, bool has_d, SlabData& D) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int idx = base + j * 128 + lane * 4;
+    D.tv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    D.dv[j] = D.tv[j];
+    if (idx < V) {
+      D.tv[j] = __ldcg(reinterpret_cast<const float4*>(tr + idx));
+      if (has_d) D.dv[j] = __ldcg(reinterpret_cast<const float4*>(dr + idx));
+    }
+  }
+}
+// Residual of this lane's 16 elements of the slab starting at `base` (0 past V; V % 4 == 0).
+__device__ __forceinline__ void slab_compute(const SlabData& D, int base, int V, float Mt, float iZt, float Md,
+                                             float iZd, bool has_d, float (&r)[16]) {
+  const int lane = threadIdx.x & 31;
+  const float4* tv = D.tv;
+  const float4* dv = D.dv;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int idx = base + j * 128 + lane * 4;
+    const bool in = idx < V;
+    r[4 * j + 0] = in ? resid(tv[j].x, dv[j].x, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 1] = in ? resid(tv[j].y, dv[j].y, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 2] = in ? resid(tv[j].z, dv[j].z, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 3] = in ? resid(tv[j].w, dv[j].w, Mt, iZt, Md, iZd, has_d) : 0.f;
+  }
+}
+__device__ __forceinline__ void slab_resid(const float* tr, const float* dr, int base, int V, float Mt, float iZt,
+                                           float Md, float iZd, bool has_d, float (&r)[16]) {
+  SlabData D;
+  slab_load(tr, dr, base, V, has_d, D);
+  slab_compute(D, base, V, Mt, iZt, Md, iZd, has_d, r);
+}
+// One slab's residual mass (compensated fp32 per lane, float-float across the warp; lane 0) and
+// the largest index with positive residual (folded into `last`).
+__device__ __forceinline__ FF slab_mass(const float (&r)[16], int base, int& last) {
   const int lane = threadIdx.x & 31;
   Kahan ks;
-  last = -1;
 #pragma unroll
-  for (int i = 0; i < EPT / 4; ++i) {
-    const int idx = start + i * 128 + lane * 4;
-    if (idx < V) {
-      const float4 r = resid4(tr, dr, idx, Mt, iZt, Md, iZd, has_d);
-      ks.add(r.x); ks.add(r.y); ks.add(r.z); ks.add(r.w);
-      last = r.w > 0.f ? idx + 3 : (r.z > 0.f ? idx + 2 : (r.y > 0.f ? idx + 1 : (r.x > 0.f ? idx : last)));
-    }
+  for (int e = 0; e < 16; ++e) {
+    ks.add(r[e]);
+    if (r[e] > 0.f) last = max(last, base + (e >> 2) * 128 + lane * 4 + (e & 3));
   }
   FF v{ks.s, -ks.c};
 #pragma unroll
@@ -401,160 +493,234 @@ __device__ __forceinline__ double warp_slice_residual(const float* tr, const flo
     w.lo = __shfl_down_sync(0xffffffffu, v.lo, o);
     if (lane < o) v = ff_add(v, w);
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  return (double)v.hi + (double)v.lo;
+  return v;
+}
+// Warp 0: slab masses of this CTA in token order, lane l owning slabs [l * pp, (l + 1) * pp):
+// its sequential float-float sum and the inclusive scan over lanes (fixed order, so every call
+// with the same masses returns the same values).
+__device__ __forceinline__ void slab_scan(const FF* s_slab, int ns, FF& lsum, FF& incl) {
+  const int lane = threadIdx.x & 31;
+  const int pp = (ns + 31) / 32;
+  lsum = FF{0.f, 0.f};
+  for (int j = 0; j < pp; ++j) {
+    const int sl = lane * pp + j;
+    if (sl < ns) lsum = ff_add(lsum, s_slab[sl]);
+  }
+  incl = warp_scan_ff(lsum);
 }
 
-// Residual pass (stochastic chain): grid (chunks, B).  Each warp sums its slice of the chunk; the
-// last CTA of the sequence walks the slice sums in token order to the slice where the cumulative
-// residual passes u * R and re-scans that slice (1024 elements for 8192-element chunks) with one
-// warp, slab by slab, with an fp64 warp scan.
-template <int EPT>
-__global__ void __launch_bounds__(kSampleThreads, 4) sample_residual(const __grid_constant__ SampleParams p) {
-  __shared__ int s_last;
-  __shared__ int s_y;
-  const int c = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slice = 32 * EPT;                 // elements per warp slice
-  const int nslices = p.nchunks * kWarps;
-  double* wsum = p.res_sum + (int64_t)b * nslices;
-  int32_t* wlast = p.res_last + (int64_t)b * nslices;
+// Stochastic chain: grid B * CS CTAs in clusters of CS (one cluster per sequence).  Every CTA
+// merges the item statistics of the sequence's rows and decides k (identical in every CTA: same
+// inputs, same order); CTA `rank` then takes slabs [rank * per, (rank + 1) * per) of the residual
+// row and records each slab's mass in shared memory (compensated fp32 per lane, float-float across
+// the warp) and its own total.  After a cluster barrier one warp reads the CS totals through
+// distributed shared memory in rank order, so every CTA agrees on R and on each CTA's prefix; the
+// CTA whose [prefix, prefix + total) holds u * R scans its slab masses, re-reads the slab that
+// passes the threshold and scans it element by element.  All of it in float-float (no fp64).
+// Every CTA takes the same cluster barriers (the decisions that steer them are identical across
+// the cluster).
+__global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __grid_constant__ SampleParams p) {
+  namespace cg = cooperative_groups;
+  extern __shared__ FF s_slab[];      // residual mass of each of this CTA's slabs
+  __shared__ float sM[2 * kMaxGamma + 1];
+  __shared__ FF sZ[2 * kMaxGamma + 1];
+  __shared__ int s_k;
+  __shared__ FF s_total;              // this CTA's residual mass (read by the whole cluster)
+  __shared__ int s_last;              // largest index with positive residual in this CTA's share
+  __shared__ int s_lastw[kFinWarps];
+  __shared__ FF s_R, s_cum;           // the cluster's total and this CTA's prefix
+  cg::cluster_group cl = cg::this_cluster();
+  const int CS = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const int b = blockIdx.x / CS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows = p.rows_t + p.rows_d;
 
-  const int k = __ldcg(&p.seq[b].k);
-  if (k < 0) return;  // invalid token: the statistics pass already wrote the row
-  bool has_d = k < p.gamma;
-  const float* tr = trow(p, b, k);
+  // ---- row statistics and accept decisions.  A warp merges a row's items 256 at a time, each
+  // lane's (M_c, S_c) loaded together before any is used (one L2 round trip per 256 items).
+  const float2* st_s = p.st_s;
+  for (int rr = warp; rr < rows; rr += kFinWarps) {
+    const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
+    float m = neg_inf();
+    FF z{0.f, 0.f};
+    for (int c0 = 0; c0 < p.schunks; c0 += 256) {
+      float mc[8];
+      float2 sc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int cc = c0 + j * 32 + lane;
+        mc[j] = cc < p.schunks ? __ldcg(p.st_m + oo + cc) : neg_inf();
+        sc[j] = cc < p.schunks ? __ldcg(st_s + oo + cc) : make_float2(0.f, 0.f);
+      }
+      float mb = neg_inf();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mb = fmaxf(mb, mc[j]);
+      mb = warp_max(mb);
+      // item weights exp(M_c - M) in fp32 (exp2f, 2 ulp; M_c - M is exact or far below 0 where the
+      // weight is negligible), products and sums in float-float in a fixed order
+      const float mn = fmaxf(m, mb);
+      FF zb{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (mc[j] != neg_inf()) zb = ff_add(zb, ff_mul_f(FF{sc[j].x, sc[j].y}, exp_shift(mc[j], mn)));
+      zb = warp_sum_ff(zb);
+      z = ff_add(m == neg_inf() ? FF{0.f, 0.f} : ff_mul_f(z, exp_shift(m, mn)), zb);
+      m = mn;
+    }
+    if (lane == 0) { sM[rr] = m; sZ[rr] = z; }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int kk = chain_decide_warp_ff(p, b, sM, sZ);
+    if (lane == 0) s_k = kk;
+  }
+  __syncthreads();
+  const int k = s_k;
+
+  const int nslabs = (p.V + kSlab - 1) / kSlab;
+  const int per = (nslabs + CS - 1) / CS;
+  const int s0 = min(nslabs, rank * per), s1 = min(nslabs, s0 + per);
+  bool has_d = k >= 0 && k < p.gamma;
+  const float* tr = trow(p, b, k >= 0 ? k : 0);
   const float* dr = has_d ? drow(p, b, k) : tr;
-  const float Mt = __ldcg(&p.seq[b].Mt);
-  const float iZt = (float)(1.0 / __ldcg(&p.seq[b].Zt));
-  const float Md = has_d ? __ldcg(&p.seq[b].Md) : 0.f;
-  const float iZd = has_d ? (float)(1.0 / __ldcg(&p.seq[b].Zd)) : 0.f;
+  const float Mt = k >= 0 ? sM[k] : 0.f;
+  const float iZt = k >= 0 ? __fdiv_rn(1.f, sZ[k].hi) : 0.f;
+  float Md = has_d ? sM[p.rows_t + k] : 0.f;
+  float iZd = has_d ? __fdiv_rn(1.f, sZ[p.rows_t + k].hi) : 0.f;
 
-  {
-    int last;
-    const double ws = warp_slice_residual<EPT>(tr, dr, c * p.chunk + warp * slice, p.V, Mt, iZt, Md, iZd, has_d, last);
-    if (lane == 0) {
-      wsum[c * kWarps + warp] = ws;
-      wlast[c * kWarps + warp] = last;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const int t = atomicAdd(&p.ticket_b[b], 1);
-      s_last = (t == p.nchunks - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-  }
-  __threadfence();
-  if (warp != 0) return;
-
-  // ---- last CTA, warp 0.  Lane l owns the consecutive slices [l * per, (l + 1) * per); an fp64
-  // exclusive scan over the lanes' sums gives every slice's prefix in token order, and R.
-  const int per = (nslices + 31) / 32;
-  auto scan_slices = [&](double& pre, double& total) {
-    double lsum = 0.0;
-    for (int j = 0; j < per; ++j) {
-      const int sl = lane * per + j;
-      if (sl < nslices) lsum += __ldcg(wsum + sl);
-    }
-    double incl = lsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    pre = incl - lsum;
-    total = __shfl_sync(0xffffffffu, incl, 31);
-  };
-  double pre, R;
-  scan_slices(pre, R);
-  if (R == 0.0) {
-    // residual identically zero: draw from P_{k+1} itself (recompute every slice with P)
-    has_d = false;
-    for (int sl = 0; sl < nslices; ++sl) {
-      int last;
-      const double ws = warp_slice_residual<EPT>(tr, tr, (sl / kWarps) * p.chunk + (sl % kWarps) * slice, p.V, Mt,
-                                                 iZt, 0.f, 0.f, false, last);
-      if (lane == 0) { wsum[sl] = ws; wlast[sl] = last; }
-    }
-    __syncwarp();
-    __threadfence_block();
-    scan_slices(pre, R);
-  }
-  const double thr = (double)p.u[(int64_t)b * p.u_sb + p.gamma] * R;
-  // the first slice whose cumulative sum passes thr: each lane checks its own slices
-  int my_sl = -1;
-  double my_acc = 0.0;
-  {
-    double run = pre;
-    for (int j = 0; j < per; ++j) {
-      const int sl = lane * per + j;
-      if (sl >= nslices) break;
-      const double ws = __ldcg(wsum + sl);
-      if (run + ws > thr) { my_sl = sl; my_acc = run; break; }
-      run += ws;
-    }
-  }
-  const unsigned found = __ballot_sync(0xffffffffu, my_sl >= 0);
-  int sstar = -1;
-  double acc = 0.0;
-  if (found) {
-    const int src = __ffs(found) - 1;
-    sstar = __shfl_sync(0xffffffffu, my_sl, src);
-    acc = __shfl_sync(0xffffffffu, my_acc, src);
-  }
-  int y = -1;
-  if (sstar >= 0) {
-    const int start = (sstar / kWarps) * p.chunk + (sstar % kWarps) * slice;
-    // the whole slice first (all loads in flight together), then the slab-by-slab scan
-    float4 rs[EPT / 4];
-#pragma unroll
-    for (int i = 0; i < EPT / 4; ++i) {
-      const int idx = start + i * 128 + lane * 4;
-      rs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (idx < p.V) rs[i] = resid4(tr, dr, idx, Mt, iZt, Md, iZd, has_d);
-    }
-    double base = acc;
-#pragma unroll
-    for (int i = 0; i < EPT / 4; ++i) {
-      if (y >= 0) break;
-      const int idx = start + i * 128 + lane * 4;
-      const float4 r = rs[i];
-      const double lsum = ((double)r.x + (double)r.y) + ((double)r.z + (double)r.w);
-      double incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const unsigned hit = __ballot_sync(0xffffffffu, base + incl > thr);
-      if (hit) {
-        const int src = __ffs(hit) - 1;
-        if (lane == src) {
-          const double run0 = base + incl - lsum;
-          const double run1 = run0 + (double)r.x, run2 = run1 + (double)r.y, run3 = run2 + (double)r.z;
-          const double run4 = run3 + (double)r.w;
-          int yy = run1 > thr ? idx : (run2 > thr ? idx + 1 : (run3 > thr ? idx + 2 : (run4 > thr ? idx + 3 : -1)));
-          if (yy < 0) yy = r.w > 0.f ? idx + 3 : (r.z > 0.f ? idx + 2 : (r.y > 0.f ? idx + 1 : idx));
-          s_y = yy;
+  FF R{0.f, 0.f}, cum{0.f, 0.f};
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    int last = -1;
+    if (k >= 0) {
+      // two slabs per step, both in flight before either is reduced
+      for (int s = s0 + warp; s < s1; s += 2 * kFinWarps) {
+        const int s2 = s + kFinWarps;
+        SlabData D0, D1;
+        slab_load(tr, dr, s * kSlab, p.V, has_d, D0);
+        if (s2 < s1) slab_load(tr, dr, s2 * kSlab, p.V, has_d, D1);
+        float r[16];
+        slab_compute(D0, s * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+        const FF m0 = slab_mass(r, s * kSlab, last);
+        if (lane == 0) s_slab[s - s0] = m0;
+        if (s2 < s1) {
+          slab_compute(D1, s2 * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+          const FF m1 = slab_mass(r, s2 * kSlab, last);
+          if (lane == 0) s_slab[s2 - s0] = m1;
         }
-        __syncwarp();
-        y = s_y;
       }
-      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (y < 0) y = __ldcg(wlast + sstar);  // rounding left the threshold at the slice end
-  }
-  if (y < 0) {
-    // no slice passed the threshold through rounding: the largest index with positive mass
-    int lst = -1;
-    for (int i = lane; i < nslices; i += 32) lst = max(lst, __ldcg(wlast + i));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lst = max(lst, __shfl_xor_sync(0xffffffffu, lst, o));
-    y = lst;
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (lane == 0) s_lastw[warp] = last;
+    __syncthreads();
+    if (warp == 0) {
+      FF lsum{0.f, 0.f}, incl{0.f, 0.f};
+      if (k >= 0) slab_scan(s_slab, s1 - s0, lsum, incl);
+      int l = lane < kFinWarps ? s_lastw[lane] : -1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
+      if (lane == 31) s_total = incl;
+      if (lane == 0) s_last = l;
+    }
+    cl.sync();
+    // the cluster's totals in rank order (one remote read per lane, then a fixed-order sum), the
+    // same in every CTA
+    if (warp == 0) {
+      FF tc{0.f, 0.f};
+      if (lane < CS) tc = *cl.map_shared_rank(&s_total, lane);
+      FF run{0.f, 0.f}, mycum{0.f, 0.f};
+      for (int c = 0; c < CS; ++c) {
+        if (c == rank) mycum = run;
+        run = ff_add(run, shfl_ff(tc, c));
+      }
+      if (lane == 0) { s_R = run; s_cum = mycum; }
+    }
+    __syncthreads();
+    R = s_R;
+    cum = s_cum;
+    if (k >= 0 && R.hi == 0.f && has_d) {
+      // residual identically zero: draw from P_{k+1} itself
+      has_d = false;
+      dr = tr;
+      Md = 0.f;
+      iZd = 0.f;
+      cl.sync();  // every CTA has read the totals before they are rewritten
+      continue;
+    }
+    break;
   }
-  if (lane == 0) write_chain_out(p, b, k, y);
+
+  if (k >= 0 && R.hi > 0.f) {
+    const float uu = p.u[(int64_t)b * p.u_sb + p.gamma];
+    const FF thr = ff_mul_f(R, uu);
+    const FF nxt = ff_add(cum, s_total);
+    if (warp == 0 && !ff_gt(cum, thr) && ff_gt(nxt, thr)) {
+      // this CTA holds the threshold: the same lane-block scan of its slab masses as for its total
+      // gives every slab's prefix in token order
+      const int ns = s1 - s0;
+      const int pp = (ns + 31) / 32;
+      FF lsum, incl;
+      slab_scan(s_slab, ns, lsum, incl);
+      int my_sl = -1;
+      FF my_acc{0.f, 0.f};
+      {
+        FF run = ff_add(cum, ff_add(incl, ff_neg(lsum)));
+        for (int j = 0; j < pp; ++j) {
+          const int sl = lane * pp + j;
+          if (sl >= ns) break;
+          const FF nx = ff_add(run, s_slab[sl]);
+          if (ff_gt(nx, thr)) { my_sl = sl; my_acc = run; break; }
+          run = nx;
+        }
+      }
+      const unsigned found = __ballot_sync(0xffffffffu, my_sl >= 0);
+      int y = -1;
+      if (found) {
+        const int src = __ffs(found) - 1;
+        const int sl = __shfl_sync(0xffffffffu, my_sl, src);
+        FF base = shfl_ff(my_acc, src);
+        // re-read the slab and scan it in token order: quarter j holds lane l's elements 4l..4l+3
+        float r[16];
+        const int sbase = (s0 + sl) * kSlab;
+        slab_resid(tr, dr, sbase, p.V, Mt, iZt, Md, iZd, has_d, r);
+        int slab_last = -1;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (r[e] > 0.f) slab_last = max(slab_last, sbase + (e >> 2) * 128 + lane * 4 + (e & 3));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) slab_last = max(slab_last, __shfl_xor_sync(0xffffffffu, slab_last, o));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (y >= 0) break;
+          const int idx = sbase + j * 128 + lane * 4;
+          const FF q = ff_add(ff_add(FF{r[4 * j], 0.f}, FF{r[4 * j + 1], 0.f}),
+                              ff_add(FF{r[4 * j + 2], 0.f}, FF{r[4 * j + 3], 0.f}));
+          const FF qi = warp_scan_ff(q);
+          const unsigned hit = __ballot_sync(0xffffffffu, ff_gt(ff_add(base, qi), thr));
+          if (hit) {
+            const int hl = __ffs(hit) - 1;
+            int yy = -1;
+            if (lane == hl) {
+              FF run = ff_add(base, ff_add(qi, ff_neg(q)));
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                run = ff_add(run, FF{r[4 * j + e], 0.f});
+                if (yy < 0 && ff_gt(run, thr)) yy = idx + e;
+              }
+              if (yy < 0)
+                yy = r[4 * j + 3] > 0.f ? idx + 3 : (r[4 * j + 2] > 0.f ? idx + 2 : (r[4 * j + 1] > 0.f ? idx + 1 : idx));
+            }
+            y = __shfl_sync(0xffffffffu, yy, hl);
+          }
+          base = ff_add(base, shfl_ff(qi, 31));
+        }
+        if (y < 0) y = slab_last;  // rounding left the threshold at the slab end
+      }
+      if (y < 0) y = s_last;  // rounding left it at the end of this CTA's share
+      if (lane == 0) write_chain_out(p, b, k, y);
+    }
+  }
+  if (k < 0 && rank == 0 && tid == 0) write_chain_out(p, b, -1, -1);
+  cl.sync();  // no CTA leaves while the cluster may still read its shared memory
 }
 
 // ------------------------------------------------------------------ small-V kernel
@@ -671,61 +837,37 @@ __global__ void __launch_bounds__(kSampleThreads) sample_small(const __grid_cons
 }
 
 // ------------------------------------------------------------------ host side
-static int pick_chunk(int V, int rows_total, int B, int num_sms) {
-  // the largest chunk that still gives every SM a few CTAs
-  const int cands[3] = {8192, 4096, 2048};
-  for (int i = 0; i < 3; ++i) {
-    const long long ctas = (long long)rows_total * B * ((V + cands[i] - 1) / cands[i]);
-    if (ctas >= 4LL * num_sms) return cands[i];
-  }
-  return 2048;
-}
-
 static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 size_t sample_workspace_bytes(int mode, int B, int rows_t, int rows_d, int V) {
   (void)mode;
-  const size_t nch = (size_t)(V + kMinChunk - 1) / kMinChunk;
   const size_t sch = (size_t)(V + kStatChunk - 1) / kStatChunk;
   const size_t rows = (size_t)rows_t + rows_d;
   size_t bytes = 256;                                        // status
-  bytes += round256(2 * (size_t)B * sizeof(int32_t));        // tickets (zeroed per call)
-  bytes += round256((size_t)B * sizeof(SeqInfo));            // accept decisions
   bytes += round256(B * rows * sch * sizeof(float));         // st_m
-  bytes += round256(B * rows * sch * sizeof(double));        // st_s / st_arg
-  bytes += round256(B * nch * 8 * sizeof(double));           // res_sum (per warp slice)
-  bytes += round256(B * nch * 8 * sizeof(int32_t));          // res_last
+  bytes += round256(B * rows * sch * sizeof(float2));        // st_s / st_arg
+  bytes += round256(B * rows * sizeof(float));               // sel
   return bytes;
 }
 
 void sample_workspace_carve(void* ws, SampleParams* p) {
-  const size_t nch = (size_t)(p->V + kMinChunk - 1) / kMinChunk;
   const size_t sch = (size_t)(p->V + kStatChunk - 1) / kStatChunk;
   const size_t rows = (size_t)p->rows_t + p->rows_d;
   const size_t B = (size_t)p->B;
   uint8_t* q = reinterpret_cast<uint8_t*>(ws);
   p->status = reinterpret_cast<uint32_t*>(q);
   q += 256;
-  p->ticket_a = reinterpret_cast<int32_t*>(q);
-  p->ticket_b = p->ticket_a + B;
-  q += round256(2 * B * sizeof(int32_t));
-  p->seq = reinterpret_cast<SeqInfo*>(q);
-  q += round256(B * sizeof(SeqInfo));
   p->st_m = reinterpret_cast<float*>(q);
   q += round256(B * rows * sch * sizeof(float));
-  p->st_s = reinterpret_cast<double*>(q);
+  p->st_s = reinterpret_cast<float2*>(q);
   p->st_arg = reinterpret_cast<int32_t*>(q);
-  q += round256(B * rows * sch * sizeof(double));
-  p->res_sum = reinterpret_cast<double*>(q);
-  q += round256(B * nch * 8 * sizeof(double));
-  p->res_last = reinterpret_cast<int32_t*>(q);
+  q += round256(B * rows * sch * sizeof(float2));
+  p->sel = reinterpret_cast<float*>(q);
 }
 
-template <int EPT>
 static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const int rows = p.rows_t + p.rows_d;
-  // status word and both ticket arrays start at zero for this call
-  cudaError_t e = cudaMemsetAsync(p.status, 0, 256 + 2 * (size_t)p.B * sizeof(int32_t), stream);
+  cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   const int items = p.schunks * rows * p.B;
   // persistent statistics grid: as many CTAs as fit on the GPU at once (warp-granular items)
@@ -737,18 +879,41 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   if (per_sm < 1) per_sm = 1;
   const int need = (items + kWarps - 1) / kWarps;
   const int g1 = need < per_sm * p.num_sms ? need : per_sm * p.num_sms;
-  if (p.mode == SPEC_SAMPLE_CHAIN) {
-    sample_stats<false><<<g1, kSampleThreads, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    sample_finalize<false><<<p.B, kSampleThreads, 0, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    dim3 g2(p.nchunks, p.B);
-    sample_residual<EPT><<<g2, kSampleThreads, 0, stream>>>(p);
-  } else {
+  if (p.mode != SPEC_SAMPLE_CHAIN) {
     sample_stats<true><<<g1, kSampleThreads, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    sample_finalize<true><<<p.B, kSampleThreads, 0, stream>>>(p);
+    sample_finalize<<<p.B, kSampleThreads, 0, stream>>>(p);
+    return cudaGetLastError();
   }
+  sample_stats<false><<<g1, kSampleThreads, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // clusters of CS CTAs per sequence: the largest CS for which every cluster of the batch can be
+  // resident at once (one wave); CS = 1 when the batch alone fills the GPU
+  const int nslabs = (p.V + kSlab - 1) / kSlab;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kFinThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int cs = 8;
+  for (; cs > 1; cs >>= 1) {
+    if ((long long)p.B * cs > p.num_sms) continue;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
+    cfg.dynamicSmemBytes = (size_t)((nslabs + cs - 1) / cs) * sizeof(FF);
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, sample_chain_finish, &cfg) == cudaSuccess && active >= p.B) break;
+    (void)cudaGetLastError();
+  }
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)((nslabs + cs - 1) / cs) * sizeof(FF);
+  e = cudaLaunchKernelEx(&cfg, sample_chain_finish, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -761,14 +926,8 @@ cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream) {
     return cudaGetLastError();
   }
   p.num_sms = num_sms;
-  p.chunk = pick_chunk(p.V, p.rows_t + p.rows_d, p.B, num_sms);
-  p.nchunks = (p.V + p.chunk - 1) / p.chunk;
   p.schunks = (p.V + kStatChunk - 1) / kStatChunk;
-  switch (p.chunk) {
-    case 8192: return launch_large<32>(p, stream);
-    case 4096: return launch_large<16>(p, stream);
-    default: return launch_large<8>(p, stream);
-  }
+  return launch_large(p, stream);
 }
 
 }  // namespace specv

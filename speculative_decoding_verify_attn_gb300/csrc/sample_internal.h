@@ -9,18 +9,9 @@ namespace specv {
 
 constexpr int kSampleThreads = 256;
 constexpr int kSmallVocab = 2048;   // V at or below: one warp per sequence does the whole step
-constexpr int kMinChunk = 2048;     // smallest residual-pass chunk per CTA (workspace is sized for it)
 constexpr int kStatChunk = 1024;    // statistics item: 1024 logits of one row, one warp
 constexpr int kMaxGamma = 32;
 constexpr int kMaxTreeNodes = 64;
-
-// Per-sequence result of the accept walk, written by the last statistics CTA of the sequence.
-struct SeqInfo {
-  int k;          // accepted drafts, -1 if a token id is invalid
-  int pad;
-  float Mt, Md;   // max logit of target row k and draft row k
-  double Zt, Zd;  // sum of exp(logit - max) of those rows
-};
 
 struct SampleParams {
   int mode, B, V;
@@ -38,19 +29,15 @@ struct SampleParams {
   int32_t* out_tok;
   int32_t* out_nacc;
   int32_t* out_nodes;
-  int chunk, nchunks;  // residual pass: vocabulary chunk per CTA and chunks per row
   int schunks;         // statistics pass: kStatChunk items per row
   int num_sms;
   // workspace
   uint32_t* status;
   float* st_m;      // [B][rows_t + rows_d][schunks] item maxima
-  double* st_s;     // [B][rows][schunks] sum of exp(x - item max)
+  float2* st_s;     // [B][rows][schunks] sum of exp(x - item max) as a float-float (hi, lo) pair
   int32_t* st_arg;  // [B][rows][schunks] item argmax (greedy)
-  double* res_sum;  // [B][nchunks][8] residual mass per warp slice of each chunk
-  int32_t* res_last;  // [B][nchunks][8] last index with positive residual in the slice, or -1
-  int32_t* ticket_a;  // [B] statistics CTAs finished per sequence (zeroed by the call)
-  int32_t* ticket_b;  // [B] residual CTAs finished per sequence (zeroed by the call)
-  SeqInfo* seq;       // [B]
+  float* sel;       // [B][rows] chain: logit of draft token x_i in target row i (at i) and in
+                    // draft row i (at rows_t + i), recorded by the statistics pass
   // tree (greedy tree mode)
   int N;
   int8_t parent[kMaxTreeNodes];

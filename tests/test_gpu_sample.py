@@ -86,6 +86,16 @@ def test_ragged_vocab_tails(sv, V):
     compare_chain(inp, out, nacc, f"V={V}")
 
 
+@pytest.mark.parametrize("B", [3, 17, 40, 100])
+def test_batch_sizes(sv, B):
+    """Batches from a few sequences (eight CTAs share a sequence's vocabulary) to more sequences
+    than SMs (one CTA per sequence)."""
+    inp = gen.chain_sample_inputs(B, 3, 20000, 300 + B, 2.0, 1.0)
+    out, nacc, st = gpu_chain(sv, inp)
+    assert st == 0
+    compare_chain(inp, out, nacc, f"B={B}")
+
+
 @pytest.mark.parametrize("V", [16, 64, 1024, 2048])
 def test_small_vocab_path(sv, V):
     inp = gen.chain_sample_inputs(3000, 4, V, 200 + V, 2.0, 0.5)

@@ -78,6 +78,20 @@ def test_tree_bf16_scaled(sv):
     assert_attn_close(o, ref, "bf16", what="tree")
 
 
+@pytest.mark.parametrize("Hq,Hkv,nq,tree", [(64, 8, 20, False), (64, 8, 40, True), (32, 2, 9, True)])
+def test_tensor_core_row_blocks(sv, Hq, Hkv, nq, tree):
+    """More than 128 query rows per kv head (160, 320 and 144 rows: pairs of row blocks per CTA,
+    one of them half empty for 320), with contexts long enough to split over many CTAs."""
+    kv_len = np.array([3000, 1500], dtype=np.int32)
+    parent = gen.random_tree(nq, 4, 8, 77) if tree else None
+    inp = gen.attn_inputs(2, Hq, Hkv, 128, nq, kv_len, 3100, "bf16", 90 + nq)
+    inp = gen.plant_tree_needles(inp, parent, "bf16", 91) if tree else gen.plant_chain_needles(inp, nq, "bf16", 91)
+    o, st = run_verify(sv, inp, "bf16", tree_parent=parent)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what=f"rows {nq * Hq // Hkv}")
+
+
 def test_chain_shaped_tree_matches_chain_on_gpu(sv):
     cfg = CONFIGS["llama3-8b-layer"]
     kv_len = np.array([640, 333], dtype=np.int32)
