@@ -606,13 +606,26 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
         }
         L += warp_sum(lw);
         const int n = min(32, nrec - i0);
-#pragma unroll 4
-        for (int t = 0; t < n; ++t) {
-          const float wt = __shfl_sync(0xffffffffu, wgt, t);
-          float v[PER];
-          load_vec<PER>(p.part_o + rec_of(i0 + t) * D + e0, v);
+        // eight records' loads in flight at once, then their weighted sum in record order
+        for (int t0 = 0; t0 < n; t0 += 8) {
+          float v[8][PER];
 #pragma unroll
-          for (int i = 0; i < PER; ++i) acc[i] = fmaf(wt, v[i], acc[i]);
+          for (int u = 0; u < 8; ++u) {
+            if (t0 + u < n) {
+              load_vec<PER>(p.part_o + rec_of(i0 + t0 + u) * D + e0, v[u]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < PER; ++i) v[u][i] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float wt = __shfl_sync(0xffffffffu, wgt, t0 + u);
+            if (t0 + u < n) {
+#pragma unroll
+              for (int i = 0; i < PER; ++i) acc[i] = fmaf(wt, v[u][i], acc[i]);
+            }
+          }
         }
       }
       if (p.has_new) {

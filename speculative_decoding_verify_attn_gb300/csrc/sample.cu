@@ -2,12 +2,13 @@
 //
 // Large vocabularies (V > kSmallVocab):
 //   sample_stats         persistent, warp-granular: every target and draft row is cut into items of
-//                        1024 logits; per item the max M_c and S_c = sum exp(x - M_c) (fp32 exp2f of
-//                        the scaled difference, compensated fp32 per lane, float-float across the
-//                        warp) -- or, in greedy modes, the item argmax.
+//                        1024 logits streamed through per-warp shared-memory rings by bulk copies;
+//                        per item the max M_c and S_c = sum exp(x - M_c) (MUFU ex2 of the scaled
+//                        difference, pairwise fp32 per lane, float-float across the warp) -- or, in
+//                        greedy modes, the item argmax -- and the logits of the draft tokens.
 //   sample_chain_finish  stochastic chain: one thread-block cluster per sequence.  Every CTA of the
-//                        cluster merges the sequence's item statistics (fp64) and takes the accept
-//                        decisions (one lane per draft); then CTA c computes the residual
+//                        cluster merges the sequence's item statistics (float-float) and takes the
+//                        accept decisions (one lane per draft); then CTA c computes the residual
 //                        max(P_{k+1} - Q_{k+1}, 0) (or P_{gamma+1}) over its share of the vocabulary
 //                        in 512-element slabs, the CTAs exchange their residual masses through
 //                        distributed shared memory, and the CTA whose share holds u * R finds its
@@ -16,9 +17,9 @@
 // Small vocabularies: one warp per sequence runs the whole step (the 16-token chi-square
 // workload runs 10^6 sequences at once).
 //
-// Every sum that decides a token is reproducible: fixed element orders, compensated fp32 per
-// thread (Kahan), float-float (Knuth's TwoSum) inside a warp, fp64 above that, no floating-point
-// atomics.
+// Every sum that decides a token is reproducible: fixed element orders, fp32 per lane (pairwise or
+// compensated), float-float (Knuth's TwoSum) across lanes, warps, CTAs and the cluster (fp64 in the
+// small-vocabulary kernel), no floating-point atomics.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -50,6 +51,15 @@ __device__ __forceinline__ float resid(float t, float d, float Mt, float iZt, fl
   const float pt = __fmul_rn(exp_shift(t, Mt), iZt);
   if (!has_d) return pt;
   const float qd = __fmul_rn(exp_shift(d, Md), iZd);
+  return fmaxf(__fsub_rn(pt, qd), 0.f);
+}
+
+// The same residual with one MUFU ex2 per exponential (flush-to-zero below 2^-126; relative error
+// about 2^-22, inside the decision band), for the large-vocabulary pass.
+__device__ __forceinline__ float resid_fast(float t, float d, float Mt, float iZt, float Md, float iZd, bool has_d) {
+  const float pt = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(t, Mt), kLog2e)), iZt);
+  if (!has_d) return pt;
+  const float qd = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(d, Md), kLog2e)), iZd);
   return fmaxf(__fsub_rn(pt, qd), 0.f);
 }
 
@@ -296,55 +306,116 @@ __device__ void tree_select_write(const SampleParams& p, int b, const int* a) {
 // ------------------------------------------------------------------ large-V kernels
 constexpr int kWarps = kSampleThreads / 32;
 
-// Statistics kernel, warp-granular and persistent: global warp w takes the items w, w + W, ...
-// (W warps in the grid), an item being kStatChunk = 1024 logits of one row, (b, row, item) in
-// row-major order.  Lane l reads elements 4l..4l+3 of each 128-element slab (coalesced 512-byte
-// warp loads).  Reductions are warp shuffles only -- no block barriers -- and the next item's
-// loads are in flight while the current one is reduced.  Per item: the max and the compensated
-// sum of exp(x - max) (float-float across lanes), or the argmax in greedy modes.
+// Statistics kernel, warp-granular and persistent (one CTA of kStatWarps warps per SM): an item is
+// kStatChunk = 1024 logits of one row, items numbered (b, row, c) in row-major order; CTA j takes
+// the contiguous items [j * k, (j + 1) * k), k = ceil(items / CTAs), and its warp w the items
+// j * k + w + i * kStatWarps, advancing (b, row, c) with carries.  Each warp streams its items through a private ring of kStatSlots
+// shared-memory slots filled by bulk copies (lane 0 issues, an mbarrier per slot completes), so
+// kStatSlots items per warp are in flight whatever the registers; the warp reads an item from shared memory
+// (lane l takes elements 4l..4l+3 of each 128-element slab), refills the slot and reduces it with
+// warp shuffles only.  Per item: the max and the sum of exp(x - max) (pairwise per lane,
+// float-float across lanes), or the argmax in greedy modes.  In the stochastic chain the warp also records the
+// logit of the row's draft token when it falls in the item.
 template <bool GREEDY>
-__global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_constant__ SampleParams p) {
-  constexpr int PER = kStatChunk / 128;  // float4 loads per lane per item
-  const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_constant__ SampleParams p) {
+  constexpr int PER = kStatChunk / 128;  // float4 per lane per item
+  extern __shared__ float4 s_ring[];     // [kStatWarps][kStatSlots][kStatChunk / 4]
+  __shared__ uint64_t s_bar[kStatWarps][kStatSlots];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows = p.rows_t + p.rows_d;
-  const int per_seq = rows * p.schunks;
-  const int items = p.B * per_seq;
-  const int W = gridDim.x * kWarps;
-  auto src_of = [&](int it, int& base) -> const float* {
-    const int b = it / per_seq;
-    const int rem = it - b * per_seq;
-    const int r = rem / p.schunks;
-    base = (rem - r * p.schunks) * kStatChunk;
-    return (r < p.rows_t) ? trow(p, b, r) : drow(p, b, r - p.rows_t);
+  const long long items = (long long)p.B * rows * p.schunks;
+  // the CTA's contiguous range of items; warp w takes items begin + w, begin + w + kStatWarps, ...
+  // (one sequential stream of memory per SM)
+  const long long per_c = (items + gridDim.x - 1) / gridDim.x;
+  const long long c_begin = (long long)blockIdx.x * per_c;
+  const long long c_end = min(items, c_begin + per_c);
+  long long it = c_begin + warp;
+  if (it >= c_end) return;
+  const int n_items = (int)((c_end - it + kStatWarps - 1) / kStatWarps);
+  float4* ring = s_ring + warp * kStatSlots * (kStatChunk / 4);
+  uint64_t* bar = s_bar[warp];
+  if (lane == 0) {
+    for (int i = 0; i < kStatSlots; ++i) mbar_init(&bar[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto row_of = [&](int bb, int rr) -> const float* {
+    return (rr < p.rows_t) ? trow(p, bb, rr) : drow(p, bb, rr - p.rows_t);
   };
-  auto load = [&](int it, float4 (&v)[PER]) {
-    int base;
-    const float* row = src_of(it, base);
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int idx = base + i * 128 + lane * 4;
-      v[i] = make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
-      if (idx < p.V) v[i] = __ldcs(reinterpret_cast<const float4*>(row + idx));
+  // issue side: coordinates of the next item to copy (lane 0 only)
+  int ib = 0, ir = 0, ic = 0, issued = 0;
+  {
+    const long long rowid = it / p.schunks;
+    ic = (int)(it % p.schunks);
+    ir = (int)(rowid % rows);
+    ib = (int)(rowid / rows);
+  }
+  int b = ib, r = ir, c = ic;  // processing side
+  auto issue = [&]() {         // lane 0: copy the next item into its slot, advance
+    const int slot = issued % kStatSlots;
+    // the warp's reads of the slot (generic proxy) come before the copy's writes (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const int base = ic * kStatChunk;
+    const uint32_t bytes = (uint32_t)(min(kStatChunk, p.V - base) * 4);
+    mbar_arrive_expect_tx(&bar[slot], bytes);
+    bulk_load(ring + slot * (kStatChunk / 4), row_of(ib, ir) + base, bytes, &bar[slot]);
+    ++issued;
+    ic += kStatWarps;
+    while (ic >= p.schunks) {
+      ic -= p.schunks;
+      if (++ir == rows) { ir = 0; ++ib; }
     }
   };
-  int it = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (it >= items) return;
-  float4 x[PER], xn[PER];
-  load(it, x);
-  for (; it < items; it += W) {
-    if (it + W < items) load(it + W, xn);
+  if (lane == 0)
+    for (int j = 0; j < kStatSlots && j < n_items; ++j) issue();
+  // offset of the row's draft token from the row start (-1: none), refreshed when the row changes
+  auto tok_of = [&](int bb, int rr) -> int {
+    if (GREEDY || p.mode != SPEC_SAMPLE_CHAIN) return -1;
+    const int ti = rr < p.rows_t ? rr : rr - p.rows_t;
+    return ti < p.gamma ? __ldg(p.tok + (int64_t)bb * p.tok_sb + ti) : -1;
+  };
+  int xtok = tok_of(b, r);
+  bool ok = true;
+  for (int k = 0; k < n_items; ++k, it += kStatWarps) {
+    const int slot = k % kStatSlots;
+    if (!mbar_wait_bounded(&bar[slot], (uint32_t)((k / kStatSlots) & 1), nullptr)) { ok = false; break; }
+    const int base = c * kStatChunk;
+    float4 x[PER];
+    if (base + kStatChunk <= p.V) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) x[i] = ring[slot * (kStatChunk / 4) + i * 32 + lane];
+    } else {  // the row's ragged last item
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int idx = base + i * 128 + lane * 4;
+        x[i] = idx < p.V ? ring[slot * (kStatChunk / 4) + i * 32 + lane]
+                         : make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && issued < n_items) issue();
     if (!GREEDY) {
       float m = neg_inf();
 #pragma unroll
       for (int i = 0; i < PER; ++i) m = fmaxf(m, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
       m = warp_max(m);
-      Kahan k;
+      // exp(x - m) = 2^((x - m) log2 e): the difference first (exact for the dominant terms), then one
+      // MUFU ex2 (flushing results below 2^-126 to zero, far below any term that counts).  The
+      // lane's 32 terms are summed pairwise (relative error at most 5 * 2^-24), the lanes in
+      // float-float.
+      float e[4 * PER];
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
-        k.add(exp_shift(x[i].x, m)); k.add(exp_shift(x[i].y, m));
-        k.add(exp_shift(x[i].z, m)); k.add(exp_shift(x[i].w, m));
+        e[4 * i + 0] = ex2_approx(__fmul_rn(__fsub_rn(x[i].x, m), kLog2e));
+        e[4 * i + 1] = ex2_approx(__fmul_rn(__fsub_rn(x[i].y, m), kLog2e));
+        e[4 * i + 2] = ex2_approx(__fmul_rn(__fsub_rn(x[i].z, m), kLog2e));
+        e[4 * i + 3] = ex2_approx(__fmul_rn(__fsub_rn(x[i].w, m), kLog2e));
       }
-      FF v{k.s, -k.c};
+#pragma unroll
+      for (int w = 4 * PER / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) e[j] = __fadd_rn(e[j], e[j + w]);
+      FF v{e[0], 0.f};
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         FF w;
@@ -356,28 +427,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_cons
         p.st_m[it] = m;
         p.st_s[it] = make_float2(v.hi, v.lo);
       }
-      // the draft token of this row, if it falls in this item: record its logit for the accept test
-      if (p.mode == SPEC_SAMPLE_CHAIN) {
-        int base;
-        src_of(it, base);
-        const int b = it / per_seq;
-        const int r = (it - b * per_seq) / p.schunks;
-        const int ti = r < p.rows_t ? r : r - p.rows_t;
-        if (ti < p.gamma) {
-          const int off = __ldg(p.tok + (int64_t)b * p.tok_sb + ti) - base;
-          if ((unsigned)off < (unsigned)kStatChunk && lane == ((off & 127) >> 2)) {
-            const int q = off >> 7, j = off & 3;
-            float val = 0.f;
+      // the row's draft token, if it falls in this item: its logit for the accept test
+      const int off = xtok - base;
+      if ((unsigned)off < (unsigned)kStatChunk && lane == ((off & 127) >> 2)) {
+        const int q = off >> 7, j = off & 3;
+        float val = 0.f;
 #pragma unroll
-            for (int i = 0; i < PER; ++i)
-              if (i == q) val = j == 0 ? x[i].x : (j == 1 ? x[i].y : (j == 2 ? x[i].z : x[i].w));
-            p.sel[(int64_t)b * rows + r] = val;
-          }
-        }
+        for (int i = 0; i < PER; ++i)
+          if (i == q) val = j == 0 ? x[i].x : (j == 1 ? x[i].y : (j == 2 ? x[i].z : x[i].w));
+        p.sel[(int64_t)b * rows + r] = val;
       }
     } else {
-      int base;
-      src_of(it, base);
       float bv = neg_inf();
       int bi = INT_MAX;
 #pragma unroll
@@ -394,8 +454,21 @@ __global__ void __launch_bounds__(kSampleThreads) sample_stats(const __grid_cons
         p.st_arg[it] = bi;
       }
     }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) x[i] = xn[i];
+    const int pb = b, pr = r;
+    c += kStatWarps;
+    while (c >= p.schunks) {
+      c -= p.schunks;
+      if (++r == rows) { r = 0; ++b; }
+    }
+    if (r != pr || b != pb) xtok = tok_of(b, r);
+  }
+  if (!ok) {
+    // a copy never completed: flag it, and wait (bounded) for the copies still in flight into
+    // this warp's slots before the CTA can leave
+    if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+    const int done = (int)((it - (c_begin + warp)) / kStatWarps);
+    for (int k = done; k < issued; ++k)
+      mbar_wait_bounded(&bar[k % kStatSlots], (uint32_t)((k / kStatSlots) & 1), nullptr);
   }
 }
 
@@ -463,10 +536,10 @@ __device__ __forceinline__ void slab_compute(const SlabData& D, int base, int V,
   for (int j = 0; j < 4; ++j) {
     const int idx = base + j * 128 + lane * 4;
     const bool in = idx < V;
-    r[4 * j + 0] = in ? resid(tv[j].x, dv[j].x, Mt, iZt, Md, iZd, has_d) : 0.f;
-    r[4 * j + 1] = in ? resid(tv[j].y, dv[j].y, Mt, iZt, Md, iZd, has_d) : 0.f;
-    r[4 * j + 2] = in ? resid(tv[j].z, dv[j].z, Mt, iZt, Md, iZd, has_d) : 0.f;
-    r[4 * j + 3] = in ? resid(tv[j].w, dv[j].w, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 0] = in ? resid_fast(tv[j].x, dv[j].x, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 1] = in ? resid_fast(tv[j].y, dv[j].y, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 2] = in ? resid_fast(tv[j].z, dv[j].z, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * j + 3] = in ? resid_fast(tv[j].w, dv[j].w, Mt, iZt, Md, iZd, has_d) : 0.f;
   }
 }
 __device__ __forceinline__ void slab_resid(const float* tr, const float* dr, int base, int V, float Mt, float iZt,
@@ -475,16 +548,13 @@ __device__ __forceinline__ void slab_resid(const float* tr, const float* dr, int
   slab_load(tr, dr, base, V, has_d, D);
   slab_compute(D, base, V, Mt, iZt, Md, iZd, has_d, r);
 }
-// One slab's residual mass (compensated fp32 per lane, float-float across the warp; lane 0) and
-// the largest index with positive residual (folded into `last`).
-__device__ __forceinline__ FF slab_mass(const float (&r)[16], int base, int& last) {
+// One slab's residual mass (compensated fp32 per lane, float-float across the warp; lane 0).  It is
+// positive exactly when the slab holds a positive residual.
+__device__ __forceinline__ FF slab_mass(const float (&r)[16]) {
   const int lane = threadIdx.x & 31;
   Kahan ks;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    ks.add(r[e]);
-    if (r[e] > 0.f) last = max(last, base + (e >> 2) * 128 + lane * 4 + (e & 3));
-  }
+  for (int e = 0; e < 16; ++e) ks.add(r[e]);
   FF v{ks.s, -ks.c};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -526,8 +596,6 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   __shared__ FF sZ[2 * kMaxGamma + 1];
   __shared__ int s_k;
   __shared__ FF s_total;              // this CTA's residual mass (read by the whole cluster)
-  __shared__ int s_last;              // largest index with positive residual in this CTA's share
-  __shared__ int s_lastw[kFinWarps];
   __shared__ FF s_R, s_cum;           // the cluster's total and this CTA's prefix
   cg::cluster_group cl = cg::this_cluster();
   const int CS = (int)cl.num_blocks(), rank = (int)cl.block_rank();
@@ -589,7 +657,6 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
 
   FF R{0.f, 0.f}, cum{0.f, 0.f};
   for (int attempt = 0; attempt < 2; ++attempt) {
-    int last = -1;
     if (k >= 0) {
       // two slabs per step, both in flight before either is reduced
       for (int s = s0 + warp; s < s1; s += 2 * kFinWarps) {
@@ -599,27 +666,20 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         if (s2 < s1) slab_load(tr, dr, s2 * kSlab, p.V, has_d, D1);
         float r[16];
         slab_compute(D0, s * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
-        const FF m0 = slab_mass(r, s * kSlab, last);
+        const FF m0 = slab_mass(r);
         if (lane == 0) s_slab[s - s0] = m0;
         if (s2 < s1) {
           slab_compute(D1, s2 * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
-          const FF m1 = slab_mass(r, s2 * kSlab, last);
+          const FF m1 = slab_mass(r);
           if (lane == 0) s_slab[s2 - s0] = m1;
         }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    if (lane == 0) s_lastw[warp] = last;
     __syncthreads();
     if (warp == 0) {
       FF lsum{0.f, 0.f}, incl{0.f, 0.f};
       if (k >= 0) slab_scan(s_slab, s1 - s0, lsum, incl);
-      int l = lane < kFinWarps ? s_lastw[lane] : -1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
       if (lane == 31) s_total = incl;
-      if (lane == 0) s_last = l;
     }
     cl.sync();
     // the cluster's totals in rank order (one remote read per lane, then a fixed-order sum), the
@@ -672,12 +732,27 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
           run = nx;
         }
       }
-      const unsigned found = __ballot_sync(0xffffffffu, my_sl >= 0);
+      unsigned found = __ballot_sync(0xffffffffu, my_sl >= 0);
+      bool at_end = false;
+      if (!found) {
+        // rounding left the threshold past this CTA's last slab: its last slab with positive mass,
+        // whose last positive element is then taken
+        int lastpos = -1;
+        for (int j = 0; j < pp; ++j) {
+          const int sl = lane * pp + j;
+          if (sl < ns && s_slab[sl].hi > 0.f) lastpos = sl;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, o));
+        my_sl = lane == 0 ? lastpos : -1;
+        found = __ballot_sync(0xffffffffu, my_sl >= 0);
+        at_end = true;
+      }
       int y = -1;
       if (found) {
         const int src = __ffs(found) - 1;
         const int sl = __shfl_sync(0xffffffffu, my_sl, src);
-        FF base = shfl_ff(my_acc, src);
+        FF base = at_end ? thr : shfl_ff(my_acc, src);
         // re-read the slab and scan it in token order: quarter j holds lane l's elements 4l..4l+3
         float r[16];
         const int sbase = (s0 + sl) * kSlab;
@@ -690,7 +765,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         for (int o = 16; o > 0; o >>= 1) slab_last = max(slab_last, __shfl_xor_sync(0xffffffffu, slab_last, o));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (y >= 0) break;
+          if (y >= 0 || at_end) break;
           const int idx = sbase + j * 128 + lane * 4;
           const FF q = ff_add(ff_add(FF{r[4 * j], 0.f}, FF{r[4 * j + 1], 0.f}),
                               ff_add(FF{r[4 * j + 2], 0.f}, FF{r[4 * j + 3], 0.f}));
@@ -715,7 +790,6 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         }
         if (y < 0) y = slab_last;  // rounding left the threshold at the slab end
       }
-      if (y < 0) y = s_last;  // rounding left it at the end of this CTA's share
       if (lane == 0) write_chain_out(p, b, k, y);
     }
   }
@@ -869,23 +943,21 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const int rows = p.rows_t + p.rows_d;
   cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
-  const int items = p.schunks * rows * p.B;
-  // persistent statistics grid: as many CTAs as fit on the GPU at once (warp-granular items)
-  int per_sm = 1;
-  if (p.mode == SPEC_SAMPLE_CHAIN)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_stats<false>, kSampleThreads, 0);
-  else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_stats<true>, kSampleThreads, 0);
-  if (per_sm < 1) per_sm = 1;
-  const int need = (items + kWarps - 1) / kWarps;
-  const int g1 = need < per_sm * p.num_sms ? need : per_sm * p.num_sms;
+  const long long items = (long long)p.schunks * rows * p.B;
+  // persistent statistics grid: one CTA per SM (its shared-memory rings fill the SM)
+  const long long need = (items + kStatWarps - 1) / kStatWarps;  // CTAs with at least a full set of items
+  const int g1 = need < (long long)p.num_sms ? (int)(need > 0 ? need : 1) : p.num_sms;
+  const size_t ring = (size_t)kStatWarps * kStatSlots * kStatChunk * sizeof(float);
+  e = cudaFuncSetAttribute(p.mode == SPEC_SAMPLE_CHAIN ? sample_stats<false> : sample_stats<true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+  if (e != cudaSuccess) return e;
   if (p.mode != SPEC_SAMPLE_CHAIN) {
-    sample_stats<true><<<g1, kSampleThreads, 0, stream>>>(p);
+    sample_stats<true><<<g1, kStatWarps * 32, ring, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     sample_finalize<<<p.B, kSampleThreads, 0, stream>>>(p);
     return cudaGetLastError();
   }
-  sample_stats<false><<<g1, kSampleThreads, 0, stream>>>(p);
+  sample_stats<false><<<g1, kStatWarps * 32, ring, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // clusters of CS CTAs per sequence: the largest CS for which every cluster of the batch can be
   // resident at once (one wave); CS = 1 when the batch alone fills the GPU

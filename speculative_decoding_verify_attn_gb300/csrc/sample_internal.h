@@ -10,6 +10,8 @@ namespace specv {
 constexpr int kSampleThreads = 256;
 constexpr int kSmallVocab = 2048;   // V at or below: one warp per sequence does the whole step
 constexpr int kStatChunk = 1024;    // statistics item: 1024 logits of one row, one warp
+constexpr int kStatWarps = 16;      // statistics CTA: warps, each with its own ring of item slots
+constexpr int kStatSlots = 3;       // items in flight per warp (4 KB each)
 constexpr int kMaxGamma = 32;
 constexpr int kMaxTreeNodes = 64;
 
