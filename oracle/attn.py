@@ -84,41 +84,59 @@ def verify_attn(q, k, v, kv_len, tree_parent=None, scale: float = 0.0) -> np.nda
     return o
 
 
-def window_slots(pos: int, W: int) -> np.ndarray:
-    """Ring slots holding the last min(pos, W) tokens: {t mod W : pos - min(pos, W) <= t < pos}."""
-    n = min(int(pos), W)
-    return np.array(sorted({t % W for t in range(int(pos) - n, int(pos))}), dtype=np.int64)
+def token_slot(t: int, W: int, n_sinks: int = 0) -> int:
+    """Ring slot of token t ([MagicDec] Implementation Step 1, with the attention sinks of Best
+    Practices §1): the first n_sinks tokens keep slots 0..n_sinks-1 for good; every later token t
+    goes to slot n_sinks + (t - n_sinks) mod (W - n_sinks).  n_sinks = 0 is the plain ring."""
+    t = int(t)
+    if t < n_sinks:
+        return t
+    return n_sinks + (t - n_sinks) % (W - n_sinks)
 
 
-def ring_append(k_ring, v_ring, pos, k_new, v_new):
-    """Write the current token's K/V (token index pos[b]-1) into slot (pos[b]-1) mod W.
+def window_tokens(pos: int, W: int, n_sinks: int = 0) -> list:
+    """Tokens the draft sees after pos tokens were written: all of them while pos <= W, else the
+    n_sinks first ones and the W - n_sinks most recent ones."""
+    pos = int(pos)
+    if pos <= W:
+        return list(range(pos))
+    return list(range(n_sinks)) + list(range(pos - (W - n_sinks), pos))
+
+
+def window_slots(pos: int, W: int, n_sinks: int = 0) -> np.ndarray:
+    """Slots holding the visible tokens (for n_sinks = 0: {t mod W : pos - min(pos, W) <= t < pos})."""
+    return np.array(sorted({token_slot(t, W, n_sinks) for t in window_tokens(pos, W, n_sinks)}), dtype=np.int64)
+
+
+def ring_append(k_ring, v_ring, pos, k_new, v_new, n_sinks: int = 0):
+    """Write the current token's K/V (token index pos[b]-1) into its slot.
     Returns new ring arrays (inputs are not modified)."""
     k_ring = np.array(k_ring, copy=True)
     v_ring = np.array(v_ring, copy=True)
     W = k_ring.shape[2]
     for b in range(k_ring.shape[0]):
-        s = (int(pos[b]) - 1) % W
+        s = token_slot(int(pos[b]) - 1, W, n_sinks)
         k_ring[b, :, s] = k_new[b]
         v_ring[b, :, s] = v_new[b]
     return k_ring, v_ring
 
 
-def draft_window_attn(q, k_ring, v_ring, pos, k_new=None, v_new=None, scale: float = 0.0):
+def draft_window_attn(q, k_ring, v_ring, pos, k_new=None, v_new=None, scale: float = 0.0, n_sinks: int = 0):
     """Single-query draft attention over the ring-buffer window.
 
     q [B, Hq, D]; k_ring, v_ring [B, Hkv, W, D]; pos [B] = tokens written including the current
-    one.  If k_new/v_new [B, Hkv, D] are given they are appended first (slot (pos-1) mod W).
+    one.  If k_new/v_new [B, Hkv, D] are given they are appended first (slot of token pos-1).
     Returns (o [B, Hq, D] float64, k_ring, v_ring after the append).
     """
     if k_new is not None:
-        k_ring, v_ring = ring_append(k_ring, v_ring, pos, k_new, v_new)
+        k_ring, v_ring = ring_append(k_ring, v_ring, pos, k_new, v_new, n_sinks)
     B, Hq, D = q.shape
     Hkv, W = k_ring.shape[1], k_ring.shape[2]
     G = Hq // Hkv
     sc = default_scale(D, scale)
     o = np.zeros((B, Hq, D), dtype=np.float64)
     for b in range(B):
-        slots = window_slots(int(pos[b]), W)
+        slots = window_slots(int(pos[b]), W, n_sinks)
         for h in range(Hq):
             g = h // G
             o[b, h] = attend(q[b, h], k_ring[b, g, slots], v_ring[b, g, slots], sc)
@@ -149,3 +167,26 @@ class RollWindowCache:
 
     def get_kv(self):
         return self.k[:, : self.n], self.v[:, : self.n]
+
+
+class SinkRollCache:
+    """The page's shift-left draft cache with attention sinks: the first n_sinks tokens stay in
+    front; behind them a FIFO of W - n_sinks slots filled in order, then shifted left by one per
+    new token.  An independently laid-out model for the sink tests."""
+
+    def __init__(self, W: int, n_sinks: int, Hkv: int, D: int):
+        self.W, self.S = W, n_sinks
+        self.sk = np.zeros((Hkv, 0, D))
+        self.sv = np.zeros((Hkv, 0, D))
+        self.fifo = RollWindowCache(W - n_sinks, Hkv, D)
+
+    def append(self, k_tok: np.ndarray, v_tok: np.ndarray) -> None:
+        if self.sk.shape[1] < self.S:
+            self.sk = np.concatenate([self.sk, k_tok[:, None]], axis=1)
+            self.sv = np.concatenate([self.sv, v_tok[:, None]], axis=1)
+        else:
+            self.fifo.append(k_tok, v_tok)
+
+    def get_kv(self):
+        fk, fv = self.fifo.get_kv()
+        return np.concatenate([self.sk, fk], axis=1), np.concatenate([self.sv, fv], axis=1)

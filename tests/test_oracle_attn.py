@@ -162,6 +162,44 @@ def test_ring_layout_matches_roll_cache_over_a_long_stream():
             assert np.allclose(o_ring[0, h], ref, atol=1e-13), (t, h)
 
 
+@pytest.mark.parametrize("W,S", [(5, 1), (8, 4), (6, 5), (12, 4)])
+def test_sink_ring_matches_sink_roll_cache_over_a_long_stream(W, S):
+    # attention sinks ([MagicDec] Best Practices §1): slot-mapped ring vs the independently laid
+    # out shift-left cache with the first S tokens kept in front
+    rng = np.random.default_rng(17 + W + S)
+    Hq, Hkv, D, T = 4, 2, 8, 3 * W + 7
+    roll = oa.SinkRollCache(W, S, Hkv, D)
+    k_ring = np.full((1, Hkv, W, D), np.nan)
+    v_ring = np.full((1, Hkv, W, D), np.nan)
+    for t in range(T):
+        kt = rng.standard_normal((Hkv, D))
+        vt = rng.standard_normal((Hkv, D))
+        q = rng.standard_normal((1, Hq, D))
+        roll.append(kt, vt)
+        o_ring, k_ring, v_ring = oa.draft_window_attn(q, k_ring, v_ring, np.array([t + 1]),
+                                                      k_new=kt[None], v_new=vt[None], n_sinks=S)
+        kk, vv = roll.get_kv()
+        assert kk.shape[1] == min(t + 1, W)
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            ref = oa.attend(q[0, h], kk[g], vv[g], 1.0 / np.sqrt(D))
+            assert np.allclose(o_ring[0, h], ref, atol=1e-13), (t, h)
+
+
+def test_sink_slots_hold_the_visible_tokens_by_simulation():
+    # write token ids into a physical slot array by the slot rule and read back the visible set
+    for W, S in ((7, 0), (7, 3), (4, 1), (9, 8)):
+        slots = [-1] * W
+        for pos in range(1, 5 * W):
+            slots[oa.token_slot(pos - 1, W, S)] = pos - 1
+            held = sorted(slots[s] for s in oa.window_slots(pos, W, S))
+            expect = list(range(pos)) if pos <= W else list(range(S)) + list(range(pos - (W - S), pos))
+            assert held == expect, (W, S, pos)
+    # no sinks: the plain ring
+    for pos in range(1, 30):
+        assert list(oa.window_slots(pos, 8, 0)) == sorted({t % 8 for t in range(max(0, pos - 8), pos)})
+
+
 def test_context_key_permutation_invariance():
     rng = np.random.default_rng(8)
     B, nq, Hq, Hkv, D, L = 1, 3, 2, 1, 8, 30
