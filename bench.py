@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling a small case)")
     ap.add_argument("--no-graphs", action="store_true", help="issue every call eagerly instead of graph replays")
+    ap.add_argument("--sinks", type=int, default=0, help="attention-sink slots at the front of the draft ring")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -248,6 +249,7 @@ class Runner:
         self.sv, self.cfg, self.inp, self.torch = sv, cfg, inp, torch
         u8 = torch.uint8
         self.mode = sv.SPEC_SAMPLE_TREE_GREEDY if cfg.tree_nodes else sv.SPEC_SAMPLE_CHAIN
+        self.n_sinks = 0
         self.ws_v = torch.empty(sv.spec_verify_attn_workspace(inp["q"], inp["k"], inp["o"]), dtype=u8, device=device)
         self.ws_s = torch.empty(sv.spec_sample_workspace(self.mode, inp["tl"]), dtype=u8, device=device)
         self.ws_w = None
@@ -258,7 +260,8 @@ class Runner:
     def draft(self, s):
         i = self.inp
         self.sv.spec_draft_window_attn(i["dq"][s], i["k_ring"], i["v_ring"], i["dpos"][s], i["do"],
-                                       k_new=i["dk"][s], v_new=i["dv"][s], workspace=self.ws_w)
+                                       k_new=i["dk"][s], v_new=i["dv"][s], workspace=self.ws_w,
+                                       n_sinks=self.n_sinks)
 
     def verify(self):
         i = self.inp
@@ -578,6 +581,7 @@ def main():
 
     inp = make_inputs(cfg, device, seed=cfg.seed + 7919 * rank)
     runner = Runner(sv, cfg, inp, device)
+    runner.n_sinks = args.sinks
     nb = step_bytes(cfg, inp)
     t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs)
     total_ms = max_over_ranks(pg, t["total_ms"], device)
@@ -607,7 +611,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.kv_dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.B, "q_heads": cfg.Hq, "kv_heads": cfg.Hkv,
                    "head_dim": cfg.D, "context": list(cfg.ctx), "gamma": cfg.gamma, "window": cfg.window,
-                   "draft_steps": cfg.draft_steps, "vocab": cfg.vocab, "kv_dtype": cfg.kv_dtype,
+                   "draft_steps": cfg.draft_steps, "draft_sinks": args.sinks, "vocab": cfg.vocab, "kv_dtype": cfg.kv_dtype,
                    "parallelism": f"replicas x{world}",
                    "launch": "one CUDA graph per op (captured through the binding), replayed" if t["graphs"]
                              else "eager calls through the binding",

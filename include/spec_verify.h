@@ -148,19 +148,24 @@ int spec_verify_attn_noalloc(const spec_attn_args* args, spec_stream_t stream);
 /* ------------------------------------------------------------------------------------------
  * spec_draft_window_attn
  *
- * Single-query draft attention over the last min(pos[b], W) tokens of sequence b, kept in a
- * ring: token t (0-based) lives in slot t mod W.  pos[b] counts the tokens written including
- * the current one.  If k_new/v_new are given, the current token's K/V take slot (pos[b] - 1)
- * mod W: the attention uses them in place of that slot's old contents, and the ring is updated
- * in place (the slot holds k_new/v_new once the call's work on the stream has completed);
- * k_new/v_new must not overlap the rings.  The visible slots are
- * {t mod W : pos[b] - min(pos[b], W) <= t < pos[b]}; since softmax over keys does not depend on
- * their order, this equals attention over the page's shift-left buffer.
+ * Single-query draft attention over the draft's bounded window of W slots per sequence, kept as
+ * a ring ([MagicDec] Implementation Step 1).  pos[b] counts the tokens written including the
+ * current one.  With n_sinks = 0 token t (0-based) lives in slot t mod W and the visible tokens
+ * are the last min(pos[b], W).  With n_sinks = S > 0 (attention sinks, [MagicDec] Best Practices
+ * §1) the first S tokens keep slots 0..S-1 for good, token t >= S lives in slot
+ * S + (t - S) mod (W - S), and the visible tokens are all of them while pos[b] <= W, else the S
+ * first and the W - S most recent.  Either way the visible tokens fill slots 0..min(pos[b], W)-1
+ * of the ring; since softmax over keys does not depend on their order, this equals attention over
+ * the page's shift-left buffer.  If k_new/v_new are given, the current token's K/V take the slot
+ * of token pos[b] - 1: the attention uses them in place of that slot's old contents, and the ring
+ * is updated in place (the slot holds k_new/v_new once the call's work on the stream has
+ * completed); k_new/v_new must not overlap the rings.
  *
  * Layout: q [B, Hq, D] (q_stride_b, q_stride_h); rings [B, Hkv, W, D] (ring_stride_b,
  * ring_stride_h; token stride D); k_new/v_new [B, Hkv, D] (new_stride_b, new_stride_h) or both
  * NULL; o [B, Hq, D] (o_stride_b, o_stride_h); pos [B] int32 device.
- * Types and limits as spec_verify_attn (nq = 1); W >= 1.
+ * Types and limits as spec_verify_attn (nq = 1); W >= 1; 0 <= n_sinks < W (else
+ * SPEC_ERR_INVALID_ARG).
  * ---------------------------------------------------------------------------------------- */
 typedef struct spec_window_args {
   int32_t B, Hq, Hkv, D, W;
@@ -175,7 +180,7 @@ typedef struct spec_window_args {
   const void* v_new;
   int64_t new_stride_b, new_stride_h;
   float scale;
-  int32_t reserved0;
+  int32_t n_sinks;    /* attention-sink slots at the front of the ring (0: plain ring) */
   void* o;
   int64_t o_stride_b, o_stride_h;
   void* workspace;

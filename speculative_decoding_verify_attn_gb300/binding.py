@@ -60,7 +60,7 @@ class SpecWindowArgs(Structure):
         ("k_ring", c_void_p), ("v_ring", c_void_p), ("ring_stride_b", c_int64), ("ring_stride_h", c_int64),
         ("pos", c_void_p),
         ("k_new", c_void_p), ("v_new", c_void_p), ("new_stride_b", c_int64), ("new_stride_h", c_int64),
-        ("scale", c_float), ("reserved0", c_int32),
+        ("scale", c_float), ("n_sinks", c_int32),
         ("o", c_void_p), ("o_stride_b", c_int64), ("o_stride_h", c_int64),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
@@ -226,7 +226,8 @@ def spec_verify_attn(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0
     return o
 
 
-def window_attn_args(q, k_ring, v_ring, pos, o, k_new=None, v_new=None, scale: float = 0.0, workspace=None):
+def window_attn_args(q, k_ring, v_ring, pos, o, k_new=None, v_new=None, scale: float = 0.0, workspace=None,
+                     n_sinks: int = 0):
     B, Hq, D = q.shape
     Hkv, W = k_ring.shape[1], k_ring.shape[2]
     if k_ring.stride(2) != D or tuple(k_ring.stride()) != tuple(v_ring.stride()):
@@ -241,7 +242,7 @@ def window_attn_args(q, k_ring, v_ring, pos, o, k_new=None, v_new=None, scale: f
         pos=_ptr(pos),
         k_new=_ptr(k_new), v_new=_ptr(v_new),
         new_stride_b=0 if k_new is None else k_new.stride(0), new_stride_h=0 if k_new is None else k_new.stride(1),
-        scale=scale,
+        scale=scale, n_sinks=n_sinks,
         o=_ptr(o), o_stride_b=o.stride(0), o_stride_h=o.stride(1),
         workspace=_ptr(workspace), workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
     )
@@ -255,17 +256,17 @@ def spec_draft_window_attn_workspace(q, k_ring, o) -> int:
 
 
 def spec_draft_window_attn(q, k_ring, v_ring, pos, o, *, k_new=None, v_new=None, scale: float = 0.0,
-                           workspace=None, stream=None):
+                           workspace=None, stream=None, n_sinks: int = 0):
     """Draft single-query attention over the ring window (appending k_new/v_new first if given).
 
     q [B, Hq, D]; k_ring, v_ring [B, Hkv, W, D] (updated in place when k_new is given);
-    pos [B] int32 (device); o [B, Hq, D]."""
+    pos [B] int32 (device); o [B, Hq, D]; n_sinks attention-sink slots at the ring's front."""
     _check_cuda(q, k_ring, v_ring, pos, o, k_new, v_new)
     need = spec_draft_window_attn_workspace(q, k_ring, o)
     if need == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, "spec_draft_window_attn_workspace")
     ws = _workspace(need, q.device, workspace)
-    a = window_attn_args(q, k_ring, v_ring, pos, o, k_new, v_new, scale, ws)
+    a = window_attn_args(q, k_ring, v_ring, pos, o, k_new, v_new, scale, ws, n_sinks)
     st = lib().spec_draft_window_attn(byref(a), _stream_handle(stream))
     if st != SPEC_OK:
         raise SpecError(st, "spec_draft_window_attn")

@@ -233,6 +233,7 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   if ((a->k_new == nullptr) != (a->v_new == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (a->k_new && (a->new_stride_b < 0 || a->new_stride_h < 0)) return SPEC_ERR_INVALID_ARG;
   if (!isfinite(a->scale)) return SPEC_ERR_INVALID_ARG;
+  if (a->n_sinks < 0 || a->n_sinks >= a->W) return SPEC_ERR_INVALID_ARG;
   const size_t need = spec_draft_window_attn_workspace(a);
   if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
 
@@ -253,6 +254,7 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   p.o_bf16 = a->o_dtype == SPEC_BF16;
   p.kv_bf16 = bf16;
   p.has_new = a->k_new != nullptr;
+  p.n_sinks = a->n_sinks;
   p.k_new = a->k_new; p.v_new = a->v_new;
   p.new_sb = a->new_stride_b; p.new_sh = a->new_stride_h;
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);

@@ -20,7 +20,7 @@
 // and the tree keys whose node is on its root path (bitmask); window: every valid ring slot.
 // Cache slots at or beyond len are never trusted: their scores are masked by select, and the
 // matching V rows are zeroed before P.V, so NaN garbage there cannot leak into the output.
-// Window with a new key: ring slot (pos - 1) mod W is about to be overwritten, so the partial
+// Window with a new key: the ring slot of token pos - 1 is about to be overwritten, so the partial
 // kernels treat it like a slot past the end, and the merge kernel adds the new key's score and
 // value to the softmax and then stores the key into the slot (after every partial has read it).
 #include <cuda.h>
@@ -123,7 +123,7 @@ __device__ __forceinline__ int combine_part(const AttnParams& p, float (&o)[D / 
     if (h == 0) {
       if (add_new && warp == 0) {
         // every warp is past this segment's tiles: store the new key into its ring slot
-        const int slot = (__ldg(p.lens + b) - 1) % p.Lmax;
+        const int slot = window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks);
         const int64_t src = (int64_t)b * p.new_sb + (int64_t)g * p.new_sh;
         const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * D;
         const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + src;
@@ -248,7 +248,7 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQ,
     float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
     const int tail_start = len - p.nq;
     // window with a new key: the ring slot being replaced (verify masks have none)
-    const int skip = (MASK == kMaskNone && p.has_new) ? (__ldg(p.lens + b) - 1) % p.Lmax : -1;
+    const int skip = (MASK == kMaskNone && p.has_new) ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
 
     int bad = 0;
     for (int key0 = kb; key0 < ke; key0 += KT) {
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ 
   int b, g, kb, ke, len;
   while (walker_next(p, w, b, g, kb, ke, len)) {
     const int tail_start = len - p.nq;
-    const int skip = p.has_new ? (__ldg(p.lens + b) - 1) % p.Lmax : -1;
+    const int skip = p.has_new ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
     const float* kseg = kb_ + b * p.kv_sb + g * p.kv_sh;
     const float* vseg = vb_ + b * p.kv_sb + g * p.kv_sh;
     for (int r = warp; r < rows_here; r += 4) {
@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
     for (int i = 0; i < PER; ++i) acc[i] *= inv;
     if (p.has_new && r == 0) {
       // every partial kernel has finished reading the ring (stream order): store the new key
-      const int slot = (__ldg(p.lens + b) - 1) % p.Lmax;
+      const int slot = window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks);
       const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * D + e0;
       if (p.kv_bf16) {
         __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.k)) + dst;
@@ -677,12 +677,12 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
 
 // ------------------------------------------------------------------ ring append
 // Separate append, used ahead of the tensor-core partial kernel (which has no replaced-slot mask):
-// one CTA per (sequence, kv head) stores k_new / v_new into ring slot (pos - 1) mod W.
+// one CTA per (sequence, kv head) stores k_new / v_new into the ring slot of token pos - 1.
 __global__ void window_append_kernel(const __grid_constant__ AttnParams p) {
   const int b = blockIdx.x / p.Hkv, g = blockIdx.x % p.Hkv;
   const int pos = p.lens[b];
   if (pos < 1) return;
-  const int slot = (pos - 1) % p.Lmax;
+  const int slot = window_slot(pos - 1, p.Lmax, p.n_sinks);
   const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)slot * p.D;
   const int64_t src = (int64_t)b * p.new_sb + (int64_t)g * p.new_sh;
   if (p.kv_bf16) {

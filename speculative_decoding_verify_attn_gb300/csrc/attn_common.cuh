@@ -16,6 +16,12 @@ __device__ __forceinline__ int seg_len(const AttnParams& p, int b) {
   return (L >= p.nq && L <= p.Lmax) ? L : 0;
 }
 
+// Ring slot of the window's token t: the first n_sinks tokens keep slots 0..n_sinks-1, later ones
+// cycle through the other W - n_sinks slots.
+__device__ __forceinline__ int window_slot(int t, int W, int n_sinks) {
+  return t < n_sinks ? t : n_sinks + (t - n_sinks) % (W - n_sinks);
+}
+
 // 128-key tiles of a segment of `len` keys (the last one may be partial).
 __device__ __forceinline__ int seg_tiles(int len) { return (len + kKeyTile - 1) / kKeyTile; }
 

@@ -48,10 +48,11 @@ struct AttnParams {
   float* part_o;                   // [slots][nks][rows][D]  (slot = segment + CTA index)
   float2* part_ml;                 // [slots][nks][rows]  (m in log2 units, l)
   uint32_t* status;
-  // window with a fused ring append: the partial kernels mask ring slot (pos - 1) mod W (about
-  // to be overwritten) and the merge kernel adds the new key (k_new, v_new) to the softmax and
-  // stores it into that slot.  has_new = 0: no append.
+  // window with a fused ring append: the partial kernels mask the slot of token pos - 1 (about
+  // to be overwritten) and the merge kernel (or, in direct mode, the partial kernel) adds the new
+  // key (k_new, v_new) to the softmax and stores it into that slot.  has_new = 0: no append.
   int has_new;
+  int n_sinks;                     // window: attention-sink slots at the front of the ring
   int kv_bf16;                     // q, k_new, v_new element type (same as the cache)
   const void* k_new;
   const void* v_new;

@@ -113,6 +113,8 @@ def test_window_host_validation(L):
     assert call(window_args(pos=None)) == -1
     assert call(window_args(k_new=FAKE)) == -1         # k_new without v_new
     assert call(window_args(workspace_bytes=0)) == -3
+    assert call(window_args(n_sinks=-1)) == -1
+    assert call(window_args(n_sinks=window_args().W)) == -1   # at least one ring slot
 
 
 def sample_args(**kw):

@@ -19,11 +19,11 @@ def sv():
     return sv
 
 
-def _run(sv, q, kr, vr, pos, kn, vn, dtype):
+def _run(sv, q, kr, vr, pos, kn, vn, dtype, n_sinks=0):
     torch = torch_mod()
     o = torch.full(q.shape, float("nan"), dtype=torch.float32, device=q.device)
     ws = torch.empty(sv.spec_draft_window_attn_workspace(q, kr, o), dtype=torch.uint8, device=q.device)
-    sv.spec_draft_window_attn(q, kr, vr, pos, o, k_new=kn, v_new=vn, workspace=ws)
+    sv.spec_draft_window_attn(q, kr, vr, pos, o, k_new=kn, v_new=vn, workspace=ws, n_sinks=n_sinks)
     torch.cuda.synchronize()
     return to_np(o), sv.read_status(ws)
 
@@ -134,3 +134,58 @@ def test_window_long_ring_split_over_ctas(sv, dtype):
         assert np.array_equal(kr_np[b, :, s], k_after[i, :, s].astype(np.float32))
     # the bad sequence's ring is untouched
     assert np.array_equal(kr_np[1], inp["k_ring"][1].astype(np.float32), equal_nan=True)
+
+
+@pytest.mark.parametrize("dtype,D,Hq,Hkv,W,S", [("bf16", 128, 32, 8, 512, 4), ("f32", 64, 4, 1, 96, 4),
+                                                ("bf16", 128, 64, 1, 256, 4), ("bf16", 128, 32, 8, 6000, 4),
+                                                ("bf16", 64, 8, 2, 64, 63)])
+def test_window_with_attention_sinks(sv, dtype, D, Hq, Hkv, W, S):
+    """Attention sinks: the first S tokens keep their slots, the rest cycle through W - S slots.
+    Covers every kernel path (direct and split mma.sync, fp32, tensor core with separate append)
+    and positions before, at and far past the window size."""
+    pos = np.array([1, 3, S, S + 1, W - 1, W, W + 1, 3 * W + 5, 70001], dtype=np.int32)
+    B = len(pos)
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, pos, dtype, seed=40 + S)
+    # unwritten slots (slot >= pos while pos <= W) hold NaN; with sinks slot s holds token s then
+    kr0, vr0 = inp["k_ring"], inp["v_ring"]
+    q, kr, vr = to_dev(inp["q"], dtype), to_dev(kr0, dtype), to_dev(vr0, dtype)
+    kn, vn = to_dev(inp["k_new"], dtype), to_dev(inp["v_new"], dtype)
+    o, st = _run(sv, q, kr, vr, to_dev(pos, "i32"), kn, vn, dtype, n_sinks=S)
+    ref, k_after, v_after = oa.draft_window_attn(inp["q"], kr0, vr0, pos, inp["k_new"], inp["v_new"], n_sinks=S)
+    assert st == 0
+    assert_attn_close(o, ref, dtype, what=f"sinks S={S} W={W}")
+    kr_np = to_np(kr)
+    for b in range(B):
+        s_ = oa.token_slot(int(pos[b]) - 1, W, S)
+        assert np.array_equal(kr_np[b, :, s_], k_after[b, :, s_].astype(np.float32))
+        other = [t for t in oa.window_slots(int(pos[b]), W, S) if t != s_]
+        assert np.array_equal(kr_np[b][:, other], kr0[b][:, other])
+
+
+def test_sink_window_round_matches_the_shift_left_cache(sv):
+    """A stream of single-token draft steps with sinks against the page's shift-left cache with the
+    first tokens kept in front, on the MagicDec window shape (W = 512, 4 sinks)."""
+    torch = torch_mod()
+    cfg = CONFIGS["magicdec-64k"]
+    W, S, T = 64, 4, 150
+    Hq, Hkv, D = cfg.Hq, cfg.Hkv, cfg.D
+    r = np.random.default_rng(99)
+    kr = torch.zeros((1, Hkv, W, D), dtype=torch.bfloat16, device="cuda")
+    vr = torch.zeros_like(kr)
+    roll = oa.SinkRollCache(W, S, Hkv, D)
+    for t in range(T):
+        kt = gen.store(r.standard_normal((Hkv, D)).astype(np.float32), "bf16")
+        vt = gen.store(r.standard_normal((Hkv, D)).astype(np.float32), "bf16")
+        q = gen.store(r.standard_normal((1, Hq, D)).astype(np.float32), "bf16")
+        roll.append(kt.astype(np.float64), vt.astype(np.float64))
+        if t % 7 != 6 and t != T - 1:
+            o, st = _run(sv, to_dev(q, "bf16"), kr, vr, to_dev(np.array([t + 1], np.int32), "i32"),
+                         to_dev(kt[None], "bf16"), to_dev(vt[None], "bf16"), "bf16", n_sinks=S)
+            continue
+        o, st = _run(sv, to_dev(q, "bf16"), kr, vr, to_dev(np.array([t + 1], np.int32), "i32"),
+                     to_dev(kt[None], "bf16"), to_dev(vt[None], "bf16"), "bf16", n_sinks=S)
+        kk, vv = roll.get_kv()
+        ref = np.stack([oa.attend(q[0, h].astype(np.float64), kk[h // (Hq // Hkv)], vv[h // (Hq // Hkv)],
+                                  1.0 / np.sqrt(D)) for h in range(Hq)])
+        assert st == 0
+        assert_attn_close(o, ref[None], "bf16", what=f"step {t}")
