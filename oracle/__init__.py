@@ -14,11 +14,11 @@ Everything here is plain NumPy in float64, written from the definitions on the p
 * "Speculative Decoding & Medusa Architecture" (zyekh) -- speculative sampling math (§2),
   expected accepted tokens per step (§1 formula block), tree attention with a 2D mask (§4).
 * "Speculative Decoding in LLM Serving Systems" (elimelt, UW CSE 599K) -- the algorithm,
-  accepting and rejecting, 1 .. gamma+1 tokens per round, tree attention over ancestors
-  (Tree-based variants).
+  accepting and rejecting (and the rollback of rejected tokens' K/V, ``commit.py``), 1 .. gamma+1
+  tokens per round, tree attention over ancestors (Tree-based variants).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms, invariants,
 brute force and hand-worked fixtures (``tests/golden/``), not against itself.
 """
 
-from . import attn, sample  # noqa: F401
+from . import attn, commit, sample  # noqa: F401
