@@ -246,12 +246,58 @@ typedef struct spec_sample_args {
 size_t spec_sample_workspace(const spec_sample_args* args);
 int spec_sample(const spec_sample_args* args, spec_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * spec_commit
+ *
+ * The rollback step after verification ("Speculative Decoding in LLM Serving Systems", Accepting
+ * and rejecting; "Guide to MagicDec", Implementation Step 3; "Speculative Decoding & Medusa" §4):
+ * keep the K/V of the accepted tokens and drop the rest, on the device, from spec_sample's
+ * outputs, so that no host round trip sits between rounds.  The nq positions verified in the
+ * round are the last nq of each sequence's cache, kv_len[b] - nq .. kv_len[b] - 1.
+ *
+ * SPEC_COMMIT_CHAIN (nq = gamma + 1): position kv_len - nq holds the last committed token and the
+ *   next gamma the drafts; with k = num_accepted[b] the first k + 1 stay:
+ *   kv_len[b] = kv_len[b] - nq + 1 + k.  No K/V moves (k and v may be NULL).
+ * SPEC_COMMIT_TREE (nq = N nodes, N <= 64): node i sits at position kv_len - N + i, node 0 (the
+ *   root) being the last committed token; with the accepted path path_nodes[b, 0..k-1] (depths
+ *   1..k, as spec_sample's out_path_nodes reports it) the K/V of path node j move to position
+ *   kv_len - N + 1 + j, for every kv head, and kv_len[b] = kv_len[b] - N + 1 + k.
+ *
+ * A sequence with num_accepted outside [0, nq - 1] (tree: or above path_cols), kv_len outside
+ * [nq, Lmax] or (tree) a path node outside [1, N) is left unchanged and SPEC_STATUS_BAD_TOKEN /
+ * SPEC_STATUS_BAD_KV_LEN is set in the status word (byte 0 of the workspace).
+ *
+ * Layout: k, v [B, Hkv, Lmax, D] with strides as spec_verify_attn (kv_dtype SPEC_BF16 or
+ * SPEC_F32, 4-byte aligned, strides even for bf16); kv_len [B] int32 device, read and written;
+ * num_accepted [B] int32 device; path_nodes [B, path_cols] int32 device, path_stride_b >=
+ * path_cols elements between rows (tree only; spec_sample's out_path_nodes fits as it is).  workspace: spec_commit_workspace() bytes, 256-byte aligned.
+ * ---------------------------------------------------------------------------------------- */
+typedef enum { SPEC_COMMIT_CHAIN = 0, SPEC_COMMIT_TREE = 1 } spec_commit_mode;
+
+typedef struct spec_commit_args {
+  int32_t mode, B, Hkv, D, nq, Lmax;
+  int32_t kv_dtype, path_cols; /* tree: node ids per path row (>= the largest num_accepted) */
+  void* k; /* device, tree mode */
+  void* v;
+  int64_t kv_stride_b, kv_stride_h;
+  int32_t* kv_len;             /* device [B], in/out */
+  const int32_t* num_accepted; /* device [B] */
+  const int32_t* path_nodes;   /* device [B, path_stride_b], tree mode */
+  int64_t path_stride_b;
+  void* workspace;
+  size_t workspace_bytes;
+} spec_commit_args;
+
+size_t spec_commit_workspace(const spec_commit_args* args);
+int spec_commit(const spec_commit_args* args, spec_stream_t stream);
+
 /* Text for a return code. */
 const char* spec_status_string(int status);
 /* ABI version: bump on any struct or semantic change. */
 int spec_abi_version(void);
 /* sizeof() of the argument structs as compiled into the library, so that a binding can check
- * its own layout: which = 0 spec_attn_args, 1 spec_window_args, 2 spec_sample_args; else 0. */
+ * its own layout: which = 0 spec_attn_args, 1 spec_window_args, 2 spec_sample_args,
+ * 3 spec_commit_args; else 0. */
 size_t spec_abi_struct_size(int which);
 
 #ifdef __cplusplus

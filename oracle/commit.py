@@ -46,7 +46,8 @@ def chain_commit(kv_len: np.ndarray, nq: int, num_accepted: np.ndarray, Lmax: in
 
 def tree_commit(k_cache: np.ndarray, v_cache: np.ndarray, kv_len: np.ndarray, N: int,
                 path_nodes: np.ndarray, num_accepted: np.ndarray):
-    """k_cache, v_cache [B, Hkv, Lmax, D]; path_nodes [B, >= max k] node ids (depth order).
+    """k_cache, v_cache [B, Hkv, Lmax, D]; path_nodes [B, path_cols] node ids (depth order); a count
+    above path_cols or a node id outside [1, N) is flagged like a bad count.
     Returns (k, v, new kv_len, flags); inputs are not modified."""
     k_cache = np.array(k_cache, copy=True)
     v_cache = np.array(v_cache, copy=True)
@@ -57,7 +58,10 @@ def tree_commit(k_cache: np.ndarray, v_cache: np.ndarray, kv_len: np.ndarray, N:
     flag = np.zeros(len(kv_len), dtype=bool)
     for b in range(len(kv_len)):
         L, kb = int(kv_len[b]), int(acc[b])
-        if kb < 0 or kb > N - 1 or L < N or L > Lmax:
+        if kb < 0 or kb > N - 1 or kb > path_nodes.shape[1] or L < N or L > Lmax:
+            flag[b] = True
+            continue
+        if any(not 1 <= int(path_nodes[b, j]) < N for j in range(kb)):
             flag[b] = True
             continue
         base = L - N

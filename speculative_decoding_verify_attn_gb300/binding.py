@@ -33,6 +33,8 @@ SPEC_STATUS_BAD_POS = 2
 SPEC_STATUS_BAD_TOKEN = 4
 SPEC_STATUS_TIMEOUT = 8
 
+SPEC_COMMIT_CHAIN = 0
+SPEC_COMMIT_TREE = 1
 SPEC_SAMPLE_CHAIN = 0
 SPEC_SAMPLE_CHAIN_GREEDY = 1
 SPEC_SAMPLE_TREE_GREEDY = 2
@@ -62,6 +64,16 @@ class SpecWindowArgs(Structure):
         ("k_new", c_void_p), ("v_new", c_void_p), ("new_stride_b", c_int64), ("new_stride_h", c_int64),
         ("scale", c_float), ("n_sinks", c_int32),
         ("o", c_void_p), ("o_stride_b", c_int64), ("o_stride_h", c_int64),
+        ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+    ]
+
+
+class SpecCommitArgs(Structure):
+    _fields_ = [
+        ("mode", c_int32), ("B", c_int32), ("Hkv", c_int32), ("D", c_int32), ("nq", c_int32), ("Lmax", c_int32),
+        ("kv_dtype", c_int32), ("path_cols", c_int32),
+        ("k", c_void_p), ("v", c_void_p), ("kv_stride_b", c_int64), ("kv_stride_h", c_int64),
+        ("kv_len", c_void_p), ("num_accepted", c_void_p), ("path_nodes", c_void_p), ("path_stride_b", c_int64),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
     ]
 
@@ -110,13 +122,17 @@ def lib() -> ctypes.CDLL:
     L.spec_sample_workspace.restype = c_size_t
     L.spec_sample.argtypes = [POINTER(SpecSampleArgs), c_void_p]
     L.spec_sample.restype = c_int
+    L.spec_commit_workspace.argtypes = [POINTER(SpecCommitArgs)]
+    L.spec_commit_workspace.restype = c_size_t
+    L.spec_commit.argtypes = [POINTER(SpecCommitArgs), c_void_p]
+    L.spec_commit.restype = c_int
     L.spec_status_string.argtypes = [c_int]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
     L.spec_abi_version.restype = c_int
     L.spec_abi_struct_size.argtypes = [c_int]
     L.spec_abi_struct_size.restype = c_size_t
-    for i, cls in enumerate((SpecAttnArgs, SpecWindowArgs, SpecSampleArgs)):
+    for i, cls in enumerate((SpecAttnArgs, SpecWindowArgs, SpecSampleArgs, SpecCommitArgs)):
         if L.spec_abi_struct_size(i) != ctypes.sizeof(cls):
             raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {L.spec_abi_struct_size(i)} "
                                f"bytes, binding {ctypes.sizeof(cls)}")
@@ -357,3 +373,40 @@ def spec_verify_attn_noalloc(q, k, v, kv_len, o, *, tree_parent=None, scale: flo
     if st != SPEC_OK:
         raise SpecError(st, "spec_verify_attn_noalloc")
     return o
+
+
+def commit_args(mode, kv_len, num_accepted, nq, *, k=None, v=None, path_nodes=None, workspace=None):
+    B = kv_len.shape[0]
+    a = SpecCommitArgs(mode=mode, B=B, nq=nq, kv_len=_ptr(kv_len), num_accepted=_ptr(num_accepted),
+                       workspace=_ptr(workspace),
+                       workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+    if k is not None:
+        if k.stride(2) != k.shape[3] or tuple(k.stride()) != tuple(v.stride()):
+            raise ValueError("k and v must share strides with token stride == head_dim")
+        a.Hkv, a.Lmax, a.D = k.shape[1], k.shape[2], k.shape[3]
+        a.kv_dtype = _dtype_code(k)
+        a.k, a.v = _ptr(k), _ptr(v)
+        a.kv_stride_b, a.kv_stride_h = k.stride(0), k.stride(1)
+    else:
+        a.Lmax = 2 ** 31 - 1
+    if path_nodes is not None:
+        a.path_nodes = _ptr(path_nodes)
+        a.path_stride_b = path_nodes.stride(0)
+        a.path_cols = path_nodes.shape[1]
+    return a
+
+
+def spec_commit(mode, kv_len, num_accepted, nq, *, k=None, v=None, path_nodes=None, workspace=None,
+                stream=None):
+    """Rollback after verification: kv_len [B] int32 (device, updated in place), num_accepted [B]
+    int32 (device); SPEC_COMMIT_CHAIN needs nothing else; SPEC_COMMIT_TREE also moves the accepted
+    path's K/V (k, v [B, Hkv, Lmax, D], path_nodes [B, path_cols] int32, e.g. spec_sample's
+    out_path_nodes)."""
+    _check_cuda(kv_len, num_accepted, k, v, path_nodes)
+    ws = _workspace(256, kv_len.device, workspace)
+    a = commit_args(mode, kv_len, num_accepted, nq, k=k, v=v, path_nodes=path_nodes, workspace=ws)
+    st = lib().spec_commit(byref(a), _stream_handle(stream))
+    if st != SPEC_OK:
+        raise SpecError(st, "spec_commit")
+    return ws
+

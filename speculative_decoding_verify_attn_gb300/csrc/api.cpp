@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "commit_internal.h"
 #include "sample_internal.h"
 #include "spec_verify.h"
 
@@ -134,13 +135,14 @@ float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / s
 
 extern "C" {
 
-int spec_abi_version(void) { return 1; }
+int spec_abi_version(void) { return 2; }
 
 size_t spec_abi_struct_size(int which) {
   switch (which) {
     case 0: return sizeof(spec_attn_args);
     case 1: return sizeof(spec_window_args);
     case 2: return sizeof(spec_sample_args);
+    case 3: return sizeof(spec_commit_args);
     default: return 0;
   }
 }
@@ -340,6 +342,41 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
   specv::sample_workspace_carve(a->workspace, &p);
   cudaError_t e = specv::launch_sample(p, sms, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+
+// ------------------------------------------------------------------ spec_commit
+size_t spec_commit_workspace(const spec_commit_args* a) {
+  if (!a) return 0;
+  return 256;
+}
+
+int spec_commit(const spec_commit_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  if (a->mode != SPEC_COMMIT_CHAIN && a->mode != SPEC_COMMIT_TREE) return SPEC_ERR_INVALID_ARG;
+  if (a->B < 1 || a->nq < 1 || a->Lmax < a->nq || !a->kv_len || !a->num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (a->B > 65535) return SPEC_ERR_UNSUPPORTED;
+  if (a->mode == SPEC_COMMIT_TREE) {
+    if (a->nq > specv::kCommitMaxNodes) return SPEC_ERR_UNSUPPORTED;
+    if (a->kv_dtype != SPEC_BF16 && a->kv_dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+    const int bf16 = a->kv_dtype == SPEC_BF16;
+    if (!a->k || !a->v || !a->path_nodes || a->Hkv < 1 || a->D < 2 || a->D > 256 || (a->D % 2)) return SPEC_ERR_INVALID_ARG;
+    if (a->path_cols < 1 || (a->B > 1 && a->path_stride_b < a->path_cols)) return SPEC_ERR_INVALID_ARG;
+    if (a->kv_stride_b < 0 || a->kv_stride_h < 0) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(a->k, 4) || !aligned(a->v, 4)) return SPEC_ERR_INVALID_ARG;
+    if (bf16 && ((a->kv_stride_b % 2) || (a->kv_stride_h % 2))) return SPEC_ERR_INVALID_ARG;
+  }
+  int st = check_workspace(a->workspace, a->workspace_bytes, spec_commit_workspace(a));
+  if (st != SPEC_OK) return st;
+  specv::CommitParams p;
+  memset(&p, 0, sizeof(p));
+  p.mode = a->mode; p.B = a->B; p.Hkv = a->Hkv; p.D = a->D; p.nq = a->nq; p.Lmax = a->Lmax;
+  p.bf16 = a->kv_dtype == SPEC_BF16;
+  p.k = a->k; p.v = a->v; p.kv_sb = a->kv_stride_b; p.kv_sh = a->kv_stride_h;
+  p.kv_len = a->kv_len; p.num_accepted = a->num_accepted;
+  p.path_nodes = a->path_nodes; p.path_sb = a->path_stride_b; p.path_cols = a->path_cols;
+  p.status = reinterpret_cast<uint32_t*>(a->workspace);
+  return specv::launch_commit(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -43,7 +43,9 @@ def test_struct_layouts_match(L):
     assert L.spec_abi_struct_size(0) == ctypes.sizeof(b.SpecAttnArgs)
     assert L.spec_abi_struct_size(1) == ctypes.sizeof(b.SpecWindowArgs)
     assert L.spec_abi_struct_size(2) == ctypes.sizeof(b.SpecSampleArgs)
-    assert L.spec_abi_version() == 1
+    assert L.spec_abi_struct_size(3) == ctypes.sizeof(b.SpecCommitArgs)
+    assert L.spec_abi_struct_size(4) == 0
+    assert L.spec_abi_version() == 2
     assert L.spec_status_string(-3).decode().startswith("workspace")
 
 
@@ -146,3 +148,31 @@ def test_sample_host_validation(L):
     assert call(sample_args(**tree, out_cols=2)) == -1    # depth 2 needs 3 output columns
     bad = np.array([-1, 0, 3, 1, 1, 2], dtype=np.int32)
     assert call(sample_args(**dict(tree, tree_parent=bad.ctypes.data), out_cols=3)) == -1
+
+
+def commit_args(**kw):
+    from speculative_decoding_verify_attn_gb300.binding import SpecCommitArgs
+    a = SpecCommitArgs(mode=1, B=2, Hkv=2, D=128, nq=8, Lmax=100, kv_dtype=1, k=FAKE, v=FAKE,
+                         kv_stride_b=2 * 100 * 128, kv_stride_h=100 * 128, kv_len=FAKE, num_accepted=FAKE,
+                         path_nodes=FAKE, path_stride_b=8, path_cols=5, workspace=FAKE, workspace_bytes=256)
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a
+
+
+def test_commit_host_validation(L):
+    call = lambda a: L.spec_commit(ctypes.byref(a), None)  # noqa: E731
+    assert L.spec_commit_workspace(ctypes.byref(commit_args())) == 256
+    assert call(commit_args(mode=5)) == -1
+    assert call(commit_args(kv_len=None)) == -1
+    assert call(commit_args(num_accepted=None)) == -1
+    assert call(commit_args(path_nodes=None)) == -1
+    assert call(commit_args(path_cols=0)) == -1
+    assert call(commit_args(path_stride_b=4)) == -1           # rows of path_cols = 5 entries
+    assert call(commit_args(nq=65)) == -2                     # trees of at most 64 nodes
+    assert call(commit_args(Lmax=7)) == -1
+    assert call(commit_args(kv_stride_h=100 * 128 + 1)) == -1  # bf16 rows must stay 4-byte aligned
+    assert call(commit_args(D=3)) == -1
+    assert call(commit_args(workspace_bytes=255)) == -3
+    # chain mode needs no K/V at all; only its own fields are validated
+    assert call(commit_args(mode=0, nq=0)) == -1

@@ -104,7 +104,8 @@ def test_tree_commit_brute_force_token_lists():
 
 
 def test_tree_commit_flags_bad_inputs():
-    k = np.zeros((2, 1, 10, 2))
-    path = np.array([[1, 2], [1, -1]])
-    _, _, new, flag = oc.tree_commit(k, k, np.array([12, 10]), 3, path, np.array([2, -1]))
-    assert list(flag) == [True, True] and list(new) == [12, 10]
+    k = np.zeros((4, 1, 10, 2))
+    path = np.array([[1, 2], [1, -1], [1, 5], [1, 2]])
+    _, _, new, flag = oc.tree_commit(k, k, np.array([12, 10, 10, 10]), 3, path, np.array([2, -1, 2, 3]))
+    # kv_len > Lmax; a bad count; a node id outside [1, N); a count above the row (and above N - 1)
+    assert list(flag) == [True, True, True, True] and list(new) == [12, 10, 10, 10]
