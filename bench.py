@@ -431,6 +431,54 @@ def time_steps(runner, K, W, pg, device, use_graphs=True):
                 kernels_per_step=gops.kernels_per_step if use_graphs else None)
 
 
+def time_commit(runner, K, device):
+    """spec_commit after the step, timed alone (CUDA graph replays, events on the stream).  Chain:
+    every draft accepted, so kv_len is unchanged and the op can be replayed as it is.  Tree: the
+    accepted paths of the last sampling call are gathered; each replay first restores kv_len from
+    a copy (a 4-byte-per-sequence device copy, included in the time)."""
+    import torch
+    sv, cfg, inp = runner.sv, runner.cfg, runner.inp
+    stream = torch.cuda.Stream(device=device)
+    kv_len = inp["kv_len"]
+    backup = kv_len.clone()
+    ws = torch.empty(256, dtype=torch.uint8, device=device)
+    if cfg.tree_nodes:
+        mode, nacc = sv.SPEC_COMMIT_TREE, inp["nacc"]
+
+        def op():
+            kv_len.copy_(backup)
+            sv.spec_commit(mode, kv_len, nacc, cfg.nq, k=inp["k"], v=inp["v"], path_nodes=inp["nodes"],
+                           workspace=ws, stream=stream)
+    else:
+        mode = sv.SPEC_COMMIT_CHAIN
+        nacc = torch.full((cfg.B,), cfg.gamma, dtype=torch.int32, device=device)
+
+        def op():
+            sv.spec_commit(mode, kv_len, nacc, cfg.nq, workspace=ws, stream=stream)
+    with torch.cuda.stream(stream):
+        op()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            op()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        kv_len.copy_(backup)
+        stream.synchronize()
+    moved = 0
+    if cfg.tree_nodes:
+        elem = 2 if cfg.kv_dtype == "bf16" else 4
+        moved = int(inp["nacc"].clamp_min(0).sum().item()) * cfg.Hkv * cfg.D * elem * 2 * 2
+    return {"mode": "tree" if cfg.tree_nodes else "chain", "us": 1000 * e0.elapsed_time(e1) / K,
+            "bytes_moved": moved, "includes_kv_len_restore": bool(cfg.tree_nodes)}
+
+
 def time_e2e(runner, K, W, device):
     """The same round through the public API with host buffers: per step, pinned host -> device
     copies of the round's inputs, the six calls, and a device -> host read of the emitted tokens."""
@@ -598,6 +646,7 @@ def main():
         tj = json.load(open(traffic_path))
         if tj.get("workload") == cfg.name and tj.get("kernel_rev") == KERNEL_REV:
             traffic = tj.get("bytes_per_launch")
+    commit = time_commit(runner, 200, device)
     e2e = None
     if not args.no_e2e:
         sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
@@ -625,6 +674,7 @@ def main():
         "draft_window_gbs": (world * nb["window"] * (cfg.draft_steps or 1) / (win_ms * 1e-3) / 1e9) if cfg.window else None,
         "sample_gbs": world * nb["sample"] / (smp_ms * 1e-3) / 1e9,
         "step_breakdown_ms": {"draft_window_x%d" % cfg.draft_steps: win_ms, "verify": ver_ms, "sample": smp_ms},
+        "commit": commit,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
                      "peak_source": peak_kind},

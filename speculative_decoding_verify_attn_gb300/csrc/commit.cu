@@ -2,11 +2,13 @@
 // in LLM Serving Systems", Accepting and rejecting; "Guide to MagicDec", Implementation Step 3;
 // "Speculative Decoding & Medusa" §4, the accepted path of a token tree).
 //
-// One CTA per sequence (it alone reads and then writes kv_len[b]).  Chain: the length drops to
-// the accepted prefix, nothing moves.  Tree: for every kv head the path nodes' K/V rows are first
-// staged in shared memory and only then written to their new positions (sources and destinations
-// of different path nodes overlap: node j moves from kv_len - N + n_j to kv_len - N + 1 + j, and
-// n_j >= j + 1), in 4-byte words.
+// One thread-block cluster per sequence, CTA r of the cluster taking kv heads r, r + CS, ...:
+// chain: the length drops to the accepted prefix, nothing moves.  Tree: for each of its heads a CTA
+// first stages the path nodes' K/V rows in shared memory and only then writes them to their new
+// positions (sources and destinations of different path nodes overlap: node j moves from
+// kv_len - N + n_j to kv_len - N + 1 + j, and n_j >= j + 1), in 4-byte words.  Every CTA reads
+// kv_len[b] first; after a cluster barrier, CTA 0 alone writes it.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -20,7 +22,10 @@ constexpr int kCommitThreads = 256;
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ CommitParams p) {
   extern __shared__ uint32_t s_rows[];  // [2][k][row words]: K rows, then V rows
   __shared__ int s_path[kCommitMaxNodes];
-  const int b = blockIdx.x, tid = threadIdx.x;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int CS = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const int b = blockIdx.x / CS, tid = threadIdx.x;
   const int L = p.kv_len[b];
   const int k = p.num_accepted[b];
   int path_bad = 0;
@@ -33,15 +38,15 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
   int bad = __syncthreads_or(path_bad) ? SPEC_STATUS_BAD_TOKEN : 0;
   if (k < 0 || k > p.nq - 1 || (p.mode == SPEC_COMMIT_TREE && k > p.path_cols)) bad |= SPEC_STATUS_BAD_TOKEN;
   if (L < p.nq || L > p.Lmax) bad |= SPEC_STATUS_BAD_KV_LEN;
-  if (bad) {
-    if (tid == 0) atomicOr(p.status, (uint32_t)bad);
+  if (bad) {  // the same verdict in every CTA of the cluster: none of them writes anything
+    if (tid == 0 && rank == 0) atomicOr(p.status, (uint32_t)bad);
     return;
   }
   const int base = L - p.nq;
   if (p.mode == SPEC_COMMIT_TREE && k > 0) {
     const int words = p.D * (p.bf16 ? 2 : 4) / 4;  // 4-byte words per row
     const int per = k * words;
-    for (int g = 0; g < p.Hkv; ++g) {
+    for (int g = rank; g < p.Hkv; g += CS) {
       const int64_t head = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh;  // elements
       const uint32_t* ks = reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(p.k) +
                                                              head * (p.bf16 ? 2 : 4));
@@ -65,7 +70,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
       __syncthreads();
     }
   }
-  if (tid == 0) p.kv_len[b] = base + 1 + k;
+  cl.sync();  // every CTA of the cluster has read kv_len[b]
+  if (tid == 0 && rank == 0) p.kv_len[b] = base + 1 + k;
 }
 
 size_t commit_smem_bytes(int nq, int D, int bf16) {
@@ -80,7 +86,22 @@ cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream) {
     e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  commit_kernel<<<p.B, kCommitThreads, smem, stream>>>(p);
+  // one CTA per kv head (at most 8 per sequence) in tree mode, one per sequence in chain mode
+  const int cs = p.mode == SPEC_COMMIT_TREE ? (p.Hkv < 8 ? p.Hkv : 8) : 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
+  cfg.blockDim = dim3(kCommitThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, commit_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
