@@ -63,12 +63,12 @@ int build_tree(const int32_t* parent, int N, unsigned long long* anc, int8_t* pa
 }
 
 bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int B, int64_t stride_h,
-                   int64_t stride_b) {
+                   int64_t stride_b, int box_keys = specv::kKeyTile) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)Hkv, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)stride_h * 2, (cuuint64_t)stride_b * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)specv::kKeyTile, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_keys, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -205,8 +205,9 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   CUtensorMap tmK, tmV;
   const int bf16 = a->kv_dtype == SPEC_BF16;
   if (bf16) {
-    if (!encode_kv_map(&tmK, a->k, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b) ||
-        !encode_kv_map(&tmV, a->v, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b))
+    const int box = specv::attn_tile_keys(p.rows, a->D);
+    if (!encode_kv_map(&tmK, a->k, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b, box) ||
+        !encode_kv_map(&tmV, a->v, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b, box))
       return SPEC_ERR_CUDA;
   }
   cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16,
@@ -262,8 +263,9 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
   CUtensorMap tmK, tmV;
   if (bf16) {
-    if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b) ||
-        !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b))
+    const int box = specv::attn_tile_keys(p.rows, a->D);
+    if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box) ||
+        !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box))
       return SPEC_ERR_CUDA;
   }
   cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16, cs);

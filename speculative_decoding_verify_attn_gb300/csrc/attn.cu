@@ -767,6 +767,8 @@ static cudaError_t launch_partial(const AttnParams& p, const CUtensorMap* tmK, c
   }
 }
 
+int attn_tile_keys(int rows, int D) { return (D == 128 && rows > 128) ? kPairTileKeys : kKeyTile; }
+
 cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
                              cudaStream_t stream) {
   AttnParams p = p_in;
@@ -790,6 +792,16 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
     }
     p.tc_groups = (p.rows + 127) / 128;
     p.rows_per_group = (p.rows + p.tc_groups - 1) / p.tc_groups;
+    if (p.tc_groups >= 2) {
+      // pairs of row blocks per CTA (each K/V tile serves up to 256 rows), one record per part
+      const int pairs = (p.tc_groups + 1) / 2;
+      p.nks = 1;
+      p.grid_x = sms / pairs > 0 ? sms / pairs : 1;
+      if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
+      e = launch_partial_tc_pair(p, tmK, tmV, stream);
+      if (e != cudaSuccess) return e;
+      return launch_merge_pair(p, stream);
+    }
     p.nks = kTcSlices;
     p.grid_x = sms / p.tc_groups > 0 ? sms / p.tc_groups : 1;
     if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;

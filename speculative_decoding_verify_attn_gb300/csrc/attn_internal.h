@@ -75,4 +75,15 @@ cudaError_t launch_partial_tc(const AttnParams& p, const CUtensorMap* tmK, const
                               cudaStream_t stream);
 size_t attn_tc_smem_bytes();
 
+// tcgen05 kernel for more than 128 rows per kv head (attn_tc_pair.cu): a pair of 128-row blocks per
+// CTA, Q in TMEM, 64-key tiles (its tensor maps use 64-key boxes); one record per row and part.
+constexpr int kPairTileKeys = 64;
+cudaError_t launch_partial_tc_pair(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                   cudaStream_t stream);
+size_t attn_tc_pair_smem_bytes();
+// merge of the pair kernel's records (column-major o blocks)
+cudaError_t launch_merge_pair(const AttnParams& p, cudaStream_t stream);
+// Keys per TMA box the bf16 tensor maps of a launch need (rows = query rows per kv head).
+int attn_tile_keys(int rows, int D);
+
 }  // namespace specv
