@@ -407,6 +407,7 @@ template <int D, int MASK, int NKS>
 __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ AttnParams p) {
+  pdl_launch_dependents();  // the merge may be scheduled as SMs free up
   constexpr int TILE = kKeyTile * D * 2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * kStages];
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
 // ------------------------------------------------------------------ fp32 partial kernel
 template <int D, int MASK>
 __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ AttnParams p) {
+  pdl_launch_dependents();
   constexpr int PER = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.y * p.rows_per_group;
@@ -555,6 +557,7 @@ __device__ __forceinline__ void load_vec(const float* src, float (&v)[PER]) {
 // per record.
 template <int D>
 __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
+  pdl_wait();  // the partial kernel's records
   constexpr int PER = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -807,8 +810,7 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
     if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
     e = launch_partial_tc(p, tmK, tmV, stream);
     if (e != cudaSuccess) return e;
-    attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(attn_merge<128>, mgrid, dim3(128), 0, stream, 0u, p);
   }
   // row groups of equal size (a multiple of 16), so one key-slice count serves the launch
   const int row_groups = (p.rows + kRowsPerGroup - 1) / kRowsPerGroup;
@@ -832,9 +834,8 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
                   : launch_partial<128>(p, tmK, tmV, kv_bf16, grid, stream);
   if (e != cudaSuccess) return e;
   if (p.direct) return cudaSuccess;
-  if (p.D == 64) attn_merge<64><<<mgrid, 128, 0, stream>>>(p);
-  else attn_merge<128><<<mgrid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return p.D == 64 ? launch_dependent(attn_merge<64>, mgrid, dim3(128), 0, stream, 0u, p)
+                   : launch_dependent(attn_merge<128>, mgrid, dim3(128), 0, stream, 0u, p);
 }
 
 }  // namespace specv

@@ -90,6 +90,7 @@ template <int MASK>
 __global__ void __launch_bounds__(kTcThreads, 1)
     attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ AttnParams p) {
+  pdl_launch_dependents();  // the merge may be scheduled as SMs free up
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kTcStages], empty[kTcStages];
   __shared__ uint64_t sfull[kTcSlices], pfull[kTcSlices], pvdone[kTcSlices], ofree[kTcSlices];

@@ -133,6 +133,7 @@ template <int MASK>
 __global__ void __launch_bounds__(kPThreads, 1)
     attn_partial_tc_pair(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ AttnParams p) {
+  pdl_launch_dependents();  // the merge may be scheduled as SMs free up
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kPStages], empty[kPStages];
   __shared__ uint64_t sfull[2][2], pfull[2][2], pvdone[2], ofree[2], qfull[2], drain[2];
@@ -492,6 +493,7 @@ constexpr int kMergeCols = 8;
 constexpr int kMergeBatch = 8;
 
 __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ AttnParams p) {
+  pdl_wait();  // the partial kernel's records
   __shared__ float tile[kMergeCols][kPRows + 1];  // [column][row]
   const int s = blockIdx.x, blk = blockIdx.y, cc = blockIdx.z;
   const int m = threadIdx.x, warp = m >> 5, lane = m & 31;
@@ -572,8 +574,7 @@ __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ A
 cudaError_t launch_merge_pair(const AttnParams& p, cudaStream_t stream) {
   if (p.D != kPD || p.nks != 1 || p.has_new) return cudaErrorInvalidValue;
   const dim3 grid(p.B * p.Hkv, 2 * ((p.tc_groups + 1) / 2), kPD / kMergeCols);
-  attn_merge_pair<<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(attn_merge_pair, grid, dim3(128), 0, stream, 0u, p);
 }
 
 template <int MASK>

@@ -22,6 +22,41 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  A producer kernel calls pdl_launch_dependents() early so that the
+// next kernel of the stream (launched with launch_dependent) can be scheduled onto SMs as they
+// free up; that kernel calls pdl_wait() before touching anything the producer wrote, which returns
+// once the producer grid has completed and its memory operations are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kern(args...)` as a programmatic dependent of the previous kernel on `stream`; with
+// cluster_x > 0 in thread-block clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // 2^x with the hardware approximation instruction (PTX ex2.approx.ftz.f32; relative error about
 // 2^-22, subnormal results flushed to zero).  Used where the result is rounded to bf16 anyway.
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -318,6 +318,7 @@ constexpr int kWarps = kSampleThreads / 32;
 // logit of the row's draft token when it falls in the item.
 template <bool GREEDY>
 __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_constant__ SampleParams p) {
+  pdl_launch_dependents();  // the finishing kernel may be scheduled as SMs free up
   constexpr int PER = kStatChunk / 128;  // float4 per lane per item
   extern __shared__ float4 s_ring[];     // [kStatWarps][kStatSlots][kStatChunk / 4]
   __shared__ uint64_t s_bar[kStatWarps][kStatSlots];
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_
 // Greedy modes, one CTA per sequence: merges the item argmaxes of its rows and applies the greedy
 // chain or tree rule.
 __global__ void __launch_bounds__(kSampleThreads) sample_finalize(const __grid_constant__ SampleParams p) {
+  pdl_wait();  // the statistics kernel's per-item records
   __shared__ int sa[kMaxTreeNodes > kMaxGamma + 1 ? kMaxTreeNodes : kMaxGamma + 1];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = p.rows_t + p.rows_d;
@@ -590,6 +592,7 @@ __device__ __forceinline__ void slab_scan(const FF* s_slab, int ns, FF& lsum, FF
 // Every CTA takes the same cluster barriers (the decisions that steer them are identical across
 // the cluster).
 __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __grid_constant__ SampleParams p) {
+  pdl_wait();  // the statistics kernel's per-item records
   namespace cg = cooperative_groups;
   extern __shared__ FF s_slab[];      // residual mass of each of this CTA's slabs
   __shared__ float sM[2 * kMaxGamma + 1];
@@ -954,8 +957,7 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   if (p.mode != SPEC_SAMPLE_CHAIN) {
     sample_stats<true><<<g1, kStatWarps * 32, ring, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    sample_finalize<<<p.B, kSampleThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(sample_finalize, dim3(p.B), dim3(kSampleThreads), 0, stream, 0u, p);
   }
   sample_stats<false><<<g1, kStatWarps * 32, ring, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -981,12 +983,8 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
     if (cudaOccupancyMaxActiveClusters(&active, sample_chain_finish, &cfg) == cudaSuccess && active >= p.B) break;
     (void)cudaGetLastError();
   }
-  attr[0].val.clusterDim.x = (unsigned)cs;
-  cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
-  cfg.dynamicSmemBytes = (size_t)((nslabs + cs - 1) / cs) * sizeof(FF);
-  e = cudaLaunchKernelEx(&cfg, sample_chain_finish, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_dependent(sample_chain_finish, dim3((unsigned)(p.B * cs)), dim3(kFinThreads),
+                          (size_t)((nslabs + cs - 1) / cs) * sizeof(FF), stream, (unsigned)cs, p);
 }
 
 cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream) {
