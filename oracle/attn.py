@@ -84,6 +84,25 @@ def verify_attn(q, k, v, kv_len, tree_parent=None, scale: float = 0.0) -> np.nda
     return o
 
 
+def append_new_tokens(k, v, kv_len, k_new, v_new):
+    """The verify step's append ("Speculative Decoding in LLM Serving Systems", The algorithm: the
+    target pass over prefix + drafts extends the target cache; "Guide to MagicDec",
+    Implementation Step 3): the nq new tokens' K/V rows ``k_new[b, j, g]`` go to cache position
+    kv_len[b] - nq + j of head g.  k, v [B, Hkv, Lmax, D]; k_new, v_new [B, nq, Hkv, D].  A
+    sequence with kv_len outside [nq, Lmax] is left as it is.  Returns new arrays."""
+    k = np.array(k, copy=True)
+    v = np.array(v, copy=True)
+    nq, Lmax = k_new.shape[1], k.shape[2]
+    for b in range(k.shape[0]):
+        L = int(kv_len[b])
+        if L < nq or L > Lmax:
+            continue
+        for j in range(nq):
+            k[b, :, L - nq + j, :] = k_new[b, j]
+            v[b, :, L - nq + j, :] = v_new[b, j]
+    return k, v
+
+
 def token_slot(t: int, W: int, n_sinks: int = 0) -> int:
     """Ring slot of token t ([MagicDec] Implementation Step 1, with the attention sinks of Best
     Practices §1): the first n_sinks tokens keep slots 0..n_sinks-1 for good; every later token t

@@ -275,3 +275,43 @@ def test_generators_round_to_storage(dtype):
     # round-to-nearest-even on an exact tie: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7
     assert gen.round_bf16(np.array([1.0 + 2 ** -8], dtype=np.float32))[0] == 1.0
     assert gen.round_bf16(np.array([1.0 + 3 * 2 ** -8], dtype=np.float32))[0] == 1.0 + 2 ** -6
+
+
+def test_append_places_rows_by_hand():
+    """Two sequences, 2 kv heads, nq = 2: sequence 0 (kv_len 5) gets its rows at positions 3 and 4
+    of each head; sequence 1 (kv_len 1 < nq) is left untouched."""
+    B, Hkv, Lmax, D, nq = 2, 2, 6, 3, 2
+    k = np.zeros((B, Hkv, Lmax, D))
+    v = -np.ones((B, Hkv, Lmax, D))
+    k_new = np.arange(B * nq * Hkv * D, dtype=np.float64).reshape(B, nq, Hkv, D) + 1.0
+    v_new = 100.0 + k_new
+    k2, v2 = oa.append_new_tokens(k, v, np.array([5, 1]), k_new, v_new)
+    # sequence 0, head g, position 3 + j holds k_new[0, j, g]; written out element by element
+    assert list(k2[0, 0, 3]) == [1.0, 2.0, 3.0] and list(k2[0, 1, 3]) == [4.0, 5.0, 6.0]
+    assert list(k2[0, 0, 4]) == [7.0, 8.0, 9.0] and list(k2[0, 1, 4]) == [10.0, 11.0, 12.0]
+    assert list(v2[0, 1, 4]) == [110.0, 111.0, 112.0]
+    untouched = np.ones((B, Hkv, Lmax), dtype=bool)
+    untouched[0, :, 3:5] = False
+    assert np.all(k2[untouched] == 0.0) and np.all(v2[untouched] == -1.0)
+    assert np.all(k == 0.0) and np.all(v == -1.0)          # inputs not modified
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_append_then_verify_equals_verify_on_the_written_cache(tree):
+    """Poison the nq tail positions with NaN, append the true rows, verify: the same output as
+    verifying the intact cache (ties the append to the pinned verify oracle)."""
+    B, Hq, Hkv, D, Lmax = 2, 8, 2, 16, 90
+    parent = gen.random_tree(9, 3, 3, 11) if tree else None
+    nq = 9 if tree else 4
+    kv_len = np.array([70, 90], dtype=np.int32)
+    inp = gen.attn_inputs(B, Hq, Hkv, D, nq, kv_len, Lmax, "f32", 5)
+    k_new = np.stack([inp["k"][b][:, kv_len[b] - nq:kv_len[b]].transpose(1, 0, 2) for b in range(B)])
+    v_new = np.stack([inp["v"][b][:, kv_len[b] - nq:kv_len[b]].transpose(1, 0, 2) for b in range(B)])
+    k_bad, v_bad = inp["k"].copy(), inp["v"].copy()
+    for b in range(B):
+        k_bad[b, :, kv_len[b] - nq:kv_len[b]] = np.nan
+        v_bad[b, :, kv_len[b] - nq:kv_len[b]] = np.nan
+    k2, v2 = oa.append_new_tokens(k_bad, v_bad, kv_len, k_new, v_new)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    got = oa.verify_attn(inp["q"], k2, v2, kv_len, tree_parent=parent)
+    assert np.array_equal(got, ref)
