@@ -479,6 +479,43 @@ def time_commit(runner, K, device):
             "bytes_moved": moved, "includes_kv_len_restore": bool(cfg.tree_nodes)}
 
 
+def time_verify_append(runner, K, device):
+    """spec_verify_attn with the fused append of the nq new tokens' K/V, timed like the verify of
+    the step (CUDA graph replays, L2 flushed before each, events on the stream).  k_new, v_new are
+    the rows already at those cache positions, so every replay leaves the cache as it was."""
+    import torch
+    sv, cfg, inp = runner.sv, runner.cfg, runner.inp
+    stream = torch.cuda.Stream(device=device)
+    lens = inp["kv_len"].cpu().tolist()
+    nq = cfg.nq
+    k_new = torch.stack([inp["k"][b, :, L - nq:L].transpose(0, 1) for b, L in enumerate(lens)]).contiguous()
+    v_new = torch.stack([inp["v"][b, :, L - nq:L].transpose(0, 1) for b, L in enumerate(lens)]).contiguous()
+
+    def op():
+        sv.spec_verify_attn(inp["q"], inp["k"], inp["v"], inp["kv_len"], inp["o"], tree_parent=inp["tree"],
+                            workspace=runner.ws_v, stream=stream, k_new=k_new, v_new=v_new)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        op()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            op()
+        for _ in range(3):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+    elem = 2 if cfg.kv_dtype == "bf16" else 4
+    return {"us": 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs])),
+            "bytes_appended": int(2 * cfg.B * nq * cfg.Hkv * cfg.D * elem),
+            "launch": "append kernel + attention in one spec_verify_attn call (one graph)"}
+
+
 def time_e2e(runner, K, W, device):
     """The same round through the public API with host buffers: per step, pinned host -> device
     copies of the round's inputs, the six calls, and a device -> host read of the emitted tokens."""
@@ -647,6 +684,7 @@ def main():
         if tj.get("workload") == cfg.name and tj.get("kernel_rev") == KERNEL_REV:
             traffic = tj.get("bytes_per_launch")
     commit = time_commit(runner, 200, device)
+    verify_append = time_verify_append(runner, max(5, min(args.steps, 50)), device)
     e2e = None
     if not args.no_e2e:
         sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
@@ -675,6 +713,7 @@ def main():
         "sample_gbs": world * nb["sample"] / (smp_ms * 1e-3) / 1e9,
         "step_breakdown_ms": {"draft_window_x%d" % cfg.draft_steps: win_ms, "verify": ver_ms, "sample": smp_ms},
         "commit": commit,
+        "verify_with_append": verify_append,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
                      "peak_source": peak_kind},

@@ -94,6 +94,17 @@ enum {
  *   o  [B, nq, Hq, D]   strides o_stride_b, o_stride_t, o_stride_h
  *   kv_len [B] int32 device
  * Types: kv_dtype SPEC_BF16 (q bf16) or SPEC_F32 (q f32); o_dtype SPEC_F32 or SPEC_BF16.
+ * Fused append ("Speculative Decoding in LLM Serving Systems", the verify step appends the
+ * drafts' K/V to the target cache; "Guide to MagicDec", Implementation Step 3): with k_new and
+ * v_new set, the call first writes the nq new tokens' K/V rows
+ *     k[b, g, kv_len[b] - nq + j, :] = k_new[b, j, g, :]   (and likewise v), j in [0, nq),
+ * on the device, then attends over the updated cache; k and v are written through in that case
+ * (the cache must be writable).  k_new, v_new: type kv_dtype, layout [B, nq, Hkv, D] with
+ * strides new_stride_b, new_stride_t, new_stride_h (elements, innermost contiguous), owned by the
+ * caller; k_new, v_new, k, v 16-byte aligned and all their strides multiples of 16 bytes (else
+ * SPEC_ERR_INVALID_ARG).  A sequence whose kv_len is out of range gets no append (and is flagged
+ * as below).
+ * With k_new == v_new == NULL the caller has already written those rows.
  * Limits: D in {64, 128}; Hq % Hkv == 0; 1 <= B <= 4096; 1 <= nq; nq * (Hq/Hkv) <= 1024;
  *   tree: nq <= 64, tree_parent[0] == -1, 0 <= tree_parent[i] < i for i >= 1.
  *   bf16 K/V: base pointers 16-byte aligned, kv_stride_h and kv_stride_b multiples of 8.
@@ -118,6 +129,9 @@ typedef struct spec_attn_args {
   int64_t o_stride_b, o_stride_t, o_stride_h;
   void* workspace;
   size_t workspace_bytes;
+  const void* k_new;          /* optional fused append (see above), device, or NULL */
+  const void* v_new;
+  int64_t new_stride_b, new_stride_t, new_stride_h;
 } spec_attn_args;
 
 /* Bytes of workspace spec_verify_attn needs for these sizes (host only, pure; reads no

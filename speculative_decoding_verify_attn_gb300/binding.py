@@ -51,6 +51,8 @@ class SpecAttnArgs(Structure):
         ("scale", c_float), ("reserved1", c_int32),
         ("o", c_void_p), ("o_stride_b", c_int64), ("o_stride_t", c_int64), ("o_stride_h", c_int64),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("k_new", c_void_p), ("v_new", c_void_p),
+        ("new_stride_b", c_int64), ("new_stride_t", c_int64), ("new_stride_h", c_int64),
     ]
 
 
@@ -198,12 +200,21 @@ def _host_i32(seq: Optional[Sequence[int]]):
 
 
 # ---------------------------------------------------------------------------- attention
-def verify_attn_args(q, k, v, kv_len, o, tree_parent=None, scale: float = 0.0, workspace=None):
-    """Fill SpecAttnArgs from tensors.  Returns (args, keepalive)."""
+def verify_attn_args(q, k, v, kv_len, o, tree_parent=None, scale: float = 0.0, workspace=None,
+                     k_new=None, v_new=None):
+    """Fill SpecAttnArgs from tensors (k_new, v_new [B, nq, Hkv, D] for the fused append, or
+    None).  Returns (args, keepalive)."""
     B, nq, Hq, D = q.shape
     Hkv, Lmax = k.shape[1], k.shape[2]
     if k.stride(2) != D or v.stride(2) != D or tuple(k.stride()) != tuple(v.stride()):
         raise ValueError("K and V must share strides with token stride == head_dim")
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        if tuple(k_new.shape) != (B, nq, Hkv, D) or tuple(k_new.stride()) != tuple(v_new.stride()):
+            raise ValueError("k_new, v_new must be [B, nq, Hkv, D] with equal strides")
+        if k_new.stride(3) != 1 or k_new.dtype != k.dtype or v_new.dtype != k.dtype:
+            raise ValueError("k_new, v_new: innermost dim contiguous, cache dtype")
     parent_arr, parent_ptr = _host_i32(tree_parent)
     a = SpecAttnArgs(
         B=B, Hq=Hq, Hkv=Hkv, D=D, nq=nq,
@@ -214,6 +225,9 @@ def verify_attn_args(q, k, v, kv_len, o, tree_parent=None, scale: float = 0.0, w
         o=_ptr(o), o_stride_b=o.stride(0), o_stride_t=o.stride(1), o_stride_h=o.stride(2),
         workspace=_ptr(workspace), workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
     )
+    if k_new is not None:
+        a.k_new, a.v_new = _ptr(k_new), _ptr(v_new)
+        a.new_stride_b, a.new_stride_t, a.new_stride_h = k_new.stride(0), k_new.stride(1), k_new.stride(2)
     return a, parent_arr
 
 
@@ -224,17 +238,21 @@ def spec_verify_attn_workspace(q, k, o, nq: Optional[int] = None) -> int:
     return lib().spec_verify_attn_workspace(byref(a))
 
 
-def spec_verify_attn(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0, workspace=None, stream=None):
+def spec_verify_attn(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0, workspace=None, stream=None,
+                     k_new=None, v_new=None):
     """Verify attention (chain if tree_parent is None, else tree; tree_parent is host data).
 
     q [B, nq, Hq, D]; k, v [B, Hkv, Lmax, D]; kv_len [B] int32 (device); o [B, nq, Hq, D].
-    Writes o and returns it."""
+    With k_new, v_new [B, nq, Hkv, D] the call first writes them into cache positions
+    kv_len - nq .. kv_len - 1 (fused append).  Writes o and returns it."""
     _check_cuda(q, k, v, kv_len, o)
+    if k_new is not None:
+        _check_cuda(k_new, v_new)
     need = spec_verify_attn_workspace(q, k, o)
     if need == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_attn_workspace")
     ws = _workspace(need, q.device, workspace)
-    a, keep = verify_attn_args(q, k, v, kv_len, o, tree_parent, scale, ws)
+    a, keep = verify_attn_args(q, k, v, kv_len, o, tree_parent, scale, ws, k_new, v_new)
     st = lib().spec_verify_attn(byref(a), _stream_handle(stream))
     del keep
     if st != SPEC_OK:

@@ -135,7 +135,7 @@ float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / s
 
 extern "C" {
 
-int spec_abi_version(void) { return 2; }
+int spec_abi_version(void) { return 3; }
 
 size_t spec_abi_struct_size(int which) {
   switch (which) {
@@ -178,6 +178,17 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   if ((st = check_o_layout(a->o, a->o_dtype, a->o_stride_b, a->o_stride_t, a->o_stride_h)) != SPEC_OK) return st;
   if (!a->kv_len) return SPEC_ERR_INVALID_ARG;
   if (!isfinite(a->scale)) return SPEC_ERR_INVALID_ARG;
+  if ((a->k_new == nullptr) != (a->v_new == nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (a->k_new) {
+    // the append moves 16-byte chunks: both row sets 16-byte aligned
+    const int64_t el = a->kv_dtype == SPEC_BF16 ? 2 : 4;
+    const int64_t st[5] = {a->new_stride_b, a->new_stride_t, a->new_stride_h, a->kv_stride_b, a->kv_stride_h};
+    for (int64_t x : st)
+      if (x < 0 || (x * el) % 16 != 0) return SPEC_ERR_INVALID_ARG;
+    const uintptr_t ptrs[4] = {(uintptr_t)a->k_new, (uintptr_t)a->v_new, (uintptr_t)a->k, (uintptr_t)a->v};
+    for (uintptr_t x : ptrs)
+      if (x % 16 != 0) return SPEC_ERR_INVALID_ARG;
+  }
   AttnParams p;
   memset(&p, 0, sizeof(p));
   p.mask = specv::kMaskChain;
@@ -200,6 +211,9 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   p.o = a->o; p.o_sb = a->o_stride_b; p.o_st = a->o_stride_t; p.o_sh = a->o_stride_h;
   p.o_bf16 = a->o_dtype == SPEC_BF16;
   p.kv_bf16 = a->kv_dtype == SPEC_BF16;
+  p.verify_append = a->k_new != nullptr;
+  p.k_new = a->k_new; p.v_new = a->v_new;
+  p.new_sb = a->new_stride_b; p.new_st = a->new_stride_t; p.new_sh = a->new_stride_h;
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
 
   CUtensorMap tmK, tmV;

@@ -678,6 +678,32 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
   }
 }
 
+// ------------------------------------------------------------------ verify append
+// The fused append of spec_verify_attn: one warp per (sequence, new token, kv head) row, each lane
+// moving one 16-byte chunk of the K row and of the V row into cache position kv_len - nq + j (no
+// append for an out-of-range kv_len, which the attention kernels flag).  Every row's loads are
+// independent, so the whole append costs about one memory latency.  Runs first in the call, so
+// the attention kernels after it read the updated cache.
+__global__ void __launch_bounds__(128) verify_append_kernel(const __grid_constant__ AttnParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // (b, j, g), g fastest
+  if (row >= (int64_t)p.B * p.nq * p.Hkv) return;
+  const int g = (int)(row % p.Hkv);
+  const int j = (int)((row / p.Hkv) % p.nq);
+  const int b = (int)(row / ((int64_t)p.Hkv * p.nq));
+  const int L = p.lens[b];
+  if (L < p.nq || L > p.Lmax) return;
+  const int elem = p.kv_bf16 ? 2 : 4;
+  if (lane >= p.D * elem / 16) return;
+  const int64_t src = ((int64_t)b * p.new_sb + (int64_t)j * p.new_st + (int64_t)g * p.new_sh) * elem + lane * 16;
+  const int64_t dst =
+      ((int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)(L - p.nq + j) * p.D) * elem + lane * 16;
+  const uint4 kx = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.k_new) + src);
+  const uint4 vx = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.v_new) + src);
+  *reinterpret_cast<uint4*>(reinterpret_cast<char*>(const_cast<void*>(p.k)) + dst) = kx;
+  *reinterpret_cast<uint4*>(reinterpret_cast<char*>(const_cast<void*>(p.v)) + dst) = vx;
+}
+
 // ------------------------------------------------------------------ ring append
 // Separate append, used ahead of the tensor-core partial kernel (which has no replaced-slot mask):
 // one CTA per (sequence, kv head) stores k_new / v_new into the ring slot of token pos - 1.
@@ -785,6 +811,11 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   p.grid_x = sms * per_sm < kMaxGridX ? sms * per_sm : kMaxGridX;
   e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
+  if (p.verify_append) {
+    const int64_t rows = (int64_t)p.B * p.nq * p.Hkv;
+    verify_append_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
   if (kv_bf16 && p.D == 128 && p.rows > 32) {
     // dense query blocks: tcgen05 tiles of 128 rows, one CTA per SM (range x row group)

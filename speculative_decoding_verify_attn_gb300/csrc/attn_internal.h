@@ -57,6 +57,10 @@ struct AttnParams {
   const void* k_new;
   const void* v_new;
   int64_t new_sb, new_sh;
+  // verify with a fused append: the nq new tokens' K/V (k_new, v_new as [B, nq, Hkv, D] with
+  // strides new_sb, new_st, new_sh) go to positions lens[b] - nq .. lens[b] - 1 first
+  int verify_append;
+  int64_t new_st;
   unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
 };
 

@@ -45,7 +45,7 @@ def test_struct_layouts_match(L):
     assert L.spec_abi_struct_size(2) == ctypes.sizeof(b.SpecSampleArgs)
     assert L.spec_abi_struct_size(3) == ctypes.sizeof(b.SpecCommitArgs)
     assert L.spec_abi_struct_size(4) == 0
-    assert L.spec_abi_version() == 2
+    assert L.spec_abi_version() == 3
     assert L.spec_status_string(-3).decode().startswith("workspace")
 
 
@@ -84,6 +84,19 @@ def test_verify_attn_host_validation(L):
     assert call_attn(L, attn_args(workspace=FAKE + 8)) == -3
     assert call_attn(L, attn_args(scale=float("nan"))) == -1
     assert call_attn(L, attn_args(Lmax=3)) == -1                      # cache smaller than nq
+
+
+def test_verify_attn_append_validation(L):
+    """Fused append arguments are checked before any launch (the call would otherwise launch on
+    the fake pointers, so only refusals are exercised here)."""
+    nq, Hkv, D = 5, 2, 128
+    ok = dict(k_new=FAKE + (2 << 30), v_new=FAKE + (3 << 30), new_stride_b=nq * Hkv * D, new_stride_t=Hkv * D,
+              new_stride_h=D)
+    assert call_attn(L, attn_args(**dict(ok, v_new=None))) == -1              # one without the other
+    assert call_attn(L, attn_args(**dict(ok, k_new=FAKE + (2 << 30) + 2))) == -1  # not 16-byte aligned
+    assert call_attn(L, attn_args(**dict(ok, new_stride_t=Hkv * D + 4))) == -1  # 8-byte stride multiple
+    assert call_attn(L, attn_args(**dict(ok, new_stride_h=-D))) == -1
+    assert call_attn(L, attn_args(**dict(ok, kv_dtype=0, q_dtype=0, k=FAKE + 4))) == -1  # f32 cache base
 
 
 def test_tree_validation(L):

@@ -196,3 +196,42 @@ def test_full_size_sampled_outputs(sv, name):
             assert err <= 2e-2 and rel <= 1e-2, (name, b, j, h, err, rel)
     del k, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case", ["llama3-8b-layer", "llama3-70b-layer", "medusa-tree-8k", "tiny"])
+def test_fused_append(sv, case):
+    """spec_verify_attn with k_new/v_new: the new tokens' rows land in the cache (bit-exact, NaN tail
+    before the call), a sequence with an out-of-range kv_len is left alone and flagged, and the
+    output equals the oracle's verify over the appended cache.  Covers the mma, tcgen05, pair and
+    fp32 paths."""
+    torch = torch_mod()
+    cfg = CONFIGS[case]
+    dtype = cfg.kv_dtype
+    parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed) \
+        if cfg.tree_nodes else None
+    nq = cfg.nq
+    kv_len = np.array([700, 333, nq - 1], dtype=np.int32)   # the last one is out of range
+    B, Lmax = len(kv_len), 800
+    inp = gen.attn_inputs(B, cfg.Hq, cfg.Hkv, cfg.D, nq, np.maximum(kv_len, nq), Lmax, dtype, cfg.seed + 3)
+    rng = np.random.default_rng(cfg.seed + 4)
+    k_new = gen.store(rng.standard_normal((B, nq, cfg.Hkv, cfg.D)).astype(np.float32), dtype)
+    v_new = gen.store(rng.standard_normal((B, nq, cfg.Hkv, cfg.D)).astype(np.float32), dtype)
+    k0, v0 = inp["k"].copy(), inp["v"].copy()
+    for b in range(B):
+        lo = max(int(kv_len[b]) - nq, 0)
+        k0[b, :, lo:lo + nq] = np.nan                          # what the append must overwrite
+        v0[b, :, lo:lo + nq] = np.nan
+    dk, dv = to_dev(k0, dtype), to_dev(v0, dtype)
+    q = to_dev(inp["q"], dtype)
+    o = torch.full(q.shape, float("nan"), dtype=torch.float32, device=q.device)
+    ws = torch.empty(sv.spec_verify_attn_workspace(q, dk, o), dtype=torch.uint8, device=q.device)
+    sv.spec_verify_attn(q, dk, dv, to_dev(kv_len, "i32"), o, tree_parent=parent, workspace=ws,
+                        k_new=to_dev(k_new, dtype), v_new=to_dev(v_new, dtype))
+    torch.cuda.synchronize()
+    k2, v2 = oa.append_new_tokens(k0, v0, kv_len, k_new, v_new)
+    assert np.array_equal(to_np(dk), k2.astype(np.float32), equal_nan=True)
+    assert np.array_equal(to_np(dv), v2.astype(np.float32), equal_nan=True)
+    assert sv.read_status(ws) & 1                              # SPEC_STATUS_BAD_KV_LEN for b = 2
+    ref = oa.verify_attn(inp["q"][:2], k2[:2], v2[:2], kv_len[:2], tree_parent=parent)
+    assert_attn_close(to_np(o)[:2], ref, dtype, what=f"fused append {case}")
+    assert np.all(to_np(o)[2] == 0.0)
