@@ -209,3 +209,81 @@ def tree_greedy(target_logits, node_tokens, parent, out_cols: int | None = None)
         out[b, len(path)] = a[b, best]
         nacc[b] = len(path)
     return out, nodes, nacc
+
+
+def tree_stochastic(target_logits, draft_logits, node_tokens, parent, uniforms, out_cols: int | None = None,
+                    band: float = NEAR_BAND):
+    """Stochastic acceptance over a token tree: multi-step speculative sampling.
+
+    The pages name tree verification with sampling (SpecInfer, "Speculative Decoding in LLM
+    Serving Systems", Tree-based variants) but do not state its rule; the reading used here
+    applies the chain rule of "Speculative Decoding & Medusa" §2 to the children of one node in
+    turn, each rejection replacing the target distribution by the normalised residual, as in the
+    chain's resampling step:
+
+    1. At node n (starting at the root, node 0, the last committed token): R = P_n =
+       softmax(target row n); Q_n = softmax(draft row n), the distribution n's children were drawn
+       from.
+    2. For each child c of n in increasing index order, with token x_c: accept iff
+       u_c * Q_n(x_c) < R(x_c) (u_c = uniforms[b, c]; division-free like the chain test).
+       Accepted: emit x_c and continue at step 1 with n = c.  Rejected: R = max(R - Q_n, 0)
+       normalised (R = P_n if that has no mass) and test the next child.
+    3. When no child of n is accepted (a leaf included): draw y from R by inverse CDF in token-id
+       order with u_0 = uniforms[b, 0] (node 0 has no accept test): y = min{y : C(y) > u_0},
+       C the cumulative sum of R; if none qualifies (rounding), the largest y with R_y > 0.
+       Emit y.
+
+    target_logits, draft_logits [B, N, V] fp32 (rows of leaves are not read), node_tokens [B, N],
+    parent [N], uniforms [B, N] in [0, 1).  Returns (out_tokens [B, out_cols], out_path_nodes
+    [B, out_cols], num_accepted [B] (-1: a child token outside [0, V); nothing emitted),
+    near [B] (an evaluated accept test with |u_c - R(x_c)/Q_n(x_c)| <= band, or a final draw
+    with min_y |u_0 - C(y)| <= band)), padded with -1 like tree_greedy.
+    """
+    B, N, V = target_logits.shape
+    depth = tree_depths(parent)
+    if out_cols is None:
+        out_cols = int(depth.max()) + 1
+    tok = np.asarray(node_tokens, dtype=np.int64)
+    u = np.asarray(uniforms, dtype=np.float32).astype(np.float64)
+    children = [[] for _ in range(N)]
+    for i in range(1, N):
+        children[int(parent[i])].append(i)
+    out = np.full((B, out_cols), -1, dtype=np.int32)
+    nodes = np.full((B, out_cols), -1, dtype=np.int32)
+    nacc = np.zeros(B, dtype=np.int32)
+    near = np.zeros(B, dtype=bool)
+    for b in range(B):
+        if np.any((tok[b, 1:] < 0) | (tok[b, 1:] >= V)):
+            nacc[b] = -1
+            continue
+        n, d = 0, 0
+        while True:
+            P = softmax64(target_logits[b, n])
+            R = P
+            moved = False
+            if children[n]:
+                Q = softmax64(draft_logits[b, n])
+                for c in children[n]:
+                    x = int(tok[b, c])
+                    if Q[x] > 0 and R[x] > 0 and abs(u[b, c] - R[x] / Q[x]) <= band:
+                        near[b] = True
+                    if u[b, c] * Q[x] < R[x]:
+                        out[b, d] = x
+                        nodes[b, d] = c
+                        d += 1
+                        n = c
+                        moved = True
+                        break
+                    r = np.maximum(R - Q, 0.0)
+                    R = r / r.sum() if r.sum() > 0 else P
+            if moved:
+                continue
+            C = np.cumsum(R)
+            past = np.nonzero(C > u[b, 0])[0]
+            y = int(past[0]) if len(past) else int(np.nonzero(R > 0)[0][-1])
+            if np.min(np.abs(C - u[b, 0])) <= band:
+                near[b] = True
+            out[b, d] = y
+            nacc[b] = d
+            break
+    return out, nodes, nacc, near
