@@ -516,6 +516,50 @@ def time_verify_append(runner, K, device):
             "launch": "append kernel + attention in one spec_verify_attn call (one graph)"}
 
 
+def time_tree_stochastic(runner, K, device):
+    """spec_sample(SPEC_SAMPLE_TREE) -- stochastic tree acceptance -- on the tree workload's shape
+    (same B, N, V and tree; draft rows correlated 0.8 with the target, children drawn from their
+    parent's draft row), CUDA graph replays with L2 flushed before each, events on the stream."""
+    import torch
+    from workloads import gen
+    sv, cfg, inp = runner.sv, runner.cfg, runner.inp
+    parent = inp["tree"]
+    host = gen.tree_stochastic_inputs(cfg.B, parent, cfg.vocab, cfg.seed + 11)
+    tl = torch.from_numpy(host["target_logits"]).to(device)
+    dl = torch.from_numpy(host["draft_logits"]).to(device)
+    tok = torch.from_numpy(host["node_tokens"]).to(device)
+    u = torch.from_numpy(host["uniforms"]).to(device)
+    cols = int(inp["out"].shape[1])
+    out = torch.empty((cfg.B, cols), dtype=torch.int32, device=device)
+    nodes = torch.empty_like(out)
+    nacc = torch.empty((cfg.B,), dtype=torch.int32, device=device)
+    ws = torch.empty(256, dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def op():
+        sv.spec_sample(sv.SPEC_SAMPLE_TREE, tl, out, nacc, draft_logits=dl, draft_tokens=tok, uniforms=u,
+                       tree_parent=parent, out_path_nodes=nodes, workspace=ws, stream=stream)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        op()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            op()
+        for _ in range(3):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+    us = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    return {"us": us, "rounds_per_s": cfg.B / (us * 1e-6), "mean_accepted": float(nacc.float().mean().item()),
+            "draft_corr": 0.8}
+
+
 def time_e2e(runner, K, W, device):
     """The same round through the public API with host buffers: per step, pinned host -> device
     copies of the round's inputs, the six calls, and a device -> host read of the emitted tokens."""
@@ -685,6 +729,7 @@ def main():
             traffic = tj.get("bytes_per_launch")
     commit = time_commit(runner, 200, device)
     verify_append = time_verify_append(runner, max(5, min(args.steps, 50)), device)
+    tree_sto = time_tree_stochastic(runner, max(5, min(args.steps, 100)), device) if cfg.tree_nodes else None
     e2e = None
     if not args.no_e2e:
         sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
@@ -714,6 +759,7 @@ def main():
         "step_breakdown_ms": {"draft_window_x%d" % cfg.draft_steps: win_ms, "verify": ver_ms, "sample": smp_ms},
         "commit": commit,
         "verify_with_append": verify_append,
+        "tree_stochastic_sample": tree_sto,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
                      "peak_source": peak_kind},

@@ -223,10 +223,21 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  *   committed token) is accepted.  The deepest accepted node d (ties to the smallest index) is
  *   chosen: out_tokens = tokens of the path's nodes at depth 1..depth(d), then argmax of row d;
  *   out_path_nodes (optional) = those node ids; out_num_accepted = depth(d).
+ * SPEC_SAMPLE_TREE (stochastic tree, n = N nodes, tree_parent HOST [N]): multi-step speculative
+ *   sampling -- the chain test applied to a node's children in turn (the pages name SpecInfer's
+ *   tree verification, "Speculative Decoding in LLM Serving Systems", without its rule; this is
+ *   the reading used).  Row n of target_logits is the target after node n (P_n), row n of
+ *   draft_logits the distribution node n's children were drawn from (Q_n; rows of leaves are not
+ *   read); uniforms [B, N].  From node n = 0: R = P_n; for each child c of n in increasing index
+ *   order accept iff uniforms[b, c] * Q_n(x_c) < R(x_c) (x_c = draft_tokens[b, c]) and continue
+ *   at c, else R = max(R - Q_n, 0) normalised (R = P_n if that has no mass) and test the next
+ *   child.  When no child is accepted, y is drawn from R by inverse CDF with uniforms[b, 0] as in
+ *   the chain mode.  Outputs as in SPEC_SAMPLE_TREE_GREEDY (path tokens, then y).
  *
  * Layout: logits rows are V contiguous fp32; target_logits [B, rows_t, V] with batch stride
- *   tl_stride_b (rows_t = gamma+1 chain, N tree); draft_logits [B, gamma, V] (dl_stride_b);
- *   draft_tokens [B, gamma] or [B, N] int32 (tok_stride_b); uniforms [B, gamma+1] fp32 in [0, 1)
+ *   tl_stride_b (rows_t = gamma+1 chain, N tree); draft_logits [B, gamma, V] or [B, N, V]
+ *   (dl_stride_b); draft_tokens [B, gamma] or [B, N] int32 (tok_stride_b); uniforms [B, gamma+1]
+ *   or [B, N] fp32 in [0, 1)
  *   (u_stride_b); out_tokens / out_path_nodes [B, out_cols] int32 (row stride out_cols);
  *   out_num_accepted [B] int32.
  * Limits: V % 4 == 0, logits pointers 16-byte aligned and tl/dl strides multiples of 4;
@@ -235,7 +246,7 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  * Floating point: exponentials in fp32, every sum above a thread's own few elements in fp64; the
  * accept ratio uses fp64 exponentials of the two selected logits.
  * ---------------------------------------------------------------------------------------- */
-enum { SPEC_SAMPLE_CHAIN = 0, SPEC_SAMPLE_CHAIN_GREEDY = 1, SPEC_SAMPLE_TREE_GREEDY = 2 };
+enum { SPEC_SAMPLE_CHAIN = 0, SPEC_SAMPLE_CHAIN_GREEDY = 1, SPEC_SAMPLE_TREE_GREEDY = 2, SPEC_SAMPLE_TREE = 3 };
 
 typedef struct spec_sample_args {
   int32_t mode, B, n, V;

@@ -38,6 +38,7 @@ SPEC_COMMIT_TREE = 1
 SPEC_SAMPLE_CHAIN = 0
 SPEC_SAMPLE_CHAIN_GREEDY = 1
 SPEC_SAMPLE_TREE_GREEDY = 2
+SPEC_SAMPLE_TREE = 3
 
 
 class SpecAttnArgs(Structure):
@@ -311,10 +312,7 @@ def spec_draft_window_attn(q, k_ring, v_ring, pos, o, *, k_new=None, v_new=None,
 def sample_args(mode, target_logits, out_tokens, out_num_accepted, *, draft_logits=None, draft_tokens=None,
                 uniforms=None, tree_parent=None, out_path_nodes=None, workspace=None):
     B, rows, V = target_logits.shape
-    if mode == SPEC_SAMPLE_TREE_GREEDY:
-        n = rows
-    else:
-        n = rows - 1
+    n = rows if mode in (SPEC_SAMPLE_TREE_GREEDY, SPEC_SAMPLE_TREE) else rows - 1
     parent_arr, parent_ptr = _host_i32(tree_parent)
     for t in (target_logits, draft_logits):
         if t is not None and t.stride(1) != V:
@@ -335,17 +333,18 @@ def sample_args(mode, target_logits, out_tokens, out_num_accepted, *, draft_logi
 
 def spec_sample_workspace(mode, target_logits, tree_parent=None) -> int:
     B, rows, V = target_logits.shape
-    n = rows if mode == SPEC_SAMPLE_TREE_GREEDY else rows - 1
+    n = rows if mode in (SPEC_SAMPLE_TREE_GREEDY, SPEC_SAMPLE_TREE) else rows - 1
     a = SpecSampleArgs(mode=mode, B=B, n=n, V=V)
     return lib().spec_sample_workspace(byref(a))
 
 
 def spec_sample(mode, target_logits, out_tokens, out_num_accepted, *, draft_logits=None, draft_tokens=None,
                 uniforms=None, tree_parent=None, out_path_nodes=None, workspace=None, stream=None):
-    """Speculative sampling (SPEC_SAMPLE_CHAIN), greedy chain or greedy tree selection.
+    """Speculative sampling (SPEC_SAMPLE_CHAIN), greedy chain, greedy tree or stochastic tree
+    (SPEC_SAMPLE_TREE) selection.
 
-    target_logits [B, gamma+1 | N, V] fp32; draft_logits [B, gamma, V] fp32 (chain);
-    draft_tokens [B, gamma] or node tokens [B, N] int32; uniforms [B, gamma+1] fp32 (chain);
+    target_logits [B, gamma+1 | N, V] fp32; draft_logits [B, gamma | N, V] fp32 (stochastic);
+    draft_tokens [B, gamma] or node tokens [B, N] int32; uniforms [B, gamma+1 | N] fp32 (stochastic);
     tree_parent host [N] (tree); out_tokens [B, out_cols] int32; out_num_accepted [B] int32."""
     _check_cuda(target_logits, draft_logits, draft_tokens, uniforms, out_tokens, out_num_accepted, out_path_nodes)
     need = spec_sample_workspace(mode, target_logits, tree_parent)

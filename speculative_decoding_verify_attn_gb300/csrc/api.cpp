@@ -301,6 +301,10 @@ static int sample_rows(const spec_sample_args* a, int* rows_t, int* rows_d) {
       if (a->n < 1 || a->n > specv::kMaxTreeNodes) return SPEC_ERR_UNSUPPORTED;
       *rows_t = a->n; *rows_d = 0;
       return SPEC_OK;
+    case SPEC_SAMPLE_TREE:
+      if (a->n < 1 || a->n > specv::kMaxTreeNodes) return SPEC_ERR_UNSUPPORTED;
+      *rows_t = a->n; *rows_d = a->n;
+      return SPEC_OK;
     default: return SPEC_ERR_INVALID_ARG;
   }
 }
@@ -324,7 +328,7 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
   if (!a->target_logits || !aligned(a->target_logits, 16) || a->tl_stride_b < 0 || (a->tl_stride_b % 4))
     return SPEC_ERR_INVALID_ARG;
   if (!a->out_tokens || !a->out_num_accepted) return SPEC_ERR_INVALID_ARG;
-  if (a->mode == SPEC_SAMPLE_CHAIN) {
+  if (a->mode == SPEC_SAMPLE_CHAIN || a->mode == SPEC_SAMPLE_TREE) {
     if (!a->draft_logits || !aligned(a->draft_logits, 16) || a->dl_stride_b < 0 || (a->dl_stride_b % 4))
       return SPEC_ERR_INVALID_ARG;
     if (!a->uniforms || a->u_stride_b < 0) return SPEC_ERR_INVALID_ARG;
@@ -333,7 +337,8 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
     return SPEC_ERR_INVALID_ARG;
   SampleParams p;
   memset(&p, 0, sizeof(p));
-  if (a->mode == SPEC_SAMPLE_TREE_GREEDY) {
+  const bool tree = a->mode == SPEC_SAMPLE_TREE_GREEDY || a->mode == SPEC_SAMPLE_TREE;
+  if (tree) {
     const int maxd = build_tree(a->tree_parent, a->n, nullptr, p.parent, p.depth);
     if (maxd < 0) return SPEC_ERR_INVALID_ARG;
     if (a->out_cols < maxd + 1) return SPEC_ERR_INVALID_ARG;
@@ -347,7 +352,7 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
   if (sms <= 0) return SPEC_ERR_CUDA;
 
   p.mode = a->mode; p.B = a->B; p.V = a->V;
-  p.gamma = a->mode == SPEC_SAMPLE_TREE_GREEDY ? 0 : a->n;
+  p.gamma = tree ? 0 : a->n;
   p.rows_t = rt; p.rows_d = rd;
   p.tl = a->target_logits; p.tl_sb = a->tl_stride_b;
   p.dl = a->draft_logits; p.dl_sb = a->dl_stride_b;

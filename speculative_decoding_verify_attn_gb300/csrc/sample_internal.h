@@ -49,5 +49,7 @@ struct SampleParams {
 size_t sample_workspace_bytes(int mode, int B, int rows_t, int rows_d, int V);
 void sample_workspace_carve(void* ws, SampleParams* p);
 cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream);
+// stochastic tree walk (sample_tree.cu), one CTA per sequence
+cudaError_t launch_sample_tree(const SampleParams& p, cudaStream_t stream);
 
 }  // namespace specv

@@ -15,7 +15,8 @@ from __future__ import annotations
 import numpy as np
 
 SUB = dict(q=1, k=2, v=3, kv_len=4, tree=5, target=6, draft=7, tokens=8, uniforms=9,
-           ring_k=10, ring_v=11, new_k=12, new_v=13, pos=14, needles=15, gumbel=16, tree_tok=17)
+           ring_k=10, ring_v=11, new_k=12, new_v=13, pos=14, needles=15, gumbel=16, tree_tok=17,
+           tree_gumbel=18)
 
 BF16_NAN = np.float32(np.nan)
 
@@ -215,3 +216,22 @@ def tree_sample_inputs(B: int, parent: np.ndarray, V: int, seed: int, target_sig
             for c, tid in zip(kids, ids):
                 tok[b, c] = tid
     return dict(target_logits=t, node_tokens=tok)
+
+
+def tree_stochastic_inputs(B: int, parent: np.ndarray, V: int, seed: int, target_sigma: float = 2.0,
+                           draft_corr: float = 0.8) -> dict:
+    """Inputs of the stochastic tree step: target_logits, draft_logits [B, N, V] fp32 (draft
+    correlated with target at ``draft_corr``), node_tokens [B, N] with each child's token drawn
+    from its parent's draft row (Gumbel-max, i.i.d. per child; node 0's token is arbitrary),
+    uniforms [B, N] in [0, 1) fp32."""
+    N = len(parent)
+    z = rng_for(seed, "target").standard_normal((B, N, V), dtype=np.float32)
+    t = (target_sigma * z).astype(np.float32)
+    eps = rng_for(seed, "draft").standard_normal((B, N, V), dtype=np.float32)
+    d = (target_sigma * (draft_corr * z + np.sqrt(1.0 - draft_corr ** 2) * eps)).astype(np.float32)
+    r = rng_for(seed, "tree_gumbel")
+    tok = np.zeros((B, N), dtype=np.int32)
+    for c in range(1, N):
+        tok[:, c] = gumbel_max_draw(d[:, int(parent[c])], r)
+    u = rng_for(seed, "uniforms").random((B, N), dtype=np.float32)
+    return dict(target_logits=t, draft_logits=d, node_tokens=tok, uniforms=u)
