@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      // every K/V tile is read once: let it leave L2 first (the records and Q stay)
+      const uint64_t pol = l2_policy_evict_first();
       int t = 0;
       bool ok = true;
       int b, g, kb, ke, len;
@@ -202,8 +204,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           mbar_arrive_expect_tx(&full[s], 2u * kPTile);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            tma_load_4d(sk + h * kPHalf, &tmK, &full[s], h * 64, key0, g, b);
-            tma_load_4d(sk + kPTile + h * kPHalf, &tmV, &full[s], h * 64, key0, g, b);
+            tma_load_4d_hint(sk + h * kPHalf, &tmK, &full[s], h * 64, key0, g, b, pol);
+            tma_load_4d_hint(sk + kPTile + h * kPHalf, &tmV, &full[s], h * 64, key0, g, b, pol);
           }
         }
       }
