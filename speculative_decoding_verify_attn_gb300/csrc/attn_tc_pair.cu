@@ -487,18 +487,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 // Merge of the pair kernel's records: grid (segments, 2 * pairs row blocks, D / 8 column chunks),
-// 128 threads, thread m = row m of the block.  The records of a row are read in batches of eight
+// 128 threads, thread m = row m of the block.  The records of a row are read in batches of six
 // with all their loads in flight at once: first the (m, l) pairs, then the o columns of the
-// column-major blocks (one 32-byte sector per column and warp).  The 8-column result is turned
-// around in shared memory so that each output row chunk is one 32-byte store.
+// column-major blocks (one 128-byte line per column and warp).  Each thread then stores its row's
+// 8 columns, one 32-byte chunk of the output row.
 constexpr int kMergeCols = 8;
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 6;
 
 __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ AttnParams p) {
   pdl_wait();  // the partial kernel's records
-  __shared__ float tile[kMergeCols][kPRows + 1];  // [column][row]
   const int s = blockIdx.x, blk = blockIdx.y, cc = blockIdx.z;
-  const int m = threadIdx.x, warp = m >> 5, lane = m & 31;
+  const int m = threadIdx.x;
   const int b = s / p.Hkv, g = s % p.Hkv;
   const int nblk = 2 * ((p.tc_groups + 1) / 2);
   const int row0 = blk * p.rows_per_group;
@@ -517,36 +516,61 @@ __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ A
     const int64_t start = cum_b + (int64_t)g * ntiles;
     const int c0 = (int)(start / per), nrec = (int)((start + ntiles - 1) / per) - c0 + 1;
     const float2* ml_row = p.part_ml + (int64_t)(s + c0) * p.rows + rr;
-    float M = neg_inf();
-    for (int i0 = 0; i0 < nrec; i0 += kMergeBatch) {
+    const float* o_row = p.part_o + ((int64_t)(s + c0) * nblk + blk) * (int64_t)(kPD * kPRows) +
+                         (cc * kMergeCols) * kPRows + m;
+    const int64_t rec_stride = (int64_t)nblk * kPD * kPRows;
+    float L = 0.f;
+    if (nrec <= kMergeBatch) {
+      // the usual case: every (m, l) pair and o column of the row in flight at once
       float2 ml[kMergeBatch];
+      float v[kMergeBatch][kMergeCols];
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u)
-        ml[u] = i0 + u < nrec ? ml_row[(int64_t)(i0 + u) * p.rows] : make_float2(neg_inf(), 0.f);
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const bool in = u < nrec;
+        ml[u] = in ? ml_row[(int64_t)u * p.rows] : make_float2(neg_inf(), 0.f);
+#pragma unroll
+        for (int e = 0; e < kMergeCols; ++e) v[u][e] = in ? o_row[u * rec_stride + e * kPRows] : 0.f;
+      }
+      float M = neg_inf();
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) M = fmaxf(M, ml[u].x);
-    }
-    float L = 0.f;
-    if (M != neg_inf()) {
-      const float* o_row = p.part_o + ((int64_t)(s + c0) * nblk + blk) * (int64_t)(kPD * kPRows) +
-                           (cc * kMergeCols) * kPRows + m;
-      const int64_t rec_stride = (int64_t)nblk * kPD * kPRows;
-      for (int i0 = 0; i0 < nrec; i0 += kMergeBatch) {
-        float2 ml[kMergeBatch];
-        float v[kMergeBatch][kMergeCols];
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          const bool in = i0 + u < nrec;
-          ml[u] = in ? ml_row[(int64_t)(i0 + u) * p.rows] : make_float2(neg_inf(), 0.f);
-#pragma unroll
-          for (int e = 0; e < kMergeCols; ++e) v[u][e] = in ? o_row[(i0 + u) * rec_stride + e * kPRows] : 0.f;
-        }
+      if (M != neg_inf()) {
 #pragma unroll
         for (int u = 0; u < kMergeBatch; ++u) {
           const float w = ml[u].x == neg_inf() ? 0.f : exp2f(ml[u].x - M);
           L += w * ml[u].y;
 #pragma unroll
           for (int e = 0; e < kMergeCols; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+        }
+      }
+    } else {
+      float M = neg_inf();
+      for (int i0 = 0; i0 < nrec; i0 += kMergeBatch) {
+        float2 ml[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u)
+          ml[u] = i0 + u < nrec ? ml_row[(int64_t)(i0 + u) * p.rows] : make_float2(neg_inf(), 0.f);
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) M = fmaxf(M, ml[u].x);
+      }
+      if (M != neg_inf()) {
+        for (int i0 = 0; i0 < nrec; i0 += kMergeBatch) {
+          float2 ml[kMergeBatch];
+          float v[kMergeBatch][kMergeCols];
+#pragma unroll
+          for (int u = 0; u < kMergeBatch; ++u) {
+            const bool in = i0 + u < nrec;
+            ml[u] = in ? ml_row[(int64_t)(i0 + u) * p.rows] : make_float2(neg_inf(), 0.f);
+#pragma unroll
+            for (int e = 0; e < kMergeCols; ++e) v[u][e] = in ? o_row[(i0 + u) * rec_stride + e * kPRows] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < kMergeBatch; ++u) {
+            const float w = ml[u].x == neg_inf() ? 0.f : exp2f(ml[u].x - M);
+            L += w * ml[u].y;
+#pragma unroll
+            for (int e = 0; e < kMergeCols; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+          }
         }
       }
     }
@@ -556,20 +580,34 @@ __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ A
   } else if (len <= 0 && m == 0 && g == 0 && blk == 0 && cc == 0) {
     atomicOr(p.status, p.is_window ? (uint32_t)SPEC_STATUS_BAD_POS : (uint32_t)SPEC_STATUS_BAD_KV_LEN);
   }
+  // the row's 8 columns are one 32-byte chunk of the output row: written by this thread
+  if (real) {
+    const int j = rr / p.G, h = g * p.G + rr % p.G;
+    const int64_t off = (int64_t)b * p.o_sb + (int64_t)j * p.o_st + (int64_t)h * p.o_sh + cc * kMergeCols;
+    // vector stores where the caller's layout makes the chunk 16-byte aligned, else scalar ones
+    if (p.o_bf16) {
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) + off;
+      if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        uint4 v;
+        v.x = pack_bf16(acc[0], acc[1]);
+        v.y = pack_bf16(acc[2], acc[3]);
+        v.z = pack_bf16(acc[4], acc[5]);
+        v.w = pack_bf16(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(dst) = v;
+      } else {
 #pragma unroll
-  for (int e = 0; e < kMergeCols; ++e) tile[e][m] = acc[e];
-  __syncthreads();
-  // warp w writes rows 32 w .. 32 w + 31, four rows of eight columns per store
-  const int col = lane & (kMergeCols - 1);
-  for (int r = warp * 32 + (lane >> 3); r < warp * 32 + 32; r += 4) {
-    if (r >= rows_here) break;
-    const int row = row0 + r;
-    const int j = row / p.G, h = g * p.G + row % p.G;
-    const int64_t off =
-        (int64_t)b * p.o_sb + (int64_t)j * p.o_st + (int64_t)h * p.o_sh + cc * kMergeCols + col;
-    const float v = tile[col][r];
-    if (p.o_bf16) reinterpret_cast<__nv_bfloat16*>(p.o)[off] = __float2bfloat16_rn(v);
-    else reinterpret_cast<float*>(p.o)[off] = v;
+        for (int e = 0; e < kMergeCols; ++e) dst[e] = __float2bfloat16_rn(acc[e]);
+      }
+    } else {
+      float* dst = reinterpret_cast<float*>(p.o) + off;
+      if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kMergeCols; ++e) dst[e] = acc[e];
+      }
+    }
   }
 }
 
