@@ -786,7 +786,7 @@ def main():
 
 
 # Revision tag of the verify kernel that profiles/verify_traffic.json was measured on.
-KERNEL_REV = "mma8w-kt128-v2"
+KERNEL_REV = "mma8w-kt128-v3"
 
 if __name__ == "__main__":
     sys.exit(main())
