@@ -580,8 +580,21 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
     const int nks = p.nks;
     const int nrec = (c1 - c0 + 1) * nks;  // per CTA that took part of the segment: one per key slice
     auto rec_of = [&](int i) -> int64_t { return ((int64_t)(s + c0 + i / nks) * nks + i % nks) * p.rows + r; };
-    float M = neg_inf();
-    for (int i = lane; i < nrec; i += 32) M = fmaxf(M, p.part_ml[rec_of(i)].x);
+    // (m, l) of records lane, lane + 32, ...; the o columns of the first eight records are
+    // loaded in the same round trip (most rows have at most eight records)
+    const float2 ml0 = lane < nrec ? p.part_ml[rec_of(lane)] : make_float2(neg_inf(), 0.f);
+    float v0[8][PER];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (u < nrec) {
+        load_vec<PER>(p.part_o + rec_of(u) * D + e0, v0[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) v0[u][i] = 0.f;
+      }
+    }
+    float M = ml0.x;
+    for (int i = lane + 32; i < nrec; i += 32) M = fmaxf(M, p.part_ml[rec_of(i)].x);
     M = warp_max(M);
     // the window's new key: score q . k_new (log2 units), weight 1 relative to itself
     float s_new = neg_inf(), kn[PER], vn[PER];
@@ -603,7 +616,7 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
       for (int i0 = 0; i0 < nrec; i0 += 32) {
         float wgt = 0.f, lw = 0.f;
         if (i0 + lane < nrec) {
-          const float2 ml = p.part_ml[rec_of(i0 + lane)];
+          const float2 ml = i0 == 0 ? ml0 : p.part_ml[rec_of(i0 + lane)];
           wgt = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
           lw = wgt * ml.y;
         }
@@ -612,9 +625,13 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
         // eight records' loads in flight at once, then their weighted sum in record order
         for (int t0 = 0; t0 < n; t0 += 8) {
           float v[8][PER];
+          const bool first = i0 == 0 && t0 == 0;  // already in flight with the (m, l) loads
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            if (t0 + u < n) {
+            if (first) {
+#pragma unroll
+              for (int i = 0; i < PER; ++i) v[u][i] = v0[u][i];
+            } else if (t0 + u < n) {
               load_vec<PER>(p.part_o + rec_of(i0 + t0 + u) * D + e0, v[u]);
             } else {
 #pragma unroll
