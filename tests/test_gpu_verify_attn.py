@@ -235,3 +235,32 @@ def test_fused_append(sv, case):
     ref = oa.verify_attn(inp["q"][:2], k2[:2], v2[:2], kv_len[:2], tree_parent=parent)
     assert_attn_close(to_np(o)[:2], ref, dtype, what=f"fused append {case}")
     assert np.all(to_np(o)[2] == 0.0)
+
+
+@pytest.mark.parametrize("layout", ["bf16", "f32-offset"])
+def test_tree_pair_output_layouts(sv, layout):
+    """The pair kernel's merge stores 8-column row chunks with 16-byte stores where the output
+    layout allows it and element stores otherwise: bf16 output, and an fp32 output view whose
+    rows start 4 bytes past a 16-byte boundary (strides of a wider tensor)."""
+    torch = torch_mod()
+    cfg = CONFIGS["medusa-tree-8k"]
+    parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+    kv_len = np.array([900, 611], dtype=np.int32)
+    B, nq = 2, cfg.tree_nodes
+    inp = gen.attn_inputs(B, cfg.Hq, cfg.Hkv, cfg.D, nq, kv_len, 1000, "bf16", cfg.seed + 9)
+    q, k, v = to_dev(inp["q"], "bf16"), to_dev(inp["k"], "bf16"), to_dev(inp["v"], "bf16")
+    if layout == "bf16":
+        o = torch.full((B, nq, cfg.Hq, cfg.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        view = o
+    else:
+        o = torch.full((B, nq, cfg.Hq, cfg.D + 3), float("nan"), dtype=torch.float32, device="cuda")
+        view = o[..., 1:cfg.D + 1]
+    ws = torch.empty(sv.spec_verify_attn_workspace(q, k, view), dtype=torch.uint8, device="cuda")
+    sv.spec_verify_attn(q, k, v, to_dev(kv_len, "i32"), view, tree_parent=parent, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    assert sv.read_status(ws) == 0
+    assert_attn_close(to_np(view.float()), ref, "bf16", "bf16" if layout == "bf16" else "f32", what=f"pair {layout}")
+    if layout != "bf16":   # the padding columns around the view are untouched
+        pad = to_np(o)[..., [0, cfg.D + 1, cfg.D + 2]]
+        assert np.all(np.isnan(pad))
