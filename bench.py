@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling a small case)")
+    ap.add_argument("--clocks-csv", default=None, help="write the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--no-graphs", action="store_true", help="issue every call eagerly instead of graph replays")
     ap.add_argument("--sinks", type=int, default=0, help="attention-sink slots at the front of the draft ring")
     a = ap.parse_args()
@@ -110,11 +111,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, csv_path=None):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None
+        self.path = csv_path      # optional: keep the raw samples of the timed region
 
     def start(self):
         try:
@@ -368,7 +368,7 @@ class GraphOps:
         self.g["sample"].replay()
 
 
-def time_steps(runner, K, W, pg, device, use_graphs=True):
+def time_steps(runner, K, W, pg, device, use_graphs=True, clocks_csv=None):
     """K timed steps bracketed by barrier + synchronize; per-op CUDA events on the launching stream."""
     import torch
     cfg = runner.cfg
@@ -399,7 +399,7 @@ def time_steps(runner, K, W, pg, device, use_graphs=True):
         flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     barrier(pg, device)
     torch.cuda.synchronize()
-    clocks = ClockSampler(device.index)
+    clocks = ClockSampler(device.index, clocks_csv)
     clocks.start()
     t0 = time.perf_counter()
     start.record(stream)
@@ -712,7 +712,8 @@ def main():
     runner = Runner(sv, cfg, inp, device)
     runner.n_sinks = args.sinks
     nb = step_bytes(cfg, inp)
-    t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs)
+    t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs,
+                   clocks_csv=args.clocks_csv)
     total_ms = max_over_ranks(pg, t["total_ms"], device)
     ver_ms = max_over_ranks(pg, t["verify_ms"], device)
     smp_ms = max_over_ranks(pg, t["sample_ms"], device)

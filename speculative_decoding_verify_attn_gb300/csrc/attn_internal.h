@@ -80,7 +80,8 @@ cudaError_t launch_partial_tc(const AttnParams& p, const CUtensorMap* tmK, const
 size_t attn_tc_smem_bytes();
 
 // tcgen05 kernel for more than 128 rows per kv head (attn_tc_pair.cu): a pair of 128-row blocks per
-// CTA, Q in TMEM, 64-key tiles (its tensor maps use 64-key boxes); one record per row and part.
+// CTA, Q in shared memory, two S buffers and O per block in TMEM, 64-key tiles (its tensor maps
+// use 64-key boxes); one record per row and part, o as column-major [D][128] blocks.
 constexpr int kPairTileKeys = 64;
 cudaError_t launch_partial_tc_pair(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                    cudaStream_t stream);
