@@ -355,10 +355,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           float mx[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
           if (!edge) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(ua[e]));
-              mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(ub[e]));
-            }
+            for (int e = 0; e < 32; ++e)
+              mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(ua[e]), __uint_as_float(ub[e]));
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -409,9 +407,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (!edge) {
 #pragma unroll
               for (int e = 0; e < 32; e += 2) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(u[e]), sc, -mu));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(u[e + 1]), sc, -mu));
-                sums[(e >> 1) & 3] += p0 + p1;
+                float x0, x1;
+                fma2(__uint_as_float(u[e]), __uint_as_float(u[e + 1]), sc, -mu, x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                add2(sums[(e >> 1) & 1], sums[2 + ((e >> 1) & 1)], p0, p1);
                 pk[e / 2] = pack_bf16(p0, p1);
               }
             } else {

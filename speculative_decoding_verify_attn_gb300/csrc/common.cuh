@@ -57,6 +57,30 @@ inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 bloc
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Blackwell packed and three-input fp32 forms (PTX fma/add .f32x2, three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (a0, a1) * (b, b) + (c, c), both lanes rounded to nearest
+__device__ __forceinline__ void fma2(float a0, float a1, float b, float c, float& d0, float& d1) {
+  unsigned long long a, bb, cc, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(bb), "l"(cc));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+// (s0, s1) += (a0, a1)
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  unsigned long long s, a, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(s) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(s), "l"(a));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(d));
+}
+
 // 2^x with the hardware approximation instruction (PTX ex2.approx.ftz.f32; relative error about
 // 2^-22, subnormal results flushed to zero).  Used where the result is rounded to bf16 anyway.
 __device__ __forceinline__ float ex2_approx(float x) {
