@@ -21,4 +21,4 @@ Every function is pinned by ``tests/test_oracle_*.py`` against closed forms, inv
 brute force and hand-worked fixtures (``tests/golden/``), not against itself.
 """
 
-from . import attn, commit, sample  # noqa: F401
+from . import attn, commit, lmhead, sample  # noqa: F401

@@ -1,0 +1,62 @@
+"""Pins for the fused LM-head + greedy oracle (CPU only): brute-force dot products, planted
+argmaxes that the greedy rules must follow through (chain: every draft accepted; tree: the
+first-child chain), and the near-tie flag on constructed ties."""
+
+import numpy as np
+
+from oracle import lmhead as ol
+from oracle import sample as osm
+from workloads import gen
+
+
+def test_logits_brute_force():
+    rng = np.random.default_rng(1)
+    h = rng.standard_normal((2, 3, 5))
+    w = rng.standard_normal((7, 5))
+    lg = ol.lmhead_logits(h, w)
+    for b in range(2):
+        for r in range(3):
+            for v in range(7):
+                assert abs(lg[b, r, v] - sum(h[b, r, k] * w[v, k] for k in range(5))) < 1e-12
+
+
+def test_planted_chain_accepts_every_draft():
+    """Row i's argmax is the planted token of row i + 1, so all gamma drafts are accepted and the
+    emitted token is the argmax of the last row."""
+    B, gamma, d, V = 6, 4, 512, 3000
+    inp = gen.lmhead_inputs(B, gamma + 1, d, V, 11, plant=1.0)
+    out, k, near = ol.lmhead_greedy_chain(inp["hidden"], inp["weight"], inp["tokens"][:, 1:])
+    lg = ol.lmhead_logits(inp["hidden"], inp["weight"])
+    assert not near.any()
+    assert np.all(k == gamma)
+    for b in range(B):
+        assert list(out[b, :gamma]) == list(inp["tokens"][b, 1:])
+        assert out[b, gamma] == int(np.argmax(lg[b, gamma]))
+
+
+def test_planted_tree_follows_first_children():
+    parent = gen.random_tree(21, 4, 3, 2)
+    first = {}
+    for c in range(1, len(parent)):
+        first.setdefault(int(parent[c]), c)
+    chain = [0]
+    while chain[-1] in first:
+        chain.append(first[chain[-1]])
+    inp = gen.lmhead_inputs(4, len(parent), 512, 3000, 12, plant=1.0, parent=parent)
+    out, nodes, k, near = ol.lmhead_tree_greedy(inp["hidden"], inp["weight"], inp["tokens"], parent)
+    assert not near.any()
+    assert np.all(k == len(chain) - 1)
+    for b in range(4):
+        assert list(nodes[b, :k[b]]) == chain[1:]
+        assert list(out[b, :k[b]]) == [int(inp["tokens"][b, c]) for c in chain[1:]]
+
+
+def test_near_flag_on_ties():
+    h = np.array([[[1.0, 2.0]]])
+    w = np.array([[1.0, 1.0], [3.0, 0.0], [0.0, 0.0]])   # logits 3, 3, 0: an exact tie
+    lg = ol.lmhead_logits(h, w)
+    assert ol.near_rows(h, w, lg)[0, 0]
+    w2 = np.array([[1.0, 1.0], [30.0, 0.0], [0.0, 0.0]])  # 3 vs 30
+    assert not ol.near_rows(h, w2, ol.lmhead_logits(h, w2))[0, 0]
+    # the greedy rule on a tie picks the smallest id (osm.argmax_rows)
+    assert osm.argmax_rows(lg)[0, 0] == 0

@@ -235,3 +235,35 @@ def tree_stochastic_inputs(B: int, parent: np.ndarray, V: int, seed: int, target
         tok[:, c] = gumbel_max_draw(d[:, int(parent[c])], r)
     u = rng_for(seed, "uniforms").random((B, N), dtype=np.float32)
     return dict(target_logits=t, draft_logits=d, node_tokens=tok, uniforms=u)
+
+
+def lmhead_inputs(B: int, R: int, d: int, V: int, seed: int, dtype: str = "bf16", plant: float = 0.6,
+                  parent=None) -> dict:
+    """Hidden states [B, R, d] ~ N(0, 1) and an LM-head weight [V, d] ~ N(0, 1/d) (stored as
+    ``dtype``), with draft tokens [B, R] whose acceptance is non-trivial: with probability
+    ``plant`` the token of row i + 1 (chain) or of each node's first child (tree, ``parent``
+    given) gets a weight row proportional to the predecessor row's hidden state, which makes it
+    that row's argmax."""
+    r = rng_for(seed, "q")
+    h = store(r.standard_normal((B, R, d), dtype=np.float32), dtype)
+    w = rng_for(seed, "k").standard_normal((V, d), dtype=np.float32) / np.float32(np.sqrt(d))
+    tok = rng_for(seed, "tokens").integers(0, V, size=(B, R)).astype(np.int32)
+    pr = rng_for(seed, "tree_tok")
+    used = set()
+    if parent is not None:   # the first child of each node (planting siblings too would tie them)
+        first = {}
+        for c in range(1, R):
+            first.setdefault(int(parent[c]), c)
+        pairs = sorted((p_, c) for p_, c in first.items())
+    else:
+        pairs = [(i, i + 1) for i in range(R - 1)]
+    for b in range(B):
+        for src, dst in pairs:
+            if pr.random() < plant:
+                t = int(pr.integers(V))
+                if t in used:
+                    continue
+                used.add(t)
+                w[t] = h[b, src] * np.float32(3.0 / np.sqrt(d))
+                tok[b, dst] = t
+    return dict(hidden=h, weight=store(w, dtype), tokens=tok)
