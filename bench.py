@@ -560,6 +560,100 @@ def time_tree_stochastic(runner, K, device):
             "draft_corr": 0.8}
 
 
+LM_HIDDEN = 4096   # hidden size of the LLaMA-3-8B / Vicuna-7B targets whose LM heads the workloads use
+
+
+def time_lmhead(runner, K, device, plant=0.6):
+    """spec_lmhead_sample -- the LM-head GEMM reduced to per-row argmaxes and the greedy rule in
+    one call -- on the workload's verify rows (B x nq hidden states of width 4096) against its
+    vocabulary, chain or tree as the workload is; beside it, for context, the unfused pipeline of
+    the same result (cuBLAS bf16 logits, an fp32 copy, spec_sample greedy).  Inputs follow the
+    LM-head recipe of the input generator (hidden N(0, 1), weight N(0, 1/d), a fraction `plant`
+    of the drafts made their row's argmax) but are drawn on the device from a seeded torch
+    generator, the 1 GB weight being too slow to draw on the host.  CUDA graph replays; the weight
+    is larger than L2 and L2 is also flushed before each replay."""
+    import torch
+    sv, cfg = runner.sv, runner.cfg
+    tree = bool(cfg.tree_nodes)
+    parent = runner.inp["tree"] if tree else None
+    B, R, d, V = cfg.B, cfg.nq, LM_HIDDEN, cfg.vocab
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg.seed + 404)
+    h = torch.randn((B, R, d), generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn((V, d), generator=g, device=device) / (d ** 0.5)).to(torch.bfloat16)
+    rng = np.random.default_rng(cfg.seed + 405)
+    tok = rng.integers(0, V, size=(B, R)).astype(np.int32)
+    if tree:
+        first = {}
+        for c in range(1, R):
+            first.setdefault(int(parent[c]), c)
+        pairs = sorted(first.items())
+    else:
+        pairs = [(i, i + 1) for i in range(R - 1)]
+    used = set()
+    for b in range(B):
+        for src, dst in pairs:
+            t = int(rng.integers(V))
+            if rng.random() < plant and t not in used:
+                used.add(t)
+                w[t] = (h[b, src].float() * (3.0 / d ** 0.5)).to(torch.bfloat16)
+                tok[b, dst] = t
+    tok_d = torch.from_numpy(tok if tree else np.ascontiguousarray(tok[:, 1:])).to(device)
+    mode = sv.SPEC_SAMPLE_TREE_GREEDY if tree else sv.SPEC_SAMPLE_CHAIN_GREEDY
+    cols = int(runner.inp["out"].shape[1]) if tree else R
+    out = torch.empty((B, cols), dtype=torch.int32, device=device)
+    nodes = torch.empty_like(out) if tree else None
+    nacc = torch.empty((B,), dtype=torch.int32, device=device)
+    ws = torch.empty(sv.spec_lmhead_sample_workspace(mode, h, w), dtype=torch.uint8, device=device)
+    out_u, nacc_u = torch.empty_like(out), torch.empty_like(nacc)
+    nodes_u = torch.empty_like(out) if tree else None
+    ws_u = torch.empty(sv.spec_sample_workspace(mode, torch.empty((B, R, V), device="meta"), parent),
+                       dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    def fused():
+        sv.spec_lmhead_sample(mode, h, w, out, nacc, draft_tokens=tok_d, tree_parent=parent, out_path_nodes=nodes,
+                              workspace=ws, stream=stream)
+
+    def unfused():
+        logits = torch.matmul(h.view(B * R, d), w.t()).float().view(B, R, V)
+        sv.spec_sample(mode, logits, out_u, nacc_u, draft_tokens=tok_d, tree_parent=parent, out_path_nodes=nodes_u,
+                       workspace=ws_u, stream=stream)
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def timed(op):
+        with torch.cuda.stream(stream):
+            op()
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream, capture_error_mode="thread_local"):
+                op()
+            for _ in range(3):
+                gr.replay()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
+            stream.synchronize()
+        return 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+    us = timed(fused)
+    us_u = timed(unfused)
+    agree = bool(torch.equal(nacc, nacc_u) and torch.equal(out, out_u))
+    rows = B * R
+    nbytes = V * d * 2 + rows * d * 2 + 2 * rows * ((V + 127) // 128) * 8 + B * (R + cols + 1) * 4
+    peak, _ = peaks()
+    return {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak,
+            "algorithmic_bytes": int(nbytes), "rows": rows, "hidden": d, "vocab": V,
+            "mode": "tree_greedy" if tree else "chain_greedy",
+            "mean_accepted": float(nacc.float().mean().item()),
+            "unfused_us": us_u, "unfused": "cuBLAS bf16 GEMM -> fp32 logits -> spec_sample greedy",
+            "unfused_same_tokens": agree}
+
+
 def time_e2e(runner, K, W, device):
     """The same round through the public API with host buffers: per step, pinned host -> device
     copies of the round's inputs, the six calls, and a device -> host read of the emitted tokens."""
@@ -731,6 +825,7 @@ def main():
     commit = time_commit(runner, 200, device)
     verify_append = time_verify_append(runner, max(5, min(args.steps, 50)), device)
     tree_sto = time_tree_stochastic(runner, max(5, min(args.steps, 100)), device) if cfg.tree_nodes else None
+    lmhead = time_lmhead(runner, max(5, min(args.steps, 50)), device)
     e2e = None
     if not args.no_e2e:
         sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
@@ -761,6 +856,7 @@ def main():
         "commit": commit,
         "verify_with_append": verify_append,
         "tree_stochastic_sample": tree_sto,
+        "lmhead_greedy_sample": lmhead,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
                      "peak_source": peak_kind},

@@ -272,6 +272,48 @@ size_t spec_sample_workspace(const spec_sample_args* args);
 int spec_sample(const spec_sample_args* args, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * spec_lmhead_sample -- the LM-head projection fused with greedy verification
+ *
+ * The verified rows' logits are the target's final hidden states times the LM-head (unembedding)
+ * matrix ("Speculative Decoding in LLM Serving Systems", The algorithm: one target pass gives a
+ * next-token distribution per drafted position; "Guide to MagicDec", Implementation Step 3).  In
+ * the greedy modes only each row's argmax is used, so this call never writes the logits: a GEMM
+ * reduces its fp32 accumulators straight to one running (max, argmax) key per row, and the rule of
+ *   SPEC_SAMPLE_CHAIN_GREEDY (n = gamma: rows 0..gamma, draft_tokens [B, gamma]) or
+ *   SPEC_SAMPLE_TREE_GREEDY  (n = N nodes: rows 0..N-1, node tokens [B, N], tree_parent HOST [N])
+ * is applied to the argmaxes exactly as spec_sample does (ties to the smallest token id).
+ * The stochastic modes are not offered: their residual draw needs a whole normalised target row
+ * that is only known after every row's statistics, i.e. a second pass over the weights.
+ *
+ * Layout: hidden bf16 [B, R, d] contiguous (R = gamma + 1 or N), weight bf16 [V, d] contiguous,
+ *   both 16-byte aligned; draft_tokens int32 with batch stride tok_stride_b; out_tokens /
+ *   out_path_nodes [B, out_cols], out_num_accepted [B] as for spec_sample.
+ * Limits: d a multiple of 64 (up to 65 536); 1 <= V <= 2^24; B * R <= 256; tree: N <= 64,
+ *   out_cols >= max depth + 1; chain: 0 <= gamma <= 32, out_cols >= gamma + 1.
+ * Floating point: bf16 products accumulated in fp32 on the tensor cores; the argmax compares those
+ *   fp32 values (an exact tie goes to the smaller id; two logits within the fp32 rounding of a
+ *   d-term sum of each other may come out in either order).
+ * Workspace: 256 bytes (status word) + B * R * 8 bytes (one running (max, argmax) key per row).
+ * ---------------------------------------------------------------------------------------- */
+typedef struct spec_lmhead_args {
+  int32_t mode, B, n, d, V;
+  int32_t out_cols;
+  const void* hidden;          /* bf16 [B, R, d], device */
+  const void* weight;          /* bf16 [V, d], device */
+  const int32_t* draft_tokens; /* device */
+  int64_t tok_stride_b;
+  const int32_t* tree_parent;  /* HOST [N] (tree mode) */
+  int32_t* out_tokens;
+  int32_t* out_num_accepted;
+  int32_t* out_path_nodes;     /* tree mode, optional */
+  void* workspace;
+  size_t workspace_bytes;
+} spec_lmhead_args;
+
+size_t spec_lmhead_sample_workspace(const spec_lmhead_args* args);
+int spec_lmhead_sample(const spec_lmhead_args* args, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * spec_commit
  *
  * The rollback step after verification ("Speculative Decoding in LLM Serving Systems", Accepting
@@ -322,7 +364,7 @@ const char* spec_status_string(int status);
 int spec_abi_version(void);
 /* sizeof() of the argument structs as compiled into the library, so that a binding can check
  * its own layout: which = 0 spec_attn_args, 1 spec_window_args, 2 spec_sample_args,
- * 3 spec_commit_args; else 0. */
+ * 3 spec_commit_args, 4 spec_lmhead_args; else 0. */
 size_t spec_abi_struct_size(int which);
 
 #ifdef __cplusplus

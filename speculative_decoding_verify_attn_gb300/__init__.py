@@ -12,3 +12,4 @@ from .binding import (  # noqa: F401
 )
 from .binding import SPEC_ERR_SCRATCH_LIMIT, spec_verify_attn_noalloc  # noqa: F401,E402
 from .binding import SPEC_COMMIT_CHAIN, SPEC_COMMIT_TREE, SpecCommitArgs, spec_commit  # noqa: F401,E402
+from .binding import SpecLmheadArgs, spec_lmhead_sample, spec_lmhead_sample_workspace  # noqa: F401,E402

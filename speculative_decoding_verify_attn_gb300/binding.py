@@ -95,6 +95,18 @@ class SpecSampleArgs(Structure):
     ]
 
 
+class SpecLmheadArgs(Structure):
+    _fields_ = [
+        ("mode", c_int32), ("B", c_int32), ("n", c_int32), ("d", c_int32), ("V", c_int32),
+        ("out_cols", c_int32),
+        ("hidden", c_void_p), ("weight", c_void_p),
+        ("draft_tokens", c_void_p), ("tok_stride_b", c_int64),
+        ("tree_parent", c_void_p),
+        ("out_tokens", c_void_p), ("out_num_accepted", c_void_p), ("out_path_nodes", c_void_p),
+        ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+    ]
+
+
 class SpecError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -125,6 +137,10 @@ def lib() -> ctypes.CDLL:
     L.spec_sample_workspace.restype = c_size_t
     L.spec_sample.argtypes = [POINTER(SpecSampleArgs), c_void_p]
     L.spec_sample.restype = c_int
+    L.spec_lmhead_sample_workspace.argtypes = [POINTER(SpecLmheadArgs)]
+    L.spec_lmhead_sample_workspace.restype = c_size_t
+    L.spec_lmhead_sample.argtypes = [POINTER(SpecLmheadArgs), c_void_p]
+    L.spec_lmhead_sample.restype = c_int
     L.spec_commit_workspace.argtypes = [POINTER(SpecCommitArgs)]
     L.spec_commit_workspace.restype = c_size_t
     L.spec_commit.argtypes = [POINTER(SpecCommitArgs), c_void_p]
@@ -135,7 +151,7 @@ def lib() -> ctypes.CDLL:
     L.spec_abi_version.restype = c_int
     L.spec_abi_struct_size.argtypes = [c_int]
     L.spec_abi_struct_size.restype = c_size_t
-    for i, cls in enumerate((SpecAttnArgs, SpecWindowArgs, SpecSampleArgs, SpecCommitArgs)):
+    for i, cls in enumerate((SpecAttnArgs, SpecWindowArgs, SpecSampleArgs, SpecCommitArgs, SpecLmheadArgs)):
         if L.spec_abi_struct_size(i) != ctypes.sizeof(cls):
             raise RuntimeError(f"ABI mismatch for {cls.__name__}: library {L.spec_abi_struct_size(i)} "
                                f"bytes, binding {ctypes.sizeof(cls)}")
@@ -358,6 +374,57 @@ def spec_sample(mode, target_logits, out_tokens, out_num_accepted, *, draft_logi
     del keep
     if st != SPEC_OK:
         raise SpecError(st, "spec_sample")
+    return out_tokens, out_num_accepted
+
+
+def lmhead_args(mode, hidden, weight, out_tokens, out_num_accepted, *, draft_tokens=None, tree_parent=None,
+                out_path_nodes=None, workspace=None):
+    B, rows, d = hidden.shape
+    V = weight.shape[0]
+    n = rows if mode == SPEC_SAMPLE_TREE_GREEDY else rows - 1
+    if not hidden.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("hidden [B, R, d] and weight [V, d] must be contiguous")
+    if weight.shape[1] != d:
+        raise ValueError("weight must be [V, d] with the hidden size d")
+    parent_arr, parent_ptr = _host_i32(tree_parent)
+    a = SpecLmheadArgs(
+        mode=mode, B=B, n=n, d=d, V=V, out_cols=out_tokens.shape[1],
+        hidden=_ptr(hidden), weight=_ptr(weight),
+        draft_tokens=_ptr(draft_tokens), tok_stride_b=0 if draft_tokens is None else draft_tokens.stride(0),
+        tree_parent=parent_ptr,
+        out_tokens=_ptr(out_tokens), out_num_accepted=_ptr(out_num_accepted), out_path_nodes=_ptr(out_path_nodes),
+        workspace=_ptr(workspace), workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+    )
+    return a, parent_arr
+
+
+def spec_lmhead_sample_workspace(mode, hidden, weight) -> int:
+    B, rows, d = hidden.shape
+    n = rows if mode == SPEC_SAMPLE_TREE_GREEDY else rows - 1
+    a = SpecLmheadArgs(mode=mode, B=B, n=n, d=d, V=weight.shape[0])
+    return lib().spec_lmhead_sample_workspace(byref(a))
+
+
+def spec_lmhead_sample(mode, hidden, weight, out_tokens, out_num_accepted, *, draft_tokens=None, tree_parent=None,
+                       out_path_nodes=None, workspace=None, stream=None):
+    """The LM-head projection fused with greedy verification: each row's logits hidden @ weight^T
+    reduced to its argmax on the GPU, then the greedy chain (SPEC_SAMPLE_CHAIN_GREEDY) or tree
+    (SPEC_SAMPLE_TREE_GREEDY) rule.
+
+    hidden [B, gamma+1 | N, d] bf16; weight [V, d] bf16; draft_tokens [B, gamma] or node tokens
+    [B, N] int32; tree_parent host [N] (tree); out_tokens [B, out_cols] int32;
+    out_num_accepted [B] int32."""
+    _check_cuda(hidden, weight, draft_tokens, out_tokens, out_num_accepted, out_path_nodes)
+    need = spec_lmhead_sample_workspace(mode, hidden, weight)
+    if need == 0:
+        raise SpecError(SPEC_ERR_INVALID_ARG, "spec_lmhead_sample_workspace")
+    ws = _workspace(need, hidden.device, workspace)
+    a, keep = lmhead_args(mode, hidden, weight, out_tokens, out_num_accepted, draft_tokens=draft_tokens,
+                          tree_parent=tree_parent, out_path_nodes=out_path_nodes, workspace=ws)
+    st = lib().spec_lmhead_sample(byref(a), _stream_handle(stream))
+    del keep
+    if st != SPEC_OK:
+        raise SpecError(st, "spec_lmhead_sample")
     return out_tokens, out_num_accepted
 
 

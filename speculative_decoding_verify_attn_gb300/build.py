@@ -21,10 +21,10 @@ LIBDIR = os.path.join(PKG, "_lib")
 LIBNAME = "libspecverify.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
-SOURCES = ["attn.cu", "attn_tc.cu", "attn_tc_pair.cu", "sample.cu", "sample_tree.cu", "commit.cu", "api.cpp",
-           "noalloc.cu"]
+SOURCES = ["attn.cu", "attn_tc.cu", "attn_tc_pair.cu", "sample.cu", "sample_tree.cu", "lmhead.cu", "commit.cu",
+           "api.cpp", "noalloc.cu"]
 HEADERS = ["common.cuh", "attn_common.cuh", "tcgen05.cuh", "ff.cuh", "attn_internal.h", "sample_internal.h",
-           "commit_internal.h"]
+           "commit_internal.h", "lmhead_internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -11,6 +11,7 @@
 
 #include "attn_internal.h"
 #include "commit_internal.h"
+#include "lmhead_internal.h"
 #include "sample_internal.h"
 #include "spec_verify.h"
 
@@ -76,6 +77,20 @@ bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int 
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 [rows, cols] row-major (cols contiguous), boxes of 64 columns x box_rows, 128B swizzle
+bool encode_2d_map(CUtensorMap* m, const void* base, int cols, int rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -135,7 +150,7 @@ float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / s
 
 extern "C" {
 
-int spec_abi_version(void) { return 3; }
+int spec_abi_version(void) { return 4; }
 
 size_t spec_abi_struct_size(int which) {
   switch (which) {
@@ -143,6 +158,7 @@ size_t spec_abi_struct_size(int which) {
     case 1: return sizeof(spec_window_args);
     case 2: return sizeof(spec_sample_args);
     case 3: return sizeof(spec_commit_args);
+    case 4: return sizeof(spec_lmhead_args);
     default: return 0;
   }
 }
@@ -365,6 +381,71 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+
+// ------------------------------------------------------------------ spec_lmhead_sample
+static int lmhead_rows(const spec_lmhead_args* a, int* R) {
+  if (a->mode == SPEC_SAMPLE_CHAIN_GREEDY) {
+    if (a->n < 0 || a->n > specv::kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+    *R = a->n + 1;
+    return SPEC_OK;
+  }
+  if (a->mode == SPEC_SAMPLE_TREE_GREEDY) {
+    if (a->n < 1 || a->n > specv::kLmMaxNodes) return SPEC_ERR_UNSUPPORTED;
+    *R = a->n;
+    return SPEC_OK;
+  }
+  if (a->mode == SPEC_SAMPLE_CHAIN || a->mode == SPEC_SAMPLE_TREE) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_ERR_INVALID_ARG;
+}
+
+size_t spec_lmhead_sample_workspace(const spec_lmhead_args* a) {
+  if (!a) return 0;
+  int R;
+  if (lmhead_rows(a, &R) != SPEC_OK) return 0;
+  if (a->B < 1 || a->V < 1 || a->V > (1 << 24) || (int64_t)a->B * R > specv::kLmMaxRows) return 0;
+  return specv::lmhead_workspace_bytes(a->B * R);
+}
+
+int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
+  if (!a) return SPEC_ERR_INVALID_ARG;
+  int R;
+  int st = lmhead_rows(a, &R);
+  if (st != SPEC_OK) return st;
+  if (a->B < 1 || a->V < 1 || a->d < 64 || (a->d % 64) != 0 || a->d > 65536) return SPEC_ERR_INVALID_ARG;
+  if (a->V > (1 << 24) || (int64_t)a->B * R > specv::kLmMaxRows) return SPEC_ERR_UNSUPPORTED;
+  if (!a->hidden || !a->weight || !aligned(a->hidden, 16) || !aligned(a->weight, 16)) return SPEC_ERR_INVALID_ARG;
+  if (!a->out_tokens || !a->out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  const bool tree = a->mode == SPEC_SAMPLE_TREE_GREEDY;
+  if ((tree || a->n > 0) && (!a->draft_tokens || a->tok_stride_b < 0)) return SPEC_ERR_INVALID_ARG;
+  specv::LmheadParams p;
+  memset(&p, 0, sizeof(p));
+  if (tree) {
+    const int maxd = build_tree(a->tree_parent, a->n, nullptr, p.parent, p.depth);
+    if (maxd < 0) return SPEC_ERR_INVALID_ARG;
+    if (a->out_cols < maxd + 1) return SPEC_ERR_INVALID_ARG;
+  } else if (a->out_cols < a->n + 1) {
+    return SPEC_ERR_INVALID_ARG;
+  }
+  const size_t need = spec_lmhead_sample_workspace(a);
+  if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
+  const int sms = num_sms();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  p.mode = a->mode; p.B = a->B; p.R = R; p.d = a->d; p.V = a->V;
+  p.nrows = a->B * R;
+  p.npad = (p.nrows + 15) / 16 * 16;
+  p.n_vtiles = (a->V + 127) / 128;
+  p.tiles_per_pass = 512 / p.npad;
+  size_t smem;
+  specv::lmhead_layout(p.npad, &p.w_stages, &p.h_stages, &p.kgroup, &smem);
+  p.tok = a->draft_tokens; p.tok_sb = a->tok_stride_b;
+  p.out_cols = a->out_cols; p.out_tok = a->out_tokens; p.out_nacc = a->out_num_accepted; p.out_nodes = a->out_path_nodes;
+  specv::lmhead_workspace_carve(a->workspace, &p);
+  CUtensorMap tmW, tmH;
+  if (!encode_2d_map(&tmW, a->weight, a->d, a->V, 128) || !encode_2d_map(&tmH, a->hidden, a->d, p.nrows, p.npad))
+    return SPEC_ERR_CUDA;
+  cudaError_t e = specv::launch_lmhead(p, &tmW, &tmH, sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 // ------------------------------------------------------------------ spec_commit
 size_t spec_commit_workspace(const spec_commit_args* a) {

@@ -1,0 +1,445 @@
+// The LM-head projection fused with greedy verification (spec_lmhead_sample): the verified rows'
+// logits are the target's final hidden states times the LM-head matrix ("Speculative Decoding in
+// LLM Serving Systems", The algorithm; "Guide to MagicDec", Implementation Step 3), and the greedy
+// rules only need each row's argmax, so the logits never leave the SM: a tcgen05 GEMM reduces its
+// accumulators straight to one 64-bit (value, id) key per hidden row, and a small kernel reads the
+// keys and applies the chain or tree rule.
+//
+// GEMM (D[v, n] = sum_k W[v, k] H[n, k]): the vocabulary is M (128 rows of W per tile, K-major,
+// 128-byte swizzle), the B*R hidden rows are N (padded to a multiple of 16, at most 256).  A CTA
+// owns a run of vocabulary tiles and keeps as many accumulators as fit in TMEM (512 / N columns)
+// at once, so each 64-element chunk of the hidden rows is staged once per pass for all of them.
+// The weight is read exactly once; the run is HBM-bound, so shared memory goes to as deep a
+// weight ring as fits beside the hidden-row ring:
+//   warp 0     weight producer: each tile's 128 x 64 chunk into a ring of 16 KB stages.
+//   warp 1     MMA issuer (one lane) and TMEM owner: 4 MMAs (K = 16) per weight chunk, a tile
+//              taking several K chunks in a row (one accumulator chain; see lmhead_layout).
+//   warps 2-5  epilogue: per 32-column block of the pass's accumulators (32 hidden rows x this
+//              warp's 32 vocabulary rows of every tile), each lane's maximum over the tiles, then
+//              two warp reductions per column (the maximum, then the smallest id reaching it;
+//              entries past V excluded) give one key per hidden row, kept in registers across
+//              passes; at the end the four warps' keys meet in shared memory and go to global
+//              memory with one 64-bit atomic max per row and CTA.
+//   warp 6     hidden-row producer: each pass's 64-column chunks into their own ring.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "lmhead_internal.h"
+#include "spec_verify.h"
+#include "tcgen05.cuh"
+
+namespace specv {
+
+constexpr int kLmThreads = 224;
+constexpr int kLmWChunk = 128 * 128;          // bytes: 128 vocabulary rows x 64 bf16
+constexpr int kLmSmemCap = 227 * 1024;        // dynamic shared memory of one CTA
+constexpr int kLmWStagesMax = 16;
+constexpr int kLmHStagesMax = 8;
+
+// A tile takes `kgroup` K chunks in a row, so its accumulator sees chains of 4 kgroup MMAs.  On
+// GB300 a chain of 4 small-N MMAs costs about 660 cycles, of 16 about 1300: chains of 4 leave the
+// single issuer slower than the weight stream, so the group is 4 chunks where the hidden ring can
+// hold two groups of them (npad <= 96) and 2 otherwise.  The hidden ring holds two groups (the one
+// in use and the next; at least 4 chunks), one chunk less if that leaves fewer than 6 weight
+// stages; the rest of shared memory is weight.
+static void lmhead_layout_g(int npad, int g, int* w_stages, int* h_stages, int* kgroup, size_t* smem) {
+  const size_t hb = (size_t)npad * 128;
+  const size_t budget = kLmSmemCap - 1024 - 2560;  // alignment pad; static barriers and keys
+  int hs = 2 * g > 4 ? 2 * g : 4;
+  int ws = (int)((budget - hs * hb) / kLmWChunk);
+  if (ws < 6) {
+    hs = hs - 1 > g + 1 ? hs - 1 : g + 1;
+    ws = (int)((budget - hs * hb) / kLmWChunk);
+  }
+  ws = ws > kLmWStagesMax ? kLmWStagesMax : ws;
+  *w_stages = ws;
+  *h_stages = hs;
+  *kgroup = g;
+  *smem = 1024 + (size_t)ws * kLmWChunk + (size_t)hs * hb;
+}
+void lmhead_layout(int npad, int* w_stages, int* h_stages, int* kgroup, size_t* smem) {
+  lmhead_layout_g(npad, npad <= 96 ? 4 : 2, w_stages, h_stages, kgroup, smem);
+}
+
+// Keys: (ord(value) << 32) | ~id, so that the unsigned order is: larger value first, then smaller id.
+__device__ __forceinline__ int lm_key_id(unsigned long long k) { return (int)(~(uint32_t)k); }
+
+// The steps of a CTA's run of vocabulary tiles: passes of up to `tpp` tiles; per pass, per group
+// of kgroup K chunks, per tile of the pass, the group's weight chunks of that tile.
+struct LmWalk {
+  int tile0, ntiles, tpp, nk;
+};
+__device__ __forceinline__ LmWalk lm_walk(const LmheadParams& p) {
+  LmWalk w;
+  const int per = (p.n_vtiles + gridDim.x - 1) / gridDim.x;
+  w.tile0 = min((int)blockIdx.x * per, p.n_vtiles);
+  w.ntiles = min(per, p.n_vtiles - w.tile0);
+  w.tpp = p.tiles_per_pass;
+  w.nk = p.d / 64;
+  return w;
+}
+
+__device__ __forceinline__ void lm_tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+// Whole warp: 16 consecutive 32-bit TMEM columns of this warp's 32 lanes, waited for in the same
+// statement (the registers are valid once it returns).
+__device__ __forceinline__ void lm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// Monotone map of fp32 to u32 (a < b  <=>  ord(a) < ord(b) for non-NaN values); 0 lies below
+// every mapped value and stands for "no entry".
+__device__ __forceinline__ uint32_t lm_ord(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t lm_redux_max(uint32_t x) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ uint32_t lm_redux_min(uint32_t x) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ void lm_epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// NC consecutive accumulator columns (hidden rows) starting at TMEM address `col0` of tile 0, over
+// the pass's nt tiles (tile t at column offset t * npad; this lane's vocabulary id vm0 + 128 t):
+// first each lane's own maximum over the tiles (earlier tile first, so equal values keep the
+// smaller id; ids >= V excluded), then per column the warp's maximum and the smallest id reaching
+// it.  Lane e keeps column e's pair in (bo, bi).
+template <int NC>
+__device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt, uint32_t vm0, uint32_t V, int lane,
+                                                uint32_t& bo, uint32_t& bi) {
+  uint32_t o[NC], ix[NC];
+#pragma unroll
+  for (int e = 0; e < NC; ++e) {
+    o[e] = 0u;
+    ix[e] = 0xffffffffu;
+  }
+  for (int t = 0; t < nt; ++t) {
+    uint32_t u[32];
+    if constexpr (NC == 32) {
+      tc::ld32(col0 + (uint32_t)(t * npad), u);
+      tc::ld_wait(u);
+    } else {
+      lm_ld16(col0 + (uint32_t)(t * npad), *reinterpret_cast<uint32_t(*)[16]>(u));
+    }
+    const uint32_t vm = vm0 + 128u * (uint32_t)t;
+    const bool valid = vm < V;
+#pragma unroll
+    for (int e = 0; e < NC; ++e) {
+      const uint32_t x = valid ? lm_ord(__uint_as_float(u[e])) : 0u;
+      if (x > o[e]) {
+        o[e] = x;
+        ix[e] = vm;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < NC; ++e) {
+    const uint32_t mo = lm_redux_max(o[e]);
+    const uint32_t mi = lm_redux_min(o[e] == mo ? ix[e] : 0xffffffffu);
+    if (lane == e) {
+      bo = mo;
+      bi = mi;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_argmax(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                  const __grid_constant__ LmheadParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t wfull[kLmWStagesMax], wempty[kLmWStagesMax], hfull[kLmHStagesMax], hempty[kLmHStagesMax];
+  __shared__ uint64_t acc_full, acc_empty, drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_abort;
+  __shared__ unsigned long long s_key[kLmMaxRows];   // this CTA's running key per hidden row
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* wring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // [stage][128 rows][128 B]
+  const int WS = p.w_stages, HS = p.h_stages;
+  const int hbytes = p.npad * 128;                                  // one hidden chunk, 1 KB multiple
+  uint8_t* hring = wring + WS * kLmWChunk;                          // [stage][npad rows][128 B]
+  const uint32_t wring_u32 = smem_u32(wring), hring_u32 = smem_u32(hring);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const LmWalk W = lm_walk(p);
+  const int npass = (W.ntiles + W.tpp - 1) / W.tpp;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < WS; ++i) {
+      mbar_init(&wfull[i], 1);
+      mbar_init(&wempty[i], 1);
+    }
+    for (int i = 0; i < HS; ++i) {
+      mbar_init(&hfull[i], 1);
+      mbar_init(&hempty[i], 1);
+    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, 4);
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  for (int r = threadIdx.x; r < kLmMaxRows; r += blockDim.x) s_key[r] = 0ull;
+  if (warp == 1) tc::alloc(&tmem_base, 512);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = tmem_base;
+  auto fail = [&]() {
+    s_abort = 1;
+    atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ weight producer
+    if (lane == 0 && W.ntiles > 0) {
+      tma_prefetch_desc(&tmW);
+      int wc = 0;
+      bool ok = true;
+      for (int p0 = 0; ok && p0 < W.ntiles; p0 += W.tpp) {
+        const int nt = min(W.tpp, W.ntiles - p0);
+        for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
+          const int gk = min(p.kgroup, W.nk - kg);
+          for (int i = 0; i < nt * gk; ++i, ++wc) {
+            const int t = i / gk, kc = kg + i % gk;
+            const int ws = wc % WS;
+            if (!mbar_wait_bounded(&wempty[ws], ((wc / WS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
+            mbar_arrive_expect_tx(&wfull[ws], (uint32_t)kLmWChunk);
+            lm_tma_load_2d(wring + ws * kLmWChunk, &tmW, &wfull[ws], kc * 64, (W.tile0 + p0 + t) * 128);
+          }
+        }
+      }
+      if (!ok) {
+        fail();
+        for (int i = 1; i <= min(wc, WS); ++i) mbar_wait_bounded(&wfull[(wc - i) % WS], ((wc - i) / WS) & 1, nullptr);
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------------ hidden-row producer
+    if (lane == 0 && W.ntiles > 0) {
+      tma_prefetch_desc(&tmH);
+      int hc = 0;
+      bool ok = true;
+      for (int ps = 0; ok && ps < npass; ++ps) {
+        for (int kc = 0; kc < W.nk; ++kc, ++hc) {
+          const int hs = hc % HS;
+          if (!mbar_wait_bounded(&hempty[hs], ((hc / HS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(&hfull[hs], (uint32_t)hbytes);
+          lm_tma_load_2d(hring + hs * hbytes, &tmH, &hfull[hs], kc * 64, 0);
+        }
+      }
+      if (!ok) {
+        fail();
+        for (int i = 1; i <= min(hc, HS); ++i) mbar_wait_bounded(&hfull[(hc - i) % HS], ((hc - i) / HS) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    // One thread issues every MMA, so its instruction stream between MMAs sets the MMA rate: ring
+    // slots and phases advance incrementally and descriptors are precomputed (a K step of 16 is
+    // +2 in the descriptor's address field, a weight slot +1024, a hidden slot +hbytes / 16).
+    if (lane == 0 && W.ntiles > 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, p.npad, 0, 0);
+      const uint64_t ad0 = tc::smem_desc(wring_u32, 16, 1024);
+      const uint64_t bd0 = tc::smem_desc(hring_u32, 16, 1024);
+      const uint32_t hstep = (uint32_t)hbytes >> 4;
+      int ws = 0, hs = 0;
+      uint32_t wph = 0, hph = 0;
+      bool ok = true;
+      for (int ps = 0; ok && ps < npass; ++ps) {
+        const int nt = min(W.tpp, W.ntiles - ps * W.tpp);
+        if (ps > 0 && !mbar_wait_bounded(&acc_empty, (ps - 1) & 1, &s_abort)) { ok = false; break; }
+        for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
+          const int gk = min(p.kgroup, W.nk - kg);
+          for (int j = 0, s2 = hs, ph = hph; j < gk; ++j) {
+            if (!mbar_wait_bounded(&hfull[s2], ph, &s_abort)) { ok = false; break; }
+            if (++s2 == HS) { s2 = 0; ph ^= 1; }
+          }
+          if (!ok) break;
+          tc::fence_after();
+          uint32_t tacc = tmem;
+          // tile by tile, each taking the group's gk chunks as one chain on its accumulator; the
+          // chain's weight slots are released together after it
+          for (int t = 0; t < nt; ++t, tacc += (uint32_t)p.npad) {
+            for (int j = 0, s2 = ws, ph = wph; j < gk; ++j) {
+              if (!mbar_wait_bounded(&wfull[s2], ph, &s_abort)) { ok = false; break; }
+              if (++s2 == WS) { s2 = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+            tc::fence_after();
+            for (int j = 0, sw = ws, sh = hs; j < gk; ++j) {
+              const uint64_t ad = ad0 + (uint64_t)(sw * (kLmWChunk >> 4));
+              const uint64_t bd = bd0 + (uint64_t)(sh * hstep);
+              tc::mma_ss(tacc, ad, bd, idesc, (kg + j) ? 1u : 0u);
+              tc::mma_ss(tacc, ad + 2, bd + 2, idesc, 1u);
+              tc::mma_ss(tacc, ad + 4, bd + 4, idesc, 1u);
+              tc::mma_ss(tacc, ad + 6, bd + 6, idesc, 1u);
+              if (++sw == WS) sw = 0;
+              if (++sh == HS) sh = 0;
+            }
+            for (int j = 0; j < gk; ++j) {
+              tc::commit(&wempty[ws]);
+              if (++ws == WS) { ws = 0; wph ^= 1; }
+            }
+          }
+          if (!ok) break;
+          for (int j = 0; j < gk; ++j) {
+            tc::commit(&hempty[hs]);
+            if (++hs == HS) { hs = 0; hph ^= 1; }
+          }
+        }
+        if (ok) tc::commit(&acc_full);
+      }
+      if (!ok) {
+        fail();
+        tc::commit(&drain);
+        mbar_wait_bounded(&drain, 0, nullptr);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2-5)
+    const int sub = warp & 3;           // TMEM lanes 32 sub .. 32 sub + 31 = vocabulary rows
+    unsigned long long kbest[kLmMaxRows / 32];   // lane's running key of hidden row 32 cc + lane
+#pragma unroll
+    for (int cc = 0; cc < kLmMaxRows / 32; ++cc) kbest[cc] = 0ull;
+    for (int ps = 0; ps < npass; ++ps) {
+      const int nt = min(W.tpp, W.ntiles - ps * W.tpp);
+      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full, ps & 1, &s_abort));
+      if (!got) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc::fence_after();
+      const uint32_t vm0 = (uint32_t)((W.tile0 + ps * W.tpp) * 128 + sub * 32 + lane);  // tile 0's vocabulary id
+      const uint32_t tb = tmem + ((uint32_t)(sub * 32) << 16);
+#pragma unroll
+      for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
+        if (cc * 32 >= p.npad) break;
+        uint32_t bo = 0, bi = 0xffffffffu;
+        if (cc * 32 + 32 <= p.npad)
+          lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
+        else
+          lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
+        const unsigned long long key = bi < (uint32_t)p.V ? (((unsigned long long)bo << 32) | (uint32_t)~bi) : 0ull;
+        kbest[cc] = key > kbest[cc] ? key : kbest[cc];
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty);
+    }
+    // the four warps' keys into the CTA's, then one global atomic per row
+#pragma unroll
+    for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
+      const int row = cc * 32 + lane;
+      if (row < p.nrows && kbest[cc] != 0ull) atomicMax(&s_key[row], kbest[cc]);
+    }
+    lm_epi_sync();
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(p.rec);
+    for (int r = threadIdx.x - 64; r < p.nrows; r += 128)
+      if (s_key[r] != 0ull) atomicMax(&keys[r], s_key[r]);
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after();
+    tc::dealloc(tmem, 512);
+  }
+}
+
+// One CTA per sequence: each row's argmax from its key, then the greedy rule of the mode.
+__global__ void __launch_bounds__(256) lmhead_finalize(const __grid_constant__ LmheadParams p) {
+  pdl_wait();  // the GEMM's keys
+  __shared__ int s_a[kLmMaxNodes];
+  const int b = blockIdx.x;
+  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(p.rec);
+  for (int r = threadIdx.x; r < p.R; r += blockDim.x) s_a[r] = lm_key_id(keys[(int64_t)b * p.R + r]);
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const int32_t* tok = p.tok + (int64_t)b * p.tok_sb;
+  int32_t* out = p.out_tok + (int64_t)b * p.out_cols;
+  int32_t* nodes = p.out_nodes ? p.out_nodes + (int64_t)b * p.out_cols : nullptr;
+  const bool tree = p.mode == SPEC_SAMPLE_TREE_GREEDY;
+  const int nt = tree ? p.R : p.R - 1;  // tokens to check: node tokens 1..N-1, or drafts 0..gamma-1
+  bool bad = false;
+  for (int i = tree ? 1 : 0; i < nt; ++i) bad |= tok[i] < 0 || tok[i] >= p.V;
+  for (int c = 0; c < p.out_cols; ++c) {
+    out[c] = -1;
+    if (nodes) nodes[c] = -1;
+  }
+  if (bad) {
+    p.out_nacc[b] = -1;
+    atomicOr(p.status, (uint32_t)SPEC_STATUS_BAD_TOKEN);
+    return;
+  }
+  if (!tree) {  // accept x_i while it equals the argmax of row i; then the argmax of row k
+    int k = 0;
+    while (k < p.R - 1 && tok[k] == s_a[k]) ++k;
+    for (int i = 0; i < k; ++i) out[i] = tok[i];
+    out[k] = s_a[k];
+    p.out_nacc[b] = k;
+    return;
+  }
+  // tree: node i accepted iff its parent is and its token is the parent row's argmax; the deepest
+  // accepted node (ties to the smallest index), its path, then the argmax of its row
+  unsigned long long acc = 1ull;
+  int best = 0;
+  for (int i = 1; i < p.R; ++i) {
+    const int par = p.parent[i];
+    if (((acc >> par) & 1ull) && tok[i] == s_a[par]) {
+      acc |= 1ull << i;
+      if (p.depth[i] > p.depth[best]) best = i;
+    }
+  }
+  const int dd = p.depth[best];
+  for (int j = best, k = dd - 1; j > 0; j = p.parent[j], --k) {
+    out[k] = tok[j];
+    if (nodes) nodes[k] = j;
+  }
+  out[dd] = s_a[best];
+  p.out_nacc[b] = dd;
+}
+
+size_t lmhead_workspace_bytes(int nrows) { return 256 + (size_t)nrows * sizeof(unsigned long long); }
+
+void lmhead_workspace_carve(void* ws, LmheadParams* p) {
+  uint8_t* b = reinterpret_cast<uint8_t*>(ws);
+  p->status = reinterpret_cast<uint32_t*>(b);
+  p->rec = b + 256;
+}
+
+cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
+                          cudaStream_t stream) {
+  // the status word and the keys (0 lies below every real key) in one memset
+  cudaError_t e = cudaMemsetAsync(p.status, 0, lmhead_workspace_bytes(p.nrows), stream);
+  if (e != cudaSuccess) return e;
+  int ws, hs, kg;
+  size_t smem;
+  lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
+  if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(lmhead_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
+  lmhead_argmax<<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_dependent(lmhead_finalize, dim3(p.B), dim3(256), 0, stream, 0u, p);
+}
+
+}  // namespace specv

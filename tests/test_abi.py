@@ -44,8 +44,9 @@ def test_struct_layouts_match(L):
     assert L.spec_abi_struct_size(1) == ctypes.sizeof(b.SpecWindowArgs)
     assert L.spec_abi_struct_size(2) == ctypes.sizeof(b.SpecSampleArgs)
     assert L.spec_abi_struct_size(3) == ctypes.sizeof(b.SpecCommitArgs)
-    assert L.spec_abi_struct_size(4) == 0
-    assert L.spec_abi_version() == 3
+    assert L.spec_abi_struct_size(4) == ctypes.sizeof(b.SpecLmheadArgs)
+    assert L.spec_abi_struct_size(5) == 0
+    assert L.spec_abi_version() == 4
     assert L.spec_status_string(-3).decode().startswith("workspace")
 
 
@@ -189,3 +190,41 @@ def test_commit_host_validation(L):
     assert call(commit_args(workspace_bytes=255)) == -3
     # chain mode needs no K/V at all; only its own fields are validated
     assert call(commit_args(mode=0, nq=0)) == -1
+
+
+def lmhead_args(**kw):
+    from speculative_decoding_verify_attn_gb300.binding import SpecLmheadArgs
+    a = SpecLmheadArgs(mode=1, B=8, n=4, d=4096, V=128256, out_cols=5, hidden=FAKE, weight=FAKE + (1 << 30),
+                       draft_tokens=FAKE, tok_stride_b=4, tree_parent=None, out_tokens=FAKE,
+                       out_num_accepted=FAKE, out_path_nodes=None, workspace=FAKE, workspace_bytes=1 << 30)
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a
+
+
+def test_lmhead_host_validation(L):
+    call = lambda a: L.spec_lmhead_sample(ctypes.byref(a), None)  # noqa: E731
+    ws = L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args()))
+    assert ws == 256 + 8 * 5 * 8                          # status + one 64-bit key per hidden row
+    assert call(lmhead_args(mode=7)) == -1
+    assert call(lmhead_args(mode=0)) == -2                 # stochastic chain: not fused
+    assert call(lmhead_args(mode=3, n=6)) == -2            # stochastic tree: not fused
+    assert L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(mode=0))) == 0
+    assert call(lmhead_args(n=33)) == -2
+    assert call(lmhead_args(B=52, n=4)) == -2              # 260 hidden rows > 256
+    assert call(lmhead_args(d=4000)) == -1                 # d a multiple of 64
+    assert call(lmhead_args(d=0)) == -1
+    assert call(lmhead_args(V=0)) == -1
+    assert call(lmhead_args(V=(1 << 24) + 1)) == -2
+    assert call(lmhead_args(hidden=FAKE + 8)) == -1
+    assert call(lmhead_args(weight=None)) == -1
+    assert call(lmhead_args(draft_tokens=None)) == -1
+    assert call(lmhead_args(out_num_accepted=None)) == -1
+    assert call(lmhead_args(out_cols=4)) == -1
+    assert call(lmhead_args(workspace_bytes=ws - 1)) == -3
+    parent = np.array([-1, 0, 0, 1, 1, 2], dtype=np.int32)
+    tree = dict(mode=2, n=6, tree_parent=parent.ctypes.data, tok_stride_b=6)
+    assert call(lmhead_args(**tree, out_cols=2)) == -1     # depth 2 needs 3 output columns
+    bad = np.array([-1, 0, 3, 1, 1, 2], dtype=np.int32)
+    assert call(lmhead_args(**dict(tree, tree_parent=bad.ctypes.data), out_cols=3)) == -1
+    assert call(lmhead_args(mode=2, n=65, tok_stride_b=65, out_cols=64)) == -2

@@ -1,0 +1,185 @@
+"""GPU parity: spec_lmhead_sample -- the LM-head projection fused with greedy chain / tree
+verification -- against the oracle.
+
+The GPU accumulates bf16 products in fp32; the oracle takes the exact float64 dot products.  Token
+decisions are compared exactly on every sequence none of whose consulted rows the oracle marks as
+near-tied (top two logits within the fp32 accumulation bound of a d-term dot product of each
+other); the near-tied ones are only checked for validity."""
+
+import numpy as np
+import pytest
+
+from oracle import lmhead as ol
+from oracle import sample as osm
+from workloads import gen
+from workloads.configs import CONFIGS
+
+from .helpers import to_dev, to_np, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verify_attn_gb300 as sv
+    sv.lib()
+    return sv
+
+
+def _gpu(sv, mode, hidden, weight, tokens, cols, parent=None):
+    torch = torch_mod()
+    B = hidden.shape[0]
+    out = torch.full((B, cols), -7, dtype=torch.int32, device="cuda")
+    nodes = torch.full((B, cols), -7, dtype=torch.int32, device="cuda")
+    nacc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    need = sv.spec_lmhead_sample_workspace(mode, hidden, weight)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    sv.spec_lmhead_sample(mode, hidden, weight, out, nacc, draft_tokens=tokens, tree_parent=parent,
+                          out_path_nodes=nodes if parent is not None else None, workspace=ws)
+    torch.cuda.synchronize()
+    return to_np(out), to_np(nodes), to_np(nacc), sv.read_status(ws)
+
+
+def _chain(sv, inp, gamma, min_ok, drafts=None):
+    drafts = inp["tokens"][:, 1:gamma + 1] if drafts is None else drafts
+    h, w = to_dev(inp["hidden"], "bf16"), to_dev(inp["weight"], "bf16")
+    tok = to_dev(drafts, "i32") if gamma > 0 else None
+    out, _, nacc, st = _gpu(sv, sv.SPEC_SAMPLE_CHAIN_GREEDY, h, w, tok, gamma + 1)
+    r_out, r_k, near = ol.lmhead_greedy_chain(inp["hidden"], inp["weight"], drafts)
+    ok = ~near
+    assert st == 0
+    assert ok.sum() >= min_ok
+    assert np.array_equal(nacc[ok], r_k[ok])
+    assert np.array_equal(out[ok], r_out[ok])
+    _valid_chain(inp, drafts, out, nacc, ~ok)
+    return r_k
+
+
+def _valid_chain(inp, drafts, out, nacc, which):
+    """Near-tied sequences: every accepted draft and the emitted token are within the fp32 bound
+    of their row's maximum."""
+    if not which.any():
+        return
+    lg = ol.lmhead_logits(inp["hidden"][which], inp["weight"])
+    for i, b in enumerate(np.nonzero(which)[0]):
+        k = int(nacc[b])
+        assert 0 <= k <= drafts.shape[1]
+        assert list(out[b, :k]) == list(drafts[b, :k])
+        for r in range(k + 1):
+            t = int(out[b, r])
+            assert lg[i, r].max() - lg[i, r, t] <= 1e-3 * np.abs(lg[i, r]).max() + 1e-6
+
+
+def _tree(sv, inp, parent, min_ok):
+    cols = int(osm.tree_depths(parent).max()) + 1
+    h, w = to_dev(inp["hidden"], "bf16"), to_dev(inp["weight"], "bf16")
+    out, nodes, nacc, st = _gpu(sv, sv.SPEC_SAMPLE_TREE_GREEDY, h, w, to_dev(inp["tokens"], "i32"), cols, parent)
+    r_out, r_nodes, r_k, near = ol.lmhead_tree_greedy(inp["hidden"], inp["weight"], inp["tokens"], parent, cols)
+    ok = ~near
+    assert st == 0
+    assert ok.sum() >= min_ok
+    assert np.array_equal(nacc[ok], r_k[ok])
+    assert np.array_equal(out[ok], r_out[ok]) and np.array_equal(nodes[ok], r_nodes[ok])
+    return r_k
+
+
+def test_chain_small_ragged_vocab(sv):
+    """8 vocabulary tiles, the last one 104 entries long; d = 128 (two K chunks)."""
+    inp = gen.lmhead_inputs(3, 5, 128, 1000, 301)
+    k = _chain(sv, inp, 4, 3)
+    assert k.max() >= 1
+
+
+def test_chain_llama3_8b_lm_head(sv):
+    """LLaMA-3-8B's LM head (d 4096, V 128 256), batch 8, gamma 4: the full-size launch."""
+    cfg = CONFIGS["llama3-8b-layer"]
+    inp = gen.lmhead_inputs(cfg.B, cfg.gamma + 1, 4096, cfg.vocab, cfg.seed)
+    k = _chain(sv, inp, cfg.gamma, cfg.B - 1)
+    assert k.max() >= 2
+
+
+def test_chain_gamma_zero(sv):
+    """No drafts: the emitted token is row 0's argmax; V = 130 leaves a 2-entry last tile."""
+    inp = gen.lmhead_inputs(2, 1, 64, 130, 302)
+    k = _chain(sv, inp, 0, 2)
+    assert np.all(k == 0)
+
+
+def test_chain_256_rows(sv):
+    """B * (gamma + 1) = 255 hidden rows: the widest accumulator (N = 256), two tiles per pass."""
+    inp = gen.lmhead_inputs(51, 5, 64, 300, 303)
+    _chain(sv, inp, 4, 48)
+
+
+def test_chain_planted_at_tile_edges(sv):
+    """Drafts planted at vocabulary ids 127, 128 and V - 1 (the last and first entries of tiles
+    and the last entry of the ragged tile), in every position of the chain."""
+    gamma, d, V = 3, 256, 1001
+    base = gen.lmhead_inputs(1, gamma + 1, d, V, 304, plant=0.0)
+    for order in ([127, 128, V - 1], [V - 1, 127, 128], [128, V - 1, 127]):
+        w = base["weight"].copy()
+        tok = base["tokens"].copy()
+        for i, t in enumerate(order):
+            w[t] = gen.store(base["hidden"][0, i] * np.float32(3.0 / np.sqrt(d)), "bf16")
+            tok[0, i + 1] = t
+        k = _chain(sv, dict(hidden=base["hidden"], weight=w, tokens=tok), gamma, 1)
+        assert k[0] == gamma
+
+
+def test_exact_tie_goes_to_smaller_id(sv):
+    """Two identical weight rows in different tiles (and CTAs): the smaller id wins."""
+    torch = torch_mod()
+    d, V = 128, 2048
+    inp = gen.lmhead_inputs(1, 1, d, V, 305, plant=0.0)
+    w = inp["weight"].copy()
+    row = gen.store(inp["hidden"][0, 0] * np.float32(3.0 / np.sqrt(d)), "bf16")
+    w[1700] = row
+    w[300] = row
+    h, wd = to_dev(inp["hidden"], "bf16"), to_dev(w, "bf16")
+    out, _, nacc, st = _gpu(sv, sv.SPEC_SAMPLE_CHAIN_GREEDY, h, wd, None, 1)
+    assert st == 0 and nacc[0] == 0 and out[0, 0] == 300
+    del torch
+
+
+def test_tree_medusa_lm_head(sv):
+    """Vicuna-7B-sized LM head (d 4096, V 32 000) over the Medusa tree (64 nodes), batch 4:
+    256 hidden rows."""
+    cfg = CONFIGS["medusa-tree-8k"]
+    parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+    inp = gen.lmhead_inputs(cfg.B, len(parent), 4096, cfg.vocab, cfg.seed, parent=parent)
+    k = _tree(sv, inp, parent, cfg.B - 1)
+    assert k.max() >= 2
+
+
+@pytest.mark.parametrize("N,depth,ch,B,d,V", [(9, 3, 3, 5, 192, 777), (2, 1, 1, 1, 64, 129), (1, 0, 0, 3, 64, 50)])
+def test_tree_small(sv, N, depth, ch, B, d, V):
+    parent = gen.random_tree(N, depth, ch, 306 + N) if N > 1 else np.array([-1], dtype=np.int32)
+    inp = gen.lmhead_inputs(B, N, d, V, 307 + N, parent=parent)
+    _tree(sv, inp, parent, B - 1)
+
+
+def test_bad_token_flagged(sv):
+    torch = torch_mod()
+    inp = gen.lmhead_inputs(3, 4, 64, 500, 308)
+    drafts = inp["tokens"][:, 1:].copy()
+    drafts[1, 2] = 500
+    h, w = to_dev(inp["hidden"], "bf16"), to_dev(inp["weight"], "bf16")
+    out, _, nacc, st = _gpu(sv, sv.SPEC_SAMPLE_CHAIN_GREEDY, h, w, to_dev(drafts, "i32"), 4)
+    assert st == sv.SPEC_STATUS_BAD_TOKEN
+    assert nacc[1] == -1 and np.all(out[1] == -1)
+    r_out, r_k, near = ol.lmhead_greedy_chain(inp["hidden"][[0, 2]], inp["weight"], drafts[[0, 2]])
+    for i, b in enumerate((0, 2)):
+        if not near[i]:
+            assert nacc[b] == r_k[i] and list(out[b]) == list(r_out[i])
+    del torch
+
+
+def test_stochastic_modes_refused(sv):
+    torch = torch_mod()
+    h = torch.zeros((1, 3, 64), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((100, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((1, 3), dtype=torch.int32, device="cuda")
+    nacc = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    with pytest.raises(sv.SpecError):
+        sv.spec_lmhead_sample(sv.SPEC_SAMPLE_CHAIN, h, w, out, nacc,
+                              draft_tokens=torch.zeros((1, 2), dtype=torch.int32, device="cuda"))
