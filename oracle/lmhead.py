@@ -26,9 +26,16 @@ from . import sample as osm
 NEAR_REL = 2.5e-4
 
 
-def lmhead_logits(hidden: np.ndarray, weight: np.ndarray) -> np.ndarray:
-    """hidden [B, R, d], weight [V, d] (values as stored) -> logits [B, R, V] in float64."""
-    return np.asarray(hidden, np.float64) @ np.asarray(weight, np.float64).T
+def lmhead_logits(hidden: np.ndarray, weight: np.ndarray, chunk: int = 8192) -> np.ndarray:
+    """hidden [B, R, d], weight [V, d] (values as stored) -> logits [B, R, V] in float64.  The
+    product is taken over blocks of ``chunk`` weight rows only to bound the float64 copy of the
+    weight; every logit is the same d-term dot product either way."""
+    h = np.asarray(hidden, np.float64)
+    V = weight.shape[0]
+    out = np.empty(h.shape[:-1] + (V,), np.float64)
+    for v0 in range(0, V, chunk):
+        out[..., v0:v0 + chunk] = h @ np.asarray(weight[v0:v0 + chunk], np.float64).T
+    return out
 
 
 def near_rows(hidden: np.ndarray, weight: np.ndarray, logits: np.ndarray, rel: float = NEAR_REL) -> np.ndarray:
@@ -37,12 +44,13 @@ def near_rows(hidden: np.ndarray, weight: np.ndarray, logits: np.ndarray, rel: f
     B, R, V = logits.shape
     top2 = np.argsort(-logits, axis=-1, kind="stable")[..., :2]
     h = np.abs(np.asarray(hidden, np.float64))
-    w = np.abs(np.asarray(weight, np.float64))
     near = np.zeros((B, R), dtype=bool)
     for b in range(B):
         for r in range(R):
             a, c = int(top2[b, r, 0]), int(top2[b, r, 1])
-            bound = rel * (float(h[b, r] @ w[a]) + float(h[b, r] @ w[c]))
+            wa = np.abs(np.asarray(weight[a], np.float64))
+            wc = np.abs(np.asarray(weight[c], np.float64))
+            bound = rel * (float(h[b, r] @ wa) + float(h[b, r] @ wc))
             near[b, r] = logits[b, r, a] - logits[b, r, c] <= bound
     return near
 

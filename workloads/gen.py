@@ -28,10 +28,13 @@ def rng_for(seed: int, what: str) -> np.random.Generator:
 def round_bf16(x: np.ndarray) -> np.ndarray:
     """Round float32 values to the nearest bf16 (ties to even); NaN stays NaN. Returns float32."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    lsb = (bits >> 16) & 1
-    rounded = ((bits + 0x7FFF + lsb) >> 16) << 16
-    out = rounded.astype(np.uint32).view(np.float32).copy()
+    out = np.empty_like(x)
+    src, dst = x.reshape(-1).view(np.uint32), out.reshape(-1).view(np.uint32)
+    step = 1 << 22   # blocks bound the temporaries for weight-sized arrays
+    for i in range(0, src.size, step):
+        b = src[i:i + step]
+        # 32-bit add wraps only for NaN bit patterns, which are restored below
+        dst[i:i + step] = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
     out[np.isnan(x)] = np.nan
     return out
 
