@@ -615,8 +615,18 @@ def time_lmhead(runner, K, device, plant=0.6):
         sv.spec_lmhead_sample(mode, h, w, out, nacc, draft_tokens=tok_d, tree_parent=parent, out_path_nodes=nodes,
                               workspace=ws, stream=stream)
 
+    h2 = h.view(B * R, d)
+    try:   # cuBLAS with fp32 output (the fused kernel's accumulator precision), where PyTorch has it
+        torch.mm(h2[:1], w[:16].t(), out_dtype=torch.float32)
+        fp32_out = True
+    except (TypeError, RuntimeError, NotImplementedError):
+        fp32_out = False
+
     def unfused():
-        logits = torch.matmul(h.view(B * R, d), w.t()).float().view(B, R, V)
+        if fp32_out:
+            logits = torch.mm(h2, w.t(), out_dtype=torch.float32).view(B, R, V)
+        else:
+            logits = torch.matmul(h2, w.t()).float().view(B, R, V)
         sv.spec_sample(mode, logits, out_u, nacc_u, draft_tokens=tok_d, tree_parent=parent, out_path_nodes=nodes_u,
                        workspace=ws_u, stream=stream)
 
@@ -650,7 +660,9 @@ def time_lmhead(runner, K, device, plant=0.6):
             "algorithmic_bytes": int(nbytes), "rows": rows, "hidden": d, "vocab": V,
             "mode": "tree_greedy" if tree else "chain_greedy",
             "mean_accepted": float(nacc.float().mean().item()),
-            "unfused_us": us_u, "unfused": "cuBLAS bf16 GEMM -> fp32 logits -> spec_sample greedy",
+            "unfused_us": us_u,
+            "unfused": ("cuBLAS bf16 GEMM with fp32 output -> spec_sample greedy" if fp32_out
+                        else "cuBLAS bf16 GEMM (bf16 output) -> fp32 copy -> spec_sample greedy"),
             "unfused_same_tokens": agree}
 
 
