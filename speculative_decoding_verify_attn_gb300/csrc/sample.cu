@@ -165,15 +165,13 @@ __device__ int chain_decide_warp(const SampleParams& p, int b, const float* sM, 
 // recorded, in fp32 arithmetic only: the exponent (t_x - M_t) - (d_x - M_d) is formed exactly as a
 // float-float, and the ratio exp(e) * Z_d / Z_t carries a relative error of a few 1e-7, far inside
 // the 1e-6 band around each threshold.  u = 0 accepts (P(x) > 0 for every token).
-__device__ int chain_decide_warp_ff(const SampleParams& p, int b, const float* sM, const FF* sZ) {
+// Lane i < gamma passes draft i's token x, the recorded target and draft logits of x (tx, dx) and
+// its uniform uu, loaded by the caller ahead of the row statistics.
+__device__ int chain_decide_warp_ff(const SampleParams& p, const float* sM, const FF* sZ, int x, float tx, float dx,
+                                    float uu) {
   const int i = threadIdx.x & 31;
   bool bad = false, acc = true;
   if (i < p.gamma) {
-    const int rows = p.rows_t + p.rows_d;
-    const int x = p.tok[(int64_t)b * p.tok_sb + i];
-    const float tx = __ldcg(p.sel + (int64_t)b * rows + i);
-    const float dx = __ldcg(p.sel + (int64_t)b * rows + p.rows_t + i);
-    const float uu = p.u[(int64_t)b * p.u_sb + i];
     bad = x < 0 || x >= p.V;
     if (!bad) {
       const FF dt = ff_add(FF{tx, 0.f}, FF{-sM[i], 0.f});
@@ -190,7 +188,8 @@ __device__ int chain_decide_warp_ff(const SampleParams& p, int b, const float* s
   return rej ? __ffs(rej) - 1 : p.gamma;
 }
 
-__device__ void write_chain_out(const SampleParams& p, int b, int k, int y) {
+// Outputs of sequence b; the accepted drafts are read from `tok` (its row of draft tokens).
+__device__ void write_chain_out(const SampleParams& p, int b, int k, int y, const int32_t* tok) {
   int32_t* out = p.out_tok + (int64_t)b * p.out_cols;
   if (k < 0) {
     for (int c = 0; c < p.out_cols; ++c) out[c] = -1;
@@ -200,11 +199,14 @@ __device__ void write_chain_out(const SampleParams& p, int b, int k, int y) {
   }
   for (int c = 0; c < p.out_cols; ++c) {
     int v = -1;
-    if (c < k) v = p.tok[(int64_t)b * p.tok_sb + c];
+    if (c < k) v = tok[c];
     else if (c == k) v = y;
     out[c] = v;
   }
   p.out_nacc[b] = k;
+}
+__device__ void write_chain_out(const SampleParams& p, int b, int k, int y) {
+  write_chain_out(p, b, k, y, p.tok + (int64_t)b * p.tok_sb);
 }
 
 // Greedy tree: a[] holds the argmax of every node's row.  Writes the outputs of sequence b.
@@ -447,6 +449,15 @@ __global__ void __launch_bounds__(kSampleThreads) sample_finalize(const __grid_c
 constexpr int kFinThreads = 512;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kSlab = 512;  // residual slab: lane l takes elements 4l..4l+3 of each 128-element quarter
+constexpr int kFinKeepMax = 160 * 1024;  // residual values a CTA keeps in shared memory for the draw
+
+// Dynamic shared memory of the finish kernel for `per` slabs per CTA: the slab masses, then (when
+// they fit) every residual value of the CTA's share, so the CTA that holds the threshold scans
+// them without re-reading the rows.
+__host__ __device__ constexpr bool fin_keeps_resid(int per) { return (size_t)per * kSlab * 4 <= (size_t)kFinKeepMax; }
+__host__ __device__ constexpr size_t fin_smem_bytes(int per) {
+  return ((size_t)per * sizeof(FF) + 15) / 16 * 16 + (fin_keeps_resid(per) ? (size_t)per * kSlab * 4 : 0);
+}
 
 // This lane's 16 logits of target and draft row in the slab starting at `base` (0 past V).
 struct SlabData {
@@ -480,6 +491,12 @@ __device__ __forceinline__ void slab_compute(const SlabData& D, int base, int V,
     r[4 * j + 2] = in ? resid_fast(tv[j].z, dv[j].z, Mt, iZt, Md, iZd, has_d) : 0.f;
     r[4 * j + 3] = in ? resid_fast(tv[j].w, dv[j].w, Mt, iZt, Md, iZd, has_d) : 0.f;
   }
+}
+// Keep this lane's 16 residual values of the CTA's local slab `sl` (4 float4, one per quarter).
+__device__ __forceinline__ void keep_slab(float4* s_r, int sl, const float (&r)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) s_r[(sl * 4 + j) * 32 + lane] = make_float4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
 }
 __device__ __forceinline__ void slab_resid(const float* tr, const float* dr, int base, int V, float Mt, float iZt,
                                            float Md, float iZd, bool has_d, float (&r)[16]) {
@@ -529,12 +546,12 @@ __device__ __forceinline__ void slab_scan(const FF* s_slab, int ns, FF& lsum, FF
 // Every CTA takes the same cluster barriers (the decisions that steer them are identical across
 // the cluster).
 __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __grid_constant__ SampleParams p) {
-  pdl_wait();  // the statistics kernel's per-item records
   namespace cg = cooperative_groups;
-  extern __shared__ FF s_slab[];      // residual mass of each of this CTA's slabs
+  extern __shared__ __align__(16) uint8_t s_fin[];
   __shared__ float sM[2 * kMaxGamma + 1];
   __shared__ FF sZ[2 * kMaxGamma + 1];
   __shared__ int s_k;
+  __shared__ int32_t s_x[kMaxGamma];  // the draft tokens (for the output row)
   __shared__ FF s_total;              // this CTA's residual mass (read by the whole cluster)
   __shared__ FF s_R, s_cum;           // the cluster's total and this CTA's prefix
   cg::cluster_group cl = cg::this_cluster();
@@ -542,6 +559,27 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   const int b = blockIdx.x / CS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = p.rows_t + p.rows_d;
+  const int nslabs = (p.V + kSlab - 1) / kSlab;
+  const int per = (nslabs + CS - 1) / CS;
+  FF* s_slab = reinterpret_cast<FF*>(s_fin);   // residual mass of each of this CTA's slabs
+  float4* s_r = reinterpret_cast<float4*>(s_fin + ((size_t)per * sizeof(FF) + 15) / 16 * 16);
+  const bool keep = fin_keeps_resid(per);      // s_r[(slab * 4 + quarter) * 32 + lane]: a lane's 4 values
+
+  // the decision's inputs, loaded ahead of the row statistics so that their latency overlaps:
+  // lane i < gamma of warp 0 takes draft i (token, uniform, then the two logits the statistics
+  // kernel recorded), lane 0 the final draw's uniform
+  int x_i = 0;
+  float u_i = 0.f, tx_i = 0.f, dx_i = 0.f, u_draw = 0.f;
+  if (warp == 0 && lane < p.gamma) {
+    x_i = p.tok[(int64_t)b * p.tok_sb + lane];
+    u_i = p.u[(int64_t)b * p.u_sb + lane];
+  }
+  if (warp == 0 && lane == 0) u_draw = p.u[(int64_t)b * p.u_sb + p.gamma];
+  pdl_wait();  // the statistics kernel's per-item records
+  if (warp == 0 && lane < p.gamma) {
+    tx_i = __ldcg(p.sel + (int64_t)b * rows + lane);
+    dx_i = __ldcg(p.sel + (int64_t)b * rows + p.rows_t + lane);
+  }
 
   // ---- row statistics and accept decisions.  A warp merges a row's items 256 at a time, each
   // lane's (M_c, S_c) loaded together before any is used (one L2 round trip per 256 items).
@@ -576,16 +614,15 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
     }
     if (lane == 0) { sM[rr] = m; sZ[rr] = z; }
   }
+  if (warp == 0 && lane < p.gamma) s_x[lane] = x_i;
   __syncthreads();
   if (warp == 0) {
-    const int kk = chain_decide_warp_ff(p, b, sM, sZ);
+    const int kk = chain_decide_warp_ff(p, sM, sZ, x_i, tx_i, dx_i, u_i);
     if (lane == 0) s_k = kk;
   }
   __syncthreads();
   const int k = s_k;
 
-  const int nslabs = (p.V + kSlab - 1) / kSlab;
-  const int per = (nslabs + CS - 1) / CS;
   const int s0 = min(nslabs, rank * per), s1 = min(nslabs, s0 + per);
   bool has_d = k >= 0 && k < p.gamma;
   const float* tr = trow(p, b, k >= 0 ? k : 0);
@@ -606,10 +643,12 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         if (s2 < s1) slab_load(tr, dr, s2 * kSlab, p.V, has_d, D1);
         float r[16];
         slab_compute(D0, s * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+        if (keep) keep_slab(s_r, s - s0, r);
         const FF m0 = slab_mass(r);
         if (lane == 0) s_slab[s - s0] = m0;
         if (s2 < s1) {
           slab_compute(D1, s2 * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+          if (keep) keep_slab(s_r, s2 - s0, r);
           const FF m1 = slab_mass(r);
           if (lane == 0) s_slab[s2 - s0] = m1;
         }
@@ -650,7 +689,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   }
 
   if (k >= 0 && R.hi > 0.f) {
-    const float uu = p.u[(int64_t)b * p.u_sb + p.gamma];
+    const float uu = __shfl_sync(0xffffffffu, u_draw, 0);   // meaningful in warp 0, the only user
     const FF thr = ff_mul_f(R, uu);
     const FF nxt = ff_add(cum, s_total);
     if (warp == 0 && !ff_gt(cum, thr) && ff_gt(nxt, thr)) {
@@ -693,23 +732,43 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         const int src = __ffs(found) - 1;
         const int sl = __shfl_sync(0xffffffffu, my_sl, src);
         FF base = at_end ? thr : shfl_ff(my_acc, src);
-        // re-read the slab and scan it in token order: quarter j holds lane l's elements 4l..4l+3
+        // the slab's residual values (kept from the mass pass, else recomputed from the rows), scanned
+        // in token order: quarter j holds lane l's elements 4l..4l+3
         float r[16];
         const int sbase = (s0 + sl) * kSlab;
-        slab_resid(tr, dr, sbase, p.V, Mt, iZt, Md, iZd, has_d, r);
+        if (keep) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 v = s_r[(sl * 4 + j) * 32 + lane];
+            r[4 * j] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
+          }
+        } else {
+          slab_resid(tr, dr, sbase, p.V, Mt, iZt, Md, iZd, has_d, r);
+        }
         int slab_last = -1;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           if (r[e] > 0.f) slab_last = max(slab_last, sbase + (e >> 2) * 128 + lane * 4 + (e & 3));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) slab_last = max(slab_last, __shfl_xor_sync(0xffffffffu, slab_last, o));
+        // the four quarters' lane sums and warp scans first (independent, so they overlap), then
+        // the quarters in order
+        FF qv[4], qiv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qv[j] = ff_add(ff_add(FF{r[4 * j], 0.f}, FF{r[4 * j + 1], 0.f}),
+                         ff_add(FF{r[4 * j + 2], 0.f}, FF{r[4 * j + 3], 0.f}));
+          qiv[j] = warp_scan_ff(qv[j]);
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (y >= 0 || at_end) break;
           const int idx = sbase + j * 128 + lane * 4;
-          const FF q = ff_add(ff_add(FF{r[4 * j], 0.f}, FF{r[4 * j + 1], 0.f}),
-                              ff_add(FF{r[4 * j + 2], 0.f}, FF{r[4 * j + 3], 0.f}));
-          const FF qi = warp_scan_ff(q);
+          const FF q = qv[j];
+          const FF qi = qiv[j];
           const unsigned hit = __ballot_sync(0xffffffffu, ff_gt(ff_add(base, qi), thr));
           if (hit) {
             const int hl = __ffs(hit) - 1;
@@ -730,10 +789,10 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
         }
         if (y < 0) y = slab_last;  // rounding left the threshold at the slab end
       }
-      if (lane == 0) write_chain_out(p, b, k, y);
+      if (lane == 0) write_chain_out(p, b, k, y, s_x);
     }
   }
-  if (k < 0 && rank == 0 && tid == 0) write_chain_out(p, b, -1, -1);
+  if (k < 0 && rank == 0 && tid == 0) write_chain_out(p, b, -1, -1, s_x);
   cl.sync();  // no CTA leaves while the cluster may still read its shared memory
 }
 
@@ -916,13 +975,21 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
     if ((long long)p.B * cs > p.num_sms) continue;
     attr[0].val.clusterDim.x = (unsigned)cs;
     cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
-    cfg.dynamicSmemBytes = (size_t)((nslabs + cs - 1) / cs) * sizeof(FF);
+    cfg.dynamicSmemBytes = fin_smem_bytes((nslabs + cs - 1) / cs);
+    if (cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)cfg.dynamicSmemBytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      continue;
+    }
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, sample_chain_finish, &cfg) == cudaSuccess && active >= p.B) break;
     (void)cudaGetLastError();
   }
-  return launch_dependent(sample_chain_finish, dim3((unsigned)(p.B * cs)), dim3(kFinThreads),
-                          (size_t)((nslabs + cs - 1) / cs) * sizeof(FF), stream, (unsigned)cs, p);
+  const size_t smem = fin_smem_bytes((nslabs + cs - 1) / cs);
+  e = cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(sample_chain_finish, dim3((unsigned)(p.B * cs)), dim3(kFinThreads), smem, stream,
+                          (unsigned)cs, p);
 }
 
 cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream) {
