@@ -100,10 +100,12 @@ __device__ __forceinline__ void lm_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
-// Monotone map of fp32 to u32 (a < b  <=>  ord(a) < ord(b) for non-NaN values); 0 lies below
+// Monotone map of fp32 to u32 (a < b  <=>  ord(a) < ord(b), a == b  <=>  ord(a) == ord(b) for
+// non-NaN values: -0 is taken as +0, so a zero maximum still ties to the smaller id); 0 lies below
 // every mapped value and stands for "no entry".
 __device__ __forceinline__ uint32_t lm_ord(float v) {
-  const uint32_t u = __float_as_uint(v);
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ uint32_t lm_redux_max(uint32_t x) {

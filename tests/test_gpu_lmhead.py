@@ -141,6 +141,19 @@ def test_exact_tie_goes_to_smaller_id(sv):
     del torch
 
 
+def test_zero_logits_tie_to_id_zero(sv):
+    """An all-zero hidden row makes every logit +0 or -0 (products of zero with weights of either
+    sign): all equal, so the argmax is id 0 -- a signed-zero order would pick some +0 instead."""
+    torch = torch_mod()
+    d, V = 64, 700
+    w = gen.lmhead_inputs(1, 1, d, V, 309, plant=0.0)["weight"]
+    h = np.zeros((2, 1, d), dtype=np.float32)
+    out, _, nacc, st = _gpu(sv, sv.SPEC_SAMPLE_CHAIN_GREEDY, to_dev(h, "bf16"), to_dev(w, "bf16"), None, 1)
+    assert st == 0 and list(nacc) == [0, 0] and list(out[:, 0]) == [0, 0]
+    assert int(np.argmax(ol.lmhead_logits(h, w)[0, 0])) == 0
+    del torch
+
+
 def test_tree_medusa_lm_head(sv):
     """Vicuna-7B-sized LM head (d 4096, V 32 000) over the Medusa tree (64 nodes), batch 4:
     256 hidden rows."""
