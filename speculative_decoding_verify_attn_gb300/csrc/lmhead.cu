@@ -436,7 +436,8 @@ cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const C
   size_t smem;
   lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
   if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(lmhead_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
+  e = cudaFuncSetAttribute(lmhead_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
   const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
   lmhead_argmax<<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);

@@ -458,6 +458,12 @@ __host__ __device__ constexpr bool fin_keeps_resid(int per) { return (size_t)per
 __host__ __device__ constexpr size_t fin_smem_bytes(int per) {
   return ((size_t)per * sizeof(FF) + 15) / 16 * 16 + (fin_keeps_resid(per) ? (size_t)per * kSlab * 4 : 0);
 }
+// The largest of them (V <= 2^20: at most 2048 slabs per CTA, residual values kept up to 80): the
+// kernel's shared-memory limit is set to this once, whatever the call, so concurrent calls with
+// different vocabularies never race on it.
+constexpr int kFinKeepSlabs = kFinKeepMax / (kSlab * 4);
+constexpr size_t kFinSmemMax = fin_smem_bytes(kFinKeepSlabs) > 2048 * sizeof(FF) ? fin_smem_bytes(kFinKeepSlabs)
+                                                                                 : 2048 * sizeof(FF);
 
 // This lane's 16 logits of target and draft row in the slab starting at `base` (0 past V).
 struct SlabData {
@@ -970,24 +976,19 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  e = cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinSmemMax);
+  if (e != cudaSuccess) return e;
   int cs = 8;
   for (; cs > 1; cs >>= 1) {
     if ((long long)p.B * cs > p.num_sms) continue;
     attr[0].val.clusterDim.x = (unsigned)cs;
     cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
     cfg.dynamicSmemBytes = fin_smem_bytes((nslabs + cs - 1) / cs);
-    if (cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)cfg.dynamicSmemBytes) != cudaSuccess) {
-      (void)cudaGetLastError();
-      continue;
-    }
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, sample_chain_finish, &cfg) == cudaSuccess && active >= p.B) break;
     (void)cudaGetLastError();
   }
   const size_t smem = fin_smem_bytes((nslabs + cs - 1) / cs);
-  e = cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   return launch_dependent(sample_chain_finish, dim3((unsigned)(p.B * cs)), dim3(kFinThreads), smem, stream,
                           (unsigned)cs, p);
 }
