@@ -277,6 +277,24 @@ def test_generators_round_to_storage(dtype):
     assert gen.round_bf16(np.array([1.0 + 3 * 2 ** -8], dtype=np.float32))[0] == 1.0 + 2 ** -6
 
 
+def test_bf16_rounding_matches_torch_and_handles_specials():
+    """The generator's bf16 rounding against PyTorch's float32 -> bfloat16 conversion (round to
+    nearest even) on random values of every magnitude, exact ties, +-0, +-inf, subnormals and NaN,
+    in an array longer than one internal block."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    bits = rng.integers(0, 2 ** 32, size=(1 << 22) + 1000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32).copy()
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1.0 + 2 ** -8, -(1.0 + 3 * 2 ** -8), 1e-40, -1e-40,
+                        3.4028235e38], dtype=np.float32)
+    x[:len(special)] = special
+    got = gen.round_bf16(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    nan = np.isnan(x)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
 def test_append_places_rows_by_hand():
     """Two sequences, 2 kv heads, nq = 2: sequence 0 (kv_len 5) gets its rows at positions 3 and 4
     of each head; sequence 1 (kv_len 1 < nq) is left untouched."""
