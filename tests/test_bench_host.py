@@ -71,3 +71,30 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_algorithmic_bytes_match_the_closed_forms():
+    """bench.step_bytes (the numerator of every roofline fraction) against the per-call byte counts
+    written out for the workloads: K+V of every visible key once, q in / o out, the logits once
+    plus the one re-read row pair, and the draft ring's visible slots."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    from workloads.configs import CONFIGS
+    md = CONFIGS["magicdec-64k"]
+    inp = {"kv_len_h": np.full(md.B, 65536), "pos0": np.full(md.B, 65536)}
+    nb = bench.step_bytes(md, inp)
+    assert nb["verify_kv"] == 32 * 65536 * 8 * 128 * 2 * 2                  # 8.59 GB
+    assert nb["verify_total"] == nb["verify_kv"] + 32 * 5 * 32 * 128 * (2 + 4)
+    assert nb["sample"] == 32 * 9 * 128256 * 4 + 32 * 2 * 128256 * 4
+    assert nb["window"] == 32 * 512 * 8 * 128 * 2 * 2 + 32 * 32 * 128 * (2 + 4)
+    tr = CONFIGS["medusa-tree-8k"]
+    nb = bench.step_bytes(tr, {"kv_len_h": np.full(tr.B, 8192)})
+    assert nb["verify_kv"] == 4 * 8192 * 8 * 128 * 2 * 2                      # 134 MB
+    assert nb["sample"] == 4 * 64 * 32000 * 4
+    b8 = CONFIGS["llama3-8b-layer"]
+    lens = np.array([16384, 20000, 32768, 17000, 25000, 30000, 16500, 31000])
+    nb = bench.step_bytes(b8, {"kv_len_h": lens})
+    assert nb["verify_kv"] == int(lens.sum()) * 8 * 128 * 4
+    assert nb["window"] == 0
