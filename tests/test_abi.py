@@ -228,3 +228,16 @@ def test_lmhead_host_validation(L):
     bad = np.array([-1, 0, 3, 1, 1, 2], dtype=np.int32)
     assert call(lmhead_args(**dict(tree, tree_parent=bad.ctypes.data), out_cols=3)) == -1
     assert call(lmhead_args(mode=2, n=65, tok_stride_b=65, out_cols=64)) == -2
+
+
+def test_header_is_plain_c():
+    """include/spec_verify.h compiles as C99 (no C++ in the boundary) and as C++17."""
+    import shutil
+    import subprocess
+    hdr = os.path.join(ROOT, "include", "spec_verify.h")
+    for cc, std, lang in (("gcc", "-std=c99", "c"), ("g++", "-std=c++17", "c++")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not installed")
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-fsyntax-only", "-x", lang, hdr],
+                           capture_output=True, text=True)
+        assert r.returncode == 0 and not r.stderr, r.stderr
