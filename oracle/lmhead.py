@@ -22,7 +22,8 @@ import numpy as np
 
 from . import sample as osm
 
-# |fp32 sum - exact| <= d * 2^-24 * sum |terms| (worst case for d = 4096: 2.4e-4 sum |terms|)
+# |fp32 sum - exact| <= d * 2^-24 * sum |terms| (worst case for d = 4096: 2.4e-4 sum |terms|);
+# near_rows uses the larger of this floor and d * 2^-24 for the actual d
 NEAR_REL = 2.5e-4
 
 
@@ -38,10 +39,13 @@ def lmhead_logits(hidden: np.ndarray, weight: np.ndarray, chunk: int = 8192) -> 
     return out
 
 
-def near_rows(hidden: np.ndarray, weight: np.ndarray, logits: np.ndarray, rel: float = NEAR_REL) -> np.ndarray:
+def near_rows(hidden: np.ndarray, weight: np.ndarray, logits: np.ndarray, rel: float | None = None) -> np.ndarray:
     """[B, R] bool: the row's two largest logits differ by at most rel * (sum_k |h_k w_ak| +
-    sum_k |h_k w_bk|), a and b the two top ids."""
+    sum_k |h_k w_bk|), a and b the two top ids; rel defaults to max(NEAR_REL, d * 2^-24), the
+    worst-case relative error of a d-term fp32 sum."""
     B, R, V = logits.shape
+    if rel is None:
+        rel = max(NEAR_REL, hidden.shape[-1] * 2.0 ** -24)
     top2 = np.argsort(-logits, axis=-1, kind="stable")[..., :2]
     h = np.abs(np.asarray(hidden, np.float64))
     near = np.zeros((B, R), dtype=bool)

@@ -60,3 +60,16 @@ def test_near_flag_on_ties():
     assert not ol.near_rows(h, w2, ol.lmhead_logits(h, w2))[0, 0]
     # the greedy rule on a tie picks the smallest id (osm.argmax_rows)
     assert osm.argmax_rows(lg)[0, 0] == 0
+
+
+def test_near_band_grows_with_the_hidden_size():
+    """The near-tie band is the worst-case relative error of a d-term fp32 sum, d * 2^-24, never
+    below the d = 4096 floor: a gap of 1e-3 of the magnitude is near at d = 65 536 (band 3.9e-3)
+    but not at d = 64 (floor 2.5e-4)."""
+    for d, expect in ((64, False), (65536, True)):
+        h = np.zeros((1, 1, d))
+        h[0, 0, 0] = 1.0
+        w = np.zeros((3, d))
+        w[0, 0], w[1, 0] = 1.0, 1.0 - 1e-3        # logits 1 and 0.999, sum |terms| = 1.999
+        lg = ol.lmhead_logits(h, w)
+        assert bool(ol.near_rows(h, w, lg)[0, 0]) is expect
