@@ -111,6 +111,30 @@ def test_chain_256_rows(sv):
     _chain(sv, inp, 4, 48)
 
 
+def test_chain_longest_gamma(sv):
+    """gamma = 32, the longest chain the ABI takes (33 rows per sequence, 231 rows in all)."""
+    inp = gen.lmhead_inputs(7, 33, 128, 1000, 310, plant=0.9)
+    k = _chain(sv, inp, 32, 6)
+    assert k.max() >= 3
+
+
+def test_largest_hidden_size(sv):
+    """d = 65 536, the largest hidden size the ABI takes (1024 K chunks per tile).  The worst-case
+    fp32 band grows with d, so every row gets a planted winner (margin ~3 sqrt(d) against N(0, 1)
+    logits): sequence 0 accepts both drafts, sequence 1 has its second draft replaced and rejects
+    it; every consulted row must then be outside the band."""
+    d, V = 65536, 300
+    inp = gen.lmhead_inputs(2, 3, d, V, 311, plant=1.0)
+    w, tok = inp["weight"].copy(), inp["tokens"].copy()
+    planted = {int(t) for t in tok[:, 1:].ravel()}
+    free = [t for t in range(V) if t not in planted]
+    for b in range(2):   # the last row's winner (no draft follows it)
+        w[free[b]] = gen.store(inp["hidden"][b, 2] * np.float32(3.0 / np.sqrt(d)), "bf16")
+    tok[1, 2] = free[2]
+    k = _chain(sv, dict(hidden=inp["hidden"], weight=w, tokens=tok), 2, 2)
+    assert list(k) == [2, 1]
+
+
 def test_chain_planted_at_tile_edges(sv):
     """Drafts planted at vocabulary ids 127, 128 and V - 1 (the last and first entries of tiles
     and the last entry of the ragged tile), in every position of the chain."""
