@@ -110,7 +110,15 @@ enum {
  *   bf16 K/V: base pointers 16-byte aligned, kv_stride_h and kv_stride_b multiples of 8.
  * scale == 0 selects 1/sqrt(D).
  * Accumulation is fp32 (scores, softmax, P.V); bf16 inputs are multiplied exactly.
+ * debug_flags: 0 in normal use (any bit other than SPEC_DEBUG_NO_LOADS returns
+ *   SPEC_ERR_INVALID_ARG).  SPEC_DEBUG_NO_LOADS is a test hook for the failure path of the bf16
+ *   kernels: they issue no K/V copies, so the first bounded wait of every CTA runs out (after about
+ *   one second), every kernel stops issuing, frees what it holds and returns, and the status word
+ *   reads SPEC_STATUS_TIMEOUT; the output is not valid.  The fp32 kernel has no device waits and
+ *   ignores the flag.
  * ---------------------------------------------------------------------------------------- */
+enum { SPEC_DEBUG_NO_LOADS = 1 };
+
 typedef struct spec_attn_args {
   int32_t B, Hq, Hkv, D, nq;
   int32_t q_dtype, kv_dtype, o_dtype;
@@ -124,7 +132,7 @@ typedef struct spec_attn_args {
   const int32_t* kv_len;      /* device [B] */
   const int32_t* tree_parent; /* HOST [nq], or NULL for chain verify */
   float scale;
-  int32_t reserved1;
+  int32_t debug_flags;        /* 0, or SPEC_DEBUG_* test hooks (see below) */
   void* o;
   int64_t o_stride_b, o_stride_t, o_stride_h;
   void* workspace;
@@ -149,8 +157,10 @@ int spec_verify_attn(const spec_attn_args* args, spec_stream_t stream);
  * GPU which loads this library holds until the process exits.  args->workspace and
  * args->workspace_bytes are ignored.  A problem whose spec_verify_attn_workspace() size exceeds
  * the array returns SPEC_ERR_SCRATCH_LIMIT before anything is launched.
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
- *    that device current); make that first call before any stream capture.
+ *  - Every call looks up the array's device address in the calling thread's current context
+ *    (cudaGetSymbolAddress); the first call in a context also loads the library's kernels into it,
+ *    so make that first call before any stream capture.  Nothing is cached across contexts, so a
+ *    caller may switch contexts (or reset the device) between calls.
  *  - Every call on a device shares the one array and leaves its contents behind; nothing in it
  *    has to start at zero (the per-call status word is cleared by the call itself).  Calls whose
  *    kernels overlap on the GPU (other streams, other host threads) race on the array: serialize
@@ -243,8 +253,22 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  * Limits: V % 4 == 0, logits pointers 16-byte aligned and tl/dl strides multiples of 4;
  *   1 <= B; chain: 1 <= gamma <= 32 (stochastic), 0 <= gamma <= 32 (greedy),
  *   out_cols >= gamma + 1; tree: 1 <= N <= 64, out_cols >= max depth + 1.
- * Floating point: exponentials in fp32, every sum above a thread's own few elements in fp64; the
- * accept ratio uses fp64 exponentials of the two selected logits.
+ * Floating point: V > 2048 (the statistics + finish kernels) uses no fp64 at all.  Each thread
+ *   sums its own elements in fp32 (pairwise or compensated); every sum above that -- across lanes,
+ *   warps, CTAs and the cluster -- is float-float (Knuth's TwoSum, about 44 significant bits), in a
+ *   fixed order, with no floating-point atomics, so every decision is reproducible.  The terms of
+ *   the softmax normalisers and of the residual CDF are fp32 2^x of the max-subtracted, log2(e)-
+ *   scaled logit (relative error about 2^-22).  The accept ratio P(x)/Q(x) is
+ *   exp((t_x - M_t) - (d_x - M_d)) * Z_d / Z_t with the exponent formed exactly as a float-float
+ *   and evaluated by fp32 expf, then fp32 division (relative error a few 1e-7).
+ *   V <= 2048 (one warp per sequence): fp32 exponentials, fp64 sums and fp64 accept ratios.
+ *   Either way a decision can differ from exact arithmetic only when its exact value lies within
+ *   about 1e-6 (relative) of its threshold.
+ * Diagnostics: after a SPEC_SAMPLE_CHAIN call with V > 2048, the 32-bit word at byte 4 of the
+ *   workspace holds the launch shape of the accept/draw kernel: the number of CTAs that share one
+ *   sequence's vocabulary (a thread-block cluster) in the low byte, and bit 8 set when the draw
+ *   re-reads the residual row from memory instead of scanning values kept on chip.  No result
+ *   depends on it; tests read it to know which code path a shape exercised.
  * ---------------------------------------------------------------------------------------- */
 enum { SPEC_SAMPLE_CHAIN = 0, SPEC_SAMPLE_CHAIN_GREEDY = 1, SPEC_SAMPLE_TREE_GREEDY = 2, SPEC_SAMPLE_TREE = 3 };
 

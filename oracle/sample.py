@@ -136,6 +136,70 @@ def _spec_sample_chain_block(t, d, x, u, band):
     return out, nacc, near
 
 
+def chain_outcome_valid(target_logits, draft_logits, draft_tokens, uniforms, out_tokens, num_accepted,
+                        band: float = NEAR_BAND) -> np.ndarray:
+    """Per sequence: is (out_tokens, num_accepted) an outcome of the chain rule above once every
+    decision whose exact value lies within ``band`` of its threshold may go either way?
+
+    These are exactly the decisions ``spec_sample_chain`` flags as near: an evaluated accept test
+    with |u_i - P_i(x_i)/Q_i(x_i)| <= band, and a final draw whose threshold u * R lies within
+    band * R of a CDF step.  So for a sequence with no near decision only the outcome
+    ``spec_sample_chain`` returns is valid, and for one with near decisions every outcome that
+    rounding on either side of those thresholds can produce is.  Steps, for the claimed k:
+
+    1. Accept tests 1..k must pass and test k+1 (if k < gamma) must fail, each unless near.
+    2. The emitted row is x_1..x_k, then y, then -1 padding.
+    3. With the residual row r of step 3 for this k (R = sum r, r = P_{k+1} if R = 0), y must hold
+       mass (r_y > 0) and its CDF step [C(y-1), C(y)) must meet [u R - band R, u R + band R].
+    A row with a draft token outside [0, V) is valid only as (-1 ..., num_accepted -1).
+    """
+    t = np.asarray(target_logits)
+    d = np.asarray(draft_logits)
+    B, g1, V = t.shape
+    gamma = g1 - 1
+    x = np.asarray(draft_tokens, dtype=np.int64).reshape(B, gamma)
+    u = np.asarray(uniforms, dtype=np.float32).astype(np.float64)
+    out = np.asarray(out_tokens)
+    nacc = np.asarray(num_accepted)
+    valid = np.zeros(B, dtype=bool)
+    for b in range(B):
+        k = int(nacc[b])
+        if np.any((x[b] < 0) | (x[b] >= V)):
+            valid[b] = k == -1 and bool(np.all(out[b] == -1))
+            continue
+        if not 0 <= k <= gamma:
+            continue
+        P = softmax64(t[b])
+        Q = softmax64(d[b]) if gamma > 0 else None
+        ok = True
+        for i in range(min(k + 1, gamma)):          # tests 1..k+1 (0-based 0..k)
+            px, qx = P[i, x[b, i]], Q[i, x[b, i]]
+            accepted = u[b, i] * qx < px
+            near = qx > 0 and px > 0 and abs(u[b, i] - px / qx) <= band
+            if accepted != (i < k) and not near:
+                ok = False
+                break
+        if not ok:
+            continue
+        if not (np.array_equal(out[b, :k], x[b, :k]) and np.all(out[b, k + 1:] == -1)):
+            continue
+        y = int(out[b, k])
+        if k < gamma:
+            r = np.maximum(P[k] - Q[k], 0.0)
+        else:
+            r = P[k]
+        if r.sum() == 0:
+            r = P[k]
+        R = r.sum()
+        if not 0 <= y < V or r[y] <= 0:
+            continue
+        C = np.cumsum(r)
+        thr = u[b, gamma] * R
+        lo = C[y - 1] if y > 0 else 0.0
+        valid[b] = lo <= thr + band * R and C[y] > thr - band * R
+    return valid
+
+
 def argmax_rows(logits: np.ndarray) -> np.ndarray:
     """Argmax over the last axis, ties to the smallest index (NumPy returns the first maximum)."""
     return np.argmax(np.asarray(logits, dtype=np.float32), axis=-1).astype(np.int64)

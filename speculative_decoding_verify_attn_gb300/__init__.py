@@ -11,5 +11,6 @@ from .binding import (  # noqa: F401
     spec_sample, spec_sample_workspace, spec_status_string, spec_verify_attn, spec_verify_attn_workspace,
 )
 from .binding import SPEC_ERR_SCRATCH_LIMIT, spec_verify_attn_noalloc  # noqa: F401,E402
+from .binding import SPEC_DEBUG_NO_LOADS  # noqa: F401,E402
 from .binding import SPEC_COMMIT_CHAIN, SPEC_COMMIT_TREE, SpecCommitArgs, spec_commit  # noqa: F401,E402
 from .binding import SpecLmheadArgs, spec_lmhead_sample, spec_lmhead_sample_workspace  # noqa: F401,E402

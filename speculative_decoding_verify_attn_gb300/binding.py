@@ -33,6 +33,8 @@ SPEC_STATUS_BAD_POS = 2
 SPEC_STATUS_BAD_TOKEN = 4
 SPEC_STATUS_TIMEOUT = 8
 
+SPEC_DEBUG_NO_LOADS = 1
+
 SPEC_COMMIT_CHAIN = 0
 SPEC_COMMIT_TREE = 1
 SPEC_SAMPLE_CHAIN = 0
@@ -49,7 +51,7 @@ class SpecAttnArgs(Structure):
         ("k", c_void_p), ("v", c_void_p), ("kv_stride_b", c_int64), ("kv_stride_h", c_int64),
         ("Lmax", c_int32), ("reserved0", c_int32),
         ("kv_len", c_void_p), ("tree_parent", c_void_p),
-        ("scale", c_float), ("reserved1", c_int32),
+        ("scale", c_float), ("debug_flags", c_int32),
         ("o", c_void_p), ("o_stride_b", c_int64), ("o_stride_t", c_int64), ("o_stride_h", c_int64),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("k_new", c_void_p), ("v_new", c_void_p),
@@ -218,7 +220,7 @@ def _host_i32(seq: Optional[Sequence[int]]):
 
 # ---------------------------------------------------------------------------- attention
 def verify_attn_args(q, k, v, kv_len, o, tree_parent=None, scale: float = 0.0, workspace=None,
-                     k_new=None, v_new=None):
+                     k_new=None, v_new=None, debug_flags: int = 0):
     """Fill SpecAttnArgs from tensors (k_new, v_new [B, nq, Hkv, D] for the fused append, or
     None).  Returns (args, keepalive)."""
     B, nq, Hq, D = q.shape
@@ -238,7 +240,7 @@ def verify_attn_args(q, k, v, kv_len, o, tree_parent=None, scale: float = 0.0, w
         q_dtype=_dtype_code(q), kv_dtype=_dtype_code(k), o_dtype=_dtype_code(o),
         q=_ptr(q), q_stride_b=q.stride(0), q_stride_t=q.stride(1), q_stride_h=q.stride(2),
         k=_ptr(k), v=_ptr(v), kv_stride_b=k.stride(0), kv_stride_h=k.stride(1),
-        Lmax=Lmax, kv_len=_ptr(kv_len), tree_parent=parent_ptr, scale=scale,
+        Lmax=Lmax, kv_len=_ptr(kv_len), tree_parent=parent_ptr, scale=scale, debug_flags=debug_flags,
         o=_ptr(o), o_stride_b=o.stride(0), o_stride_t=o.stride(1), o_stride_h=o.stride(2),
         workspace=_ptr(workspace), workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
     )
@@ -256,12 +258,13 @@ def spec_verify_attn_workspace(q, k, o, nq: Optional[int] = None) -> int:
 
 
 def spec_verify_attn(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0, workspace=None, stream=None,
-                     k_new=None, v_new=None):
+                     k_new=None, v_new=None, debug_flags: int = 0):
     """Verify attention (chain if tree_parent is None, else tree; tree_parent is host data).
 
     q [B, nq, Hq, D]; k, v [B, Hkv, Lmax, D]; kv_len [B] int32 (device); o [B, nq, Hq, D].
     With k_new, v_new [B, nq, Hkv, D] the call first writes them into cache positions
-    kv_len - nq .. kv_len - 1 (fused append).  Writes o and returns it."""
+    kv_len - nq .. kv_len - 1 (fused append).  debug_flags: SPEC_DEBUG_* test hooks (0 in normal
+    use).  Writes o and returns it."""
     _check_cuda(q, k, v, kv_len, o)
     if k_new is not None:
         _check_cuda(k_new, v_new)
@@ -269,7 +272,7 @@ def spec_verify_attn(q, k, v, kv_len, o, *, tree_parent=None, scale: float = 0.0
     if need == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_attn_workspace")
     ws = _workspace(need, q.device, workspace)
-    a, keep = verify_attn_args(q, k, v, kv_len, o, tree_parent, scale, ws, k_new, v_new)
+    a, keep = verify_attn_args(q, k, v, kv_len, o, tree_parent, scale, ws, k_new, v_new, debug_flags)
     st = lib().spec_verify_attn(byref(a), _stream_handle(stream))
     del keep
     if st != SPEC_OK:
@@ -442,7 +445,7 @@ def spec_verify_attn_noalloc(q, k, v, kv_len, o, *, tree_parent=None, scale: flo
     """spec_verify_attn for callers that cannot allocate device memory: the library uses its own
     fixed 64 MiB device scratch array instead of a caller workspace, and nothing here allocates
     (no torch workspace either).  Calls on one device share that array, so calls whose kernels
-    overlap on the GPU must not be issued; the first call on a device must precede any stream
+    overlap on the GPU must not be issued; the first call in a context must precede any stream
     capture.  Writes o and returns it."""
     global _noalloc_fn
     _check_cuda(q, k, v, kv_len, o)

@@ -22,9 +22,9 @@ LIBNAME = "libspecverify.so"
 LIBPATH = os.path.join(LIBDIR, LIBNAME)
 
 SOURCES = ["attn.cu", "attn_tc.cu", "attn_tc_pair.cu", "sample.cu", "sample_tree.cu", "lmhead.cu", "commit.cu",
-           "api.cpp", "noalloc.cu"]
+           "api.cpp", "noalloc.cu", "launch_cache.cpp"]
 HEADERS = ["common.cuh", "attn_common.cuh", "tcgen05.cuh", "ff.cuh", "attn_internal.h", "sample_internal.h",
-           "commit_internal.h", "lmhead_internal.h"]
+           "commit_internal.h", "lmhead_internal.h", "launch_cache.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -150,7 +150,7 @@ float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / s
 
 extern "C" {
 
-int spec_abi_version(void) { return 4; }
+int spec_abi_version(void) { return 5; }
 
 size_t spec_abi_struct_size(int which) {
   switch (which) {
@@ -194,6 +194,7 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   if ((st = check_o_layout(a->o, a->o_dtype, a->o_stride_b, a->o_stride_t, a->o_stride_h)) != SPEC_OK) return st;
   if (!a->kv_len) return SPEC_ERR_INVALID_ARG;
   if (!isfinite(a->scale)) return SPEC_ERR_INVALID_ARG;
+  if ((a->debug_flags & ~SPEC_DEBUG_NO_LOADS) != 0) return SPEC_ERR_INVALID_ARG;
   if ((a->k_new == nullptr) != (a->v_new == nullptr)) return SPEC_ERR_INVALID_ARG;
   if (a->k_new) {
     // the append moves 16-byte chunks: both row sets 16-byte aligned
@@ -228,6 +229,7 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
   p.o_bf16 = a->o_dtype == SPEC_BF16;
   p.kv_bf16 = a->kv_dtype == SPEC_BF16;
   p.verify_append = a->k_new != nullptr;
+  p.debug_no_loads = (a->debug_flags & SPEC_DEBUG_NO_LOADS) != 0;
   p.k_new = a->k_new; p.v_new = a->v_new;
   p.new_sb = a->new_stride_b; p.new_st = a->new_stride_t; p.new_sh = a->new_stride_h;
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);

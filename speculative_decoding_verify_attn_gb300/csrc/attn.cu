@@ -30,6 +30,7 @@
 #include "attn_common.cuh"
 #include "attn_internal.h"
 #include "common.cuh"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
       int issued = 0;
       int b, g, kb, ke, len;
       bool ok = true;
-      while (ok && walker_next(p, w, b, g, kb, ke, len)) {
+      while (ok && !p.debug_no_loads && walker_next(p, w, b, g, kb, ke, len)) {
         for (int key0 = kb; key0 < ke; key0 += kKeyTile) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, &s_abort)) {
             s_abort = 1;
@@ -771,7 +772,7 @@ static cudaError_t launch_bf16(const AttnParams& p, const CUtensorMap* tmK, cons
                                cudaStream_t stream) {
   const size_t smem = 1024 + kStages * 2 * (size_t)(kKeyTile * D * 2) + (size_t)kConsumerWarps * 16 * D * 2;
   auto kern = attn_partial_bf16<D, MASK, NKS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, (kConsumerWarps + 1) * 32, smem, stream>>>(*tmK, *tmV, p);
   return cudaGetLastError();

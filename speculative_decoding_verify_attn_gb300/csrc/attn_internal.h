@@ -61,6 +61,7 @@ struct AttnParams {
   // strides new_sb, new_st, new_sh) go to positions lens[b] - nq .. lens[b] - 1 first
   int verify_append;
   int64_t new_st;
+  int debug_no_loads;              // test hook: the producers issue no K/V copies (waits run out)
   unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
 };
 

@@ -31,6 +31,7 @@
 #include "attn_internal.h"
 #include "common.cuh"
 #include "tcgen05.cuh"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int t = 0;
       bool ok = true;
       int b, g, kb, ke, len;
-      while (ok && walker_next(p, w, b, g, kb, ke, len)) {
+      while (ok && !p.debug_no_loads && walker_next(p, w, b, g, kb, ke, len)) {
         for (int key0 = kb; key0 < ke; key0 += kTcKeys, ++t) {
           const int s = t % kTcStages;
           if (!mbar_wait_bounded(&empty[s], ((t / kTcStages) & 1) ^ 1u, &s_abort)) {
@@ -483,7 +484,7 @@ static cudaError_t launch_tc_mask(const AttnParams& p, const CUtensorMap* tmK, c
                                   cudaStream_t stream) {
   const size_t smem = attn_tc_smem_bytes();
   auto kern = attn_partial_tc<MASK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<p.grid_x * p.tc_groups, kTcThreads, smem, stream>>>(*tmK, *tmV, p);
   return cudaGetLastError();

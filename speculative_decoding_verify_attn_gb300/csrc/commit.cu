@@ -14,6 +14,7 @@
 
 #include "commit_internal.h"
 #include "common.cuh"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -83,7 +84,7 @@ cudaError_t launch_commit(const CommitParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const size_t smem = p.mode == SPEC_COMMIT_TREE ? commit_smem_bytes(p.nq, p.D, p.bf16) : 0;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(commit_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
   // one CTA per kv head (at most 8 per sequence) in tree mode, one per sequence in chain mode

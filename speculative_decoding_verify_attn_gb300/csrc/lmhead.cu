@@ -30,6 +30,7 @@
 #include "lmhead_internal.h"
 #include "spec_verify.h"
 #include "tcgen05.cuh"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -437,7 +438,7 @@ cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const C
   lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
   if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup) return cudaErrorInvalidValue;
   // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
-  e = cudaFuncSetAttribute(lmhead_argmax, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmemCap - 2560);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_argmax), kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
   const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
   lmhead_argmax<<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);

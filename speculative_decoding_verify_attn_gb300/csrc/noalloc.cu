@@ -8,34 +8,25 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the library holds its
 // SPEC_NOALLOC_SCRATCH_BYTES until the process exits.  Host code cannot use the symbol itself as
-// a device address (on the host it only names a shadow), so the array's device address is looked
-// up once per device with cudaGetSymbolAddress, with that device current, on the first call made
-// on it.  Calls share the array; calls that overlap on the GPU race on it.
+// a device address (on the host it only names a shadow), so every call looks the array's device
+// address up with cudaGetSymbolAddress in the context current on the calling thread.  The address
+// is not cached: it belongs to one context, and a caller may switch contexts (its own driver-API
+// context, or a new primary context after cudaDeviceReset) between calls, where a cached address
+// would point at memory the new context does not map.  After the first call in a context the
+// lookup is a host-side table read.  Calls share the array; calls that overlap on the GPU race.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "spec_verify.h"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_verify_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_verify_scratch on the current device (looked up once per device).
-int scratch_for_current_device(void** out) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return SPEC_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+// Device address of g_verify_scratch in the calling thread's current context.
+int scratch_for_current_context(void** out) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || p == nullptr) return SPEC_ERR_CUDA;
+  *out = p;
   return SPEC_OK;
 }
 
@@ -47,7 +38,7 @@ extern "C" int spec_verify_attn_noalloc(const spec_attn_args* args, spec_stream_
   if (need == 0) return SPEC_ERR_INVALID_ARG;
   if (need > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
-  const int st = scratch_for_current_device(&scratch);
+  const int st = scratch_for_current_context(&scratch);
   if (st != SPEC_OK) return st;
   spec_attn_args a = *args;
   a.workspace = scratch;

@@ -27,6 +27,7 @@
 #include "common.cuh"
 #include "ff.cuh"
 #include "sample_internal.h"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -570,6 +571,9 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   FF* s_slab = reinterpret_cast<FF*>(s_fin);   // residual mass of each of this CTA's slabs
   float4* s_r = reinterpret_cast<float4*>(s_fin + ((size_t)per * sizeof(FF) + 15) / 16 * 16);
   const bool keep = fin_keeps_resid(per);      // s_r[(slab * 4 + quarter) * 32 + lane]: a lane's 4 values
+  // diagnostic word at byte 4 of the workspace: this launch's CTAs per sequence, and whether the
+  // draw re-reads the residual row (bit 8) instead of scanning values kept in shared memory
+  if (blockIdx.x == 0 && tid == 0) p.status[1] = (uint32_t)CS | (keep ? 0u : 0x100u);
 
   // the decision's inputs, loaded ahead of the row statistics so that their latency overlaps:
   // lane i < gamma of warp 0 takes draft i (token, uniform, then the two logits the statistics
@@ -954,8 +958,7 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const long long need = (items + kStatWarps - 1) / kStatWarps;  // CTAs with at least a full set of items
   const int g1 = need < (long long)p.num_sms ? (int)(need > 0 ? need : 1) : p.num_sms;
   const size_t ring = (size_t)kStatWarps * kStatSlots * kStatChunk * sizeof(float);
-  e = cudaFuncSetAttribute(p.mode == SPEC_SAMPLE_CHAIN ? sample_stats<false> : sample_stats<true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(p.mode == SPEC_SAMPLE_CHAIN ? sample_stats<false> : sample_stats<true>), (int)ring);
   if (e != cudaSuccess) return e;
   if (p.mode != SPEC_SAMPLE_CHAIN) {
     sample_stats<true><<<g1, kStatWarps * 32, ring, stream>>>(p);
@@ -976,7 +979,7 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaFuncSetAttribute(sample_chain_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinSmemMax);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(sample_chain_finish), (int)kFinSmemMax);
   if (e != cudaSuccess) return e;
   int cs = 8;
   for (; cs > 1; cs >>= 1) {
@@ -985,7 +988,7 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
     cfg.gridDim = dim3((unsigned)(p.B * cs), 1, 1);
     cfg.dynamicSmemBytes = fin_smem_bytes((nslabs + cs - 1) / cs);
     int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, sample_chain_finish, &cfg) == cudaSuccess && active >= p.B) break;
+    if (max_active_clusters(&active, reinterpret_cast<const void*>(sample_chain_finish), &cfg) == cudaSuccess && active >= p.B) break;
     (void)cudaGetLastError();
   }
   const size_t smem = fin_smem_bytes((nslabs + cs - 1) / cs);

@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "ff.cuh"
 #include "sample_internal.h"
+#include "launch_cache.h"
 
 namespace specv {
 
@@ -457,7 +458,7 @@ cudaError_t launch_sample_tree(const SampleParams& p, cudaStream_t stream) {
   const int share4 = (p.V / 4 + kTreeCS - 1) / kTreeCS;
   const size_t smem = 2 * (size_t)share4 * sizeof(float4);
   if (smem <= kTreeSmemMax) {
-    e = cudaFuncSetAttribute(sample_tree_stochastic<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(sample_tree_stochastic<true>), (int)smem);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = smem;
     e = cudaLaunchKernelEx(&cfg, sample_tree_stochastic<true>, p);

@@ -46,7 +46,7 @@ def test_struct_layouts_match(L):
     assert L.spec_abi_struct_size(3) == ctypes.sizeof(b.SpecCommitArgs)
     assert L.spec_abi_struct_size(4) == ctypes.sizeof(b.SpecLmheadArgs)
     assert L.spec_abi_struct_size(5) == 0
-    assert L.spec_abi_version() == 4
+    assert L.spec_abi_version() == 5
     assert L.spec_status_string(-3).decode().startswith("workspace")
 
 

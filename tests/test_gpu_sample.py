@@ -1,9 +1,10 @@
 """GPU parity: spec_sample through the C ABI against the CPU oracle.
 
 Accepted counts and emitted token ids must be bit-exact given the same uniforms, except in
-sequences where the oracle reports a decision within 1e-6 of its threshold (counted and reported
-separately).  Both the one-warp-per-sequence small-vocabulary path and the chunked
-large-vocabulary path are covered, with ragged vocabulary tails.
+sequences where the oracle reports a decision within 1e-6 of its threshold.  Those are counted and
+reported separately, and their outcome must still be one the rule gives with the near decisions
+taken either way.  Both the one-warp-per-sequence small-vocabulary path and the chunked
+large-vocabulary path are covered, with ragged vocabulary tails and the batches the bench times.
 """
 
 import numpy as np
@@ -27,7 +28,7 @@ def sv():
     return sv
 
 
-def gpu_chain(sv, inp, mode=None):
+def gpu_chain(sv, inp, mode=None, diag=False):
     torch = torch_mod()
     mode = sv.SPEC_SAMPLE_CHAIN if mode is None else mode
     tl = to_dev(inp["target_logits"])
@@ -37,16 +38,30 @@ def gpu_chain(sv, inp, mode=None):
     u = to_dev(inp["uniforms"]) if mode == sv.SPEC_SAMPLE_CHAIN else None
     out = torch.full((B, rows), -7, dtype=torch.int32, device=tl.device)
     nacc = torch.full((B,), -7, dtype=torch.int32, device=tl.device)
-    ws = torch.empty(sv.spec_sample_workspace(mode, tl), dtype=torch.uint8, device=tl.device)
+    ws = torch.zeros(sv.spec_sample_workspace(mode, tl), dtype=torch.uint8, device=tl.device)
     sv.spec_sample(mode, tl, out, nacc, draft_logits=dl, draft_tokens=x, uniforms=u, workspace=ws)
     torch.cuda.synchronize()
-    return to_np(out), to_np(nacc), sv.read_status(ws)
+    res = (to_np(out), to_np(nacc), sv.read_status(ws))
+    if diag:
+        # the finish kernel's launch shape (byte 4 of the workspace): CTAs per sequence, and bit 8
+        # when the draw re-reads the residual row instead of scanning kept values
+        w = int(ws[4:8].view(torch.int32).item())
+        res = res + ({"ctas_per_sequence": w & 0xFF, "rereads_residual": bool(w & 0x100)},)
+    return res
 
 
-def compare_chain(inp, out, nacc, what, max_near_frac=0.5):
-    """Bit-exact outside the near-threshold band.  With a 128K vocabulary the band for the final
-    draw (1e-6 * R around any CDF step) is comparable to one token's mass, so a sizeable share of
-    draws falls inside it; those are counted, and how many of them still match is reported."""
+# Sequences with a decision within 1e-6 of its threshold, as a share of a batch: with V = 128 256
+# and logits of standard deviation 2 the final draw's band (1e-6 R on each side of a CDF step) holds
+# about 15 % of the draws (5 of 32, 0 of 16 and 14 of 100 sequences in the bench-shaped batches);
+# twice that leaves room for batch-to-batch spread and still fails a band that swallowed the draws.
+MAX_NEAR_FRAC = 0.3
+
+
+def compare_chain(inp, out, nacc, what, max_near_frac=MAX_NEAR_FRAC):
+    """Bit-exact outside the near-threshold band; inside it (a decision within 1e-6 of its
+    threshold, which fp32 kernels and the fp64 oracle may round to different sides), the outcome
+    must still be one the rule gives with those decisions taken either way (oracle
+    chain_outcome_valid).  Counts are printed and returned."""
     ref_out, ref_k, near = osm.spec_sample_chain(inp["target_logits"], inp["draft_logits"],
                                                  inp["draft_tokens"], inp["uniforms"])
     far = ~near
@@ -54,8 +69,14 @@ def compare_chain(inp, out, nacc, what, max_near_frac=0.5):
     bad_t = np.nonzero(np.any(out != ref_out, axis=1) & far)[0]
     assert len(bad_k) == 0, f"{what}: accepted counts differ at {bad_k[:10]} ({nacc[bad_k[:5]]} vs {ref_k[bad_k[:5]]})"
     assert len(bad_t) == 0, f"{what}: tokens differ at {bad_t[:10]}"
+    idx = np.nonzero(near)[0]
+    if len(idx):
+        ok = osm.chain_outcome_valid(inp["target_logits"][idx], inp["draft_logits"][idx], inp["draft_tokens"][idx],
+                                     inp["uniforms"][idx], out[idx], nacc[idx])
+        assert np.all(ok), f"{what}: near-threshold sequences {idx[~ok][:10]} have outcomes no rounding explains"
     near_match = int(np.sum(near & (nacc == ref_k) & np.all(out == ref_out, axis=1)))
-    print(f"{what}: {len(near)} sequences, {int(near.sum())} near-threshold ({near_match} of them match too)")
+    print(f"{what}: {len(near)} sequences, {int(near.sum())} near-threshold (all valid; {near_match} of them "
+          f"identical to the oracle's own outcome)")
     assert near.mean() <= max_near_frac, f"{what}: {near.sum()} near-threshold sequences"
     return int(near.sum())
 
@@ -76,6 +97,24 @@ def test_large_vocab_configs(sv, name, B):
     out, nacc, st = gpu_chain(sv, inp)
     assert st == 0
     compare_chain(inp, out, nacc, name)
+
+
+@pytest.mark.parametrize("name,B,cs,rereads", [
+    ("magicdec-64k", 32, 4, False),      # the MagicDec bench batch: 4 CTAs per sequence, values kept
+    ("llama3-70b-layer", 16, 8, False),  # the 70B bench batch (gamma 6, correlated draft): 8 CTAs
+    ("llama3-8b-layer", 100, 1, True),   # more sequences than 152 / 2 SMs: one CTA per sequence,
+                                         # 251 slabs, the draw re-reads the residual row
+])
+def test_bench_batches_full_vocab(sv, name, B, cs, rereads):
+    """Stochastic chain at V = 128 256 with the batches the bench times.  The finish kernel's
+    cluster size depends on B, so each case asserts which configuration it exercised."""
+    cfg = CONFIGS[name]
+    inp = gen.chain_sample_inputs(B, cfg.gamma, cfg.vocab, cfg.seed + B, cfg.target_sigma, cfg.draft_noise_sigma,
+                                  cfg.draft_corr)
+    out, nacc, st, shape = gpu_chain(sv, inp, diag=True)
+    assert st == 0
+    assert shape == {"ctas_per_sequence": cs, "rereads_residual": rereads}, shape
+    compare_chain(inp, out, nacc, f"{name} B={B}")
 
 
 @pytest.mark.parametrize("V", [2052, 5000, 8196, 40000])

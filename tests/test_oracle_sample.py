@@ -310,3 +310,75 @@ def test_near_threshold_flag():
     _, _, f1 = osm.spec_sample_chain(tl, dl, x, near_u)
     _, _, f2 = osm.spec_sample_chain(tl, dl, x, far_u)
     assert f1[0] and not f2[0]
+
+
+def test_outcome_validity_accepts_own_outcome_and_only_it_away_from_thresholds():
+    """chain_outcome_valid: the oracle's own outcome is always valid; for a sequence with no near
+    decision, changing the count by one or the emitted token by one makes it invalid."""
+    rng = np.random.default_rng(31)
+    B, gamma, V = 400, 3, 12
+    tl = (2 * rng.standard_normal((B, gamma + 1, V))).astype(np.float32)
+    dl = (tl[:, :gamma] + rng.standard_normal((B, gamma, V))).astype(np.float32)
+    Q = sp_softmax(dl.astype(np.float64), axis=-1)
+    x = np.stack([_draw_tokens(rng, Q[b, i], ()) for b in range(B) for i in range(gamma)]).reshape(B, gamma)
+    u = rng.random((B, gamma + 1), dtype=np.float32)
+    out, nacc, near = osm.spec_sample_chain(tl, dl, x, u)
+    assert np.all(osm.chain_outcome_valid(tl, dl, x, u, out, nacc))
+    far = np.nonzero(~near)[0]
+    assert len(far) > 300
+    for b in far:
+        k, y = int(nacc[b]), int(out[b, nacc[b]])
+        for y2 in (y - 1, y + 1):
+            if 0 <= y2 < V:
+                o2 = out[b:b + 1].copy()
+                o2[0, k] = y2
+                assert not osm.chain_outcome_valid(tl[b:b + 1], dl[b:b + 1], x[b:b + 1], u[b:b + 1], o2, nacc[b:b + 1])[0]
+        for k2 in (k - 1, k + 1):
+            if 0 <= k2 <= gamma:
+                o2 = np.full((1, gamma + 1), -1, np.int32)
+                o2[0, :k2] = x[b, :k2]
+                # every token is tried at the new count: none may be valid
+                for y2 in range(V):
+                    o2[0, k2] = y2
+                    assert not osm.chain_outcome_valid(tl[b:b + 1], dl[b:b + 1], x[b:b + 1], u[b:b + 1], o2,
+                                                       np.array([k2]))[0]
+
+
+def test_outcome_validity_lets_near_decisions_go_either_way():
+    # draw: uniform P over 4 tokens, every draft accepted (Q = P), u R = 0.5 = C(1) exactly: the
+    # exact rule gives y = 2, and y = 1 lies on the other side of the step
+    V, gamma = 4, 1
+    tl = np.zeros((1, gamma + 1, V), np.float32)
+    dl = np.zeros((1, gamma, V), np.float32)
+    x = np.array([[0]], np.int32)
+    u = np.array([[0.3, 0.5]], np.float32)
+    out, nacc, near = osm.spec_sample_chain(tl, dl, x, u)
+    assert nacc[0] == 1 and out[0, 1] == 2 and near[0]
+    for y, ok in ((0, False), (1, True), (2, True), (3, False)):
+        o = np.array([[0, y]], np.int32)
+        assert osm.chain_outcome_valid(tl, dl, x, u, o, nacc)[0] == ok, y
+    # accept test: P(x)/Q(x) = 0.5 and u = 0.5 (rejected by the strict test, but near): both counts
+    P = np.array([0.25, 0.25, 0.25, 0.25])
+    Qd = np.array([0.5, 0.5 / 3, 0.5 / 3, 0.5 / 3])
+    tl = _logits_from_probs(P)[None, None].repeat(2, 1)
+    dl = _logits_from_probs(Qd)[None, None]
+    ratio = sp_softmax(tl[0, 0].astype(np.float64))[0] / sp_softmax(dl[0, 0].astype(np.float64))[0]
+    u = np.array([[np.float32(ratio), 0.9]], np.float32)
+    out, nacc, near = osm.spec_sample_chain(tl, dl, x, u)
+    assert near[0]
+    # the count the exact rule did not take, with the draw its residual row gives
+    k2 = 1 - int(nacc[0])
+    u_draw = np.array([[0.0, 0.9]], np.float32) if k2 == 1 else np.array([[0.99, 0.9]], np.float32)
+    o2, n2, _ = osm.spec_sample_chain(tl, dl, x, u_draw)
+    assert n2[0] == k2
+    assert osm.chain_outcome_valid(tl, dl, x, u, out, nacc)[0]
+    assert osm.chain_outcome_valid(tl, dl, x, u, o2, n2)[0]
+
+
+def test_outcome_validity_bad_token_row():
+    tl = np.zeros((1, 3, 4), np.float32)
+    dl = np.zeros((1, 2, 4), np.float32)
+    x = np.array([[1, 9]], np.int32)
+    u = np.full((1, 3), 0.5, np.float32)
+    assert osm.chain_outcome_valid(tl, dl, x, u, np.full((1, 3), -1, np.int32), np.array([-1]))[0]
+    assert not osm.chain_outcome_valid(tl, dl, x, u, np.array([[1, 2, -1]], np.int32), np.array([1]))[0]
