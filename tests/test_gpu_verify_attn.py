@@ -164,6 +164,7 @@ def _device_inputs(cfg, seed):
     return q, k, v, kv_len
 
 
+@pytest.mark.timeout(900)
 @pytest.mark.parametrize("name", ["magicdec-64k", "llama3-70b-layer", "medusa-tree-8k", "llama3-8b-layer"])
 def test_full_size_every_segment(sv, name):
     """The full-size workloads in the launch configuration the bench times, checked segment by
