@@ -36,7 +36,10 @@ from workloads.configs import get_config  # noqa: E402
 METRIC = "verify-attn KV GB/s (% HBM peak); spec_sample rounds/s; at 1 GB300"
 DEFAULT_WORKLOAD = "magicdec-64k"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 126 << 20
+# the bench line's sub-records: every workload that has verify attention at full size
+SUB_WORKLOADS = ("llama3-70b-layer", "llama3-8b-layer", "medusa-tree-8k", "magicdec-64k")
 
 
 def parse():
@@ -52,6 +55,8 @@ def parse():
     ap.add_argument("--clocks-csv", default=None, help="write the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--no-graphs", action="store_true", help="issue every call eagerly instead of graph replays")
     ap.add_argument("--sinks", type=int, default=0, help="attention-sink slots at the front of the draft ring")
+    ap.add_argument("--no-sub-configs", action="store_true",
+                    help="time only --workload, not the other full-size workloads' sub-records")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -63,6 +68,28 @@ def peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: copy, read+write bytes)"
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: a kernel timed alone) and where it comes from."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16 burst (no MEASURED_PEAKS.json)"
+
+
+def profile_counters(workload):
+    """ncu counters committed for a workload's verify kernel (profiles/roofline_counters.json),
+    or None when absent or taken on another kernel revision than the one built now."""
+    path = os.path.join(ROOT, "profiles", "roofline_counters.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(workload)
+    if not d or d.get("kernel_rev") != KERNEL_REVS.get(workload):
+        return None
+    return d
 
 
 # ---------------------------------------------------------------------------- distributed plumbing
@@ -795,6 +822,148 @@ def run_reference(args, cfg):
     return 0
 
 
+def verify_flops(cfg, inp):
+    """Dense-over-context flops of one verify call: 4 * sum_b L_b * Hq * nq * D (QK^T and PV)."""
+    return 4 * int(inp["kv_len_h"].sum()) * cfg.Hq * cfg.nq * cfg.D
+
+
+def time_draft_cold(runner, K, device):
+    """One draft-window call (one appended token) with L2 flushed before every replay: the
+    cold-cache figure of the draft step, beside the in-round figure where steps 2-4 re-read a
+    ring that the step before left in L2."""
+    import torch
+    cfg, inp = runner.cfg, runner.inp
+    stream = torch.cuda.Stream(device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        runner.draft(0)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            runner.draft(0)
+        for _ in range(3):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+    us = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    nb = step_bytes(cfg, inp)["window"]
+    return {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "bytes": nb, "l2": "flushed (512 MB write) before every call"}
+
+
+def oracle_check_sampling(cfg, runner):
+    """CPU-oracle leg: the oracle's spec_sample on the bench's own sampling inputs (copied back
+    from the device), against the GPU's outputs of the last timed call.  Returns the counts the
+    near-threshold rule reports separately: sequences with a decision within 1e-6 of its threshold,
+    how many of them are valid outcomes and how many identical; and the mismatches elsewhere (0)."""
+    from oracle import sample as osm
+    inp = runner.inp
+    if cfg.tree_nodes:
+        parent = inp["tree"]
+        out, nodes, nacc = osm.tree_greedy(inp["tl"].cpu().numpy(), inp["x"].cpu().numpy(), parent,
+                                           int(inp["out"].shape[1]))
+        same = bool(np.array_equal(out, inp["out"].cpu().numpy()) and np.array_equal(nacc, inp["nacc"].cpu().numpy()))
+        return {"mode": "tree_greedy", "sequences": cfg.B, "near": 0, "mismatch": 0 if same else cfg.B,
+                "note": "greedy argmax decisions are exact; no near-threshold band"}
+    tl, dl = inp["tl"].cpu().numpy(), inp["dl"].cpu().numpy()
+    x, u = inp["x"].cpu().numpy(), inp["u"].cpu().numpy()
+    g_out, g_k = inp["out"].cpu().numpy(), inp["nacc"].cpu().numpy()
+    r_out, r_k, near = osm.spec_sample_chain(tl, dl, x, u)
+    far = ~near
+    mism = int(np.sum(far & ((g_k != r_k) | np.any(g_out != r_out, axis=1))))
+    idx = np.nonzero(near)[0]
+    valid = int(np.sum(osm.chain_outcome_valid(tl[idx], dl[idx], x[idx], u[idx], g_out[idx], g_k[idx]))) if len(idx) else 0
+    ident = int(np.sum(near & (g_k == r_k) & np.all(g_out == r_out, axis=1)))
+    return {"mode": "chain", "sequences": int(cfg.B), "near": int(near.sum()), "near_valid": valid,
+            "near_identical": ident, "far_mismatch": mism, "band": osm.NEAR_BAND}
+
+
+def measure(cfg, args, pg, device, rank, world, full):
+    """Times one workload's step (graph replays) and returns its record; with `full` also the
+    extra legs (commit, verify with append, stochastic tree, LM-head, cold draft, e2e)."""
+    import torch
+    import speculative_decoding_verify_attn_gb300 as sv
+    inp = make_inputs(cfg, device, seed=cfg.seed + 7919 * rank)
+    runner = Runner(sv, cfg, inp, device)
+    runner.n_sinks = args.sinks if full else 0
+    nb = step_bytes(cfg, inp)
+    t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs,
+                   clocks_csv=args.clocks_csv if full else None)
+    total_ms = max_over_ranks(pg, t["total_ms"], device)
+    ver_ms = max_over_ranks(pg, t["verify_ms"], device)
+    smp_ms = max_over_ranks(pg, t["sample_ms"], device)
+    win_ms = max_over_ranks(pg, t["window_ms"], device)
+    kv_all = sum_over_ranks(pg, float(nb["verify_kv"]), device)
+    value = kv_all / (ver_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    tpeak, tpeak_kind = tensor_peak()
+    achieved = nb["verify_total"] / (t["verify_ms"] * 1e-3) / 1e9
+    tflops = verify_flops(cfg, inp) / (t["verify_ms"] * 1e-3) / 1e12
+    counters = profile_counters(cfg.name)
+    rec = {
+        "workload": cfg.name,
+        "config": {"batch": cfg.B, "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D,
+                   "context": list(cfg.ctx), "gamma": cfg.gamma, "tree_nodes": cfg.tree_nodes,
+                   "query_rows_per_kv_head": cfg.nq * cfg.G, "window": cfg.window, "vocab": cfg.vocab,
+                   "kv_dtype": cfg.kv_dtype},
+        "verify_kv_gbs": value,
+        "hbm_frac_verify": value / world / peak,
+        "verify_ms": ver_ms,
+        "verify_tflops": tflops,
+        "tensor_frac_verify": tflops / tpeak,
+        "tokens_verified_per_s": world * cfg.B * cfg.nq / (ver_ms * 1e-3),
+        "spec_sample_rounds_per_s": world * cfg.B / (smp_ms * 1e-3),
+        "sample_gbs": world * nb["sample"] / (smp_ms * 1e-3) / 1e9,
+        "sample_hbm_frac": nb["sample"] / (smp_ms * 1e-3) / 1e9 / peak,
+        "draft_window_gbs": (world * nb["window"] * (cfg.draft_steps or 1) / (win_ms * 1e-3) / 1e9) if cfg.window else None,
+        "step_breakdown_ms": {"draft_window_x%d" % cfg.draft_steps: win_ms, "verify": ver_ms, "sample": smp_ms},
+        "ms_per_step": total_ms / args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": counters.get("dram_bytes_per_launch") if counters else None,
+                     "kernel": "spec_verify_attn (partial + merge, one call)", "peak_source": peak_kind},
+        "tensor_roofline": {"achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                            "flops": "4 * sum(kv_len) * Hq * nq * D (dense over the context)",
+                            "peak_source": tpeak_kind,
+                            "ncu_tensor_pipe_active_pct": counters.get("tensor_pipe_active_pct") if counters else None},
+        "l2": ("L2 flushed (512 MB write) before every timed step; flush time excluded" if t["l2_flush"] else
+               f"inputs larger than L2: the {nb['verify_kv'] / 1e9:.2f} GB verify cache streamed each step evicts L2"
+               + ("; draft steps 2-4 of a round re-read the ring (may be L2-resident)" if cfg.window else "")),
+        "clocks": t["clocks"],
+    }
+    extra = {"t": t, "nb": nb, "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "value": value,
+             "total_ms": total_ms, "ver_ms": ver_ms, "smp_ms": smp_ms, "win_ms": win_ms, "counters": counters,
+             "launches_per_step": t["kernels_per_step"] if t["kernels_per_step"] is not None
+                                  else runner.launches_per_step()}
+    if full:
+        rec["commit"] = time_commit(runner, 200, device)
+        rec["verify_with_append"] = time_verify_append(runner, max(5, min(args.steps, 50)), device)
+        rec["tree_stochastic_sample"] = time_tree_stochastic(runner, max(5, min(args.steps, 100)), device) \
+            if cfg.tree_nodes else None
+        rec["lmhead_greedy_sample"] = time_lmhead(runner, max(5, min(args.steps, 50)), device)
+        if cfg.window:
+            cold = time_draft_cold(runner, max(5, min(args.steps, 50)), device)
+            cold["gbs"] = sum_over_ranks(pg, cold["gbs"], device)
+            rec["draft_window_cold"] = cold
+        e2e = None
+        if not args.no_e2e:
+            sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
+            sec = max_over_ranks(pg, sec, device)
+            e2e = {"value": sum_over_ranks(pg, float(nb["verify_kv"]), device) / sec / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                   "ms_per_step": 1000 * sec, "rounds_per_s": world * cfg.B / sec}
+        extra["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        rec["sample_near_threshold"] = oracle_check_sampling(cfg, runner)
+    del runner, inp
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec, extra
+
+
 def main():
     args = parse()
     cfg = get_config(args.workload)
@@ -812,42 +981,18 @@ def main():
     torch.cuda.set_device(device)
     from speculative_decoding_verify_attn_gb300 import build as _build
     _build.build()
-    import speculative_decoding_verify_attn_gb300 as sv
 
-    inp = make_inputs(cfg, device, seed=cfg.seed + 7919 * rank)
-    runner = Runner(sv, cfg, inp, device)
-    runner.n_sinks = args.sinks
-    nb = step_bytes(cfg, inp)
-    t = time_steps(runner, args.steps, args.warmup, pg, device, use_graphs=not args.no_graphs,
-                   clocks_csv=args.clocks_csv)
-    total_ms = max_over_ranks(pg, t["total_ms"], device)
-    ver_ms = max_over_ranks(pg, t["verify_ms"], device)
-    smp_ms = max_over_ranks(pg, t["sample_ms"], device)
-    win_ms = max_over_ranks(pg, t["window_ms"], device)
-    kv_all = sum_over_ranks(pg, float(nb["verify_kv"]), device)
-    value = kv_all / (ver_ms * 1e-3) / 1e9
-    peak, peak_kind = peaks()
-    achieved = nb["verify_total"] / (t["verify_ms"] * 1e-3) / 1e9
-    traffic_path = os.path.join(ROOT, "profiles", "verify_traffic.json")
-    traffic = None
-    if os.path.exists(traffic_path):
-        tj = json.load(open(traffic_path))
-        if tj.get("workload") == cfg.name and tj.get("kernel_rev") == KERNEL_REV:
-            traffic = tj.get("bytes_per_launch")
-    commit = time_commit(runner, 200, device)
-    verify_append = time_verify_append(runner, max(5, min(args.steps, 50)), device)
-    tree_sto = time_tree_stochastic(runner, max(5, min(args.steps, 100)), device) if cfg.tree_nodes else None
-    lmhead = time_lmhead(runner, max(5, min(args.steps, 50)), device)
-    e2e = None
-    if not args.no_e2e:
-        sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
-        sec = max_over_ranks(pg, sec, device)
-        e2e = {"value": sum_over_ranks(pg, float(nb["verify_kv"]), device) / sec / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": 1000 * sec, "rounds_per_s": world * cfg.B / sec}
+    main_rec, x = measure(cfg, args, pg, device, rank, world, full=True)
+    subs = {}
+    if not args.no_sub_configs and not args.batch:
+        for name in SUB_WORKLOADS:
+            if name != cfg.name:
+                subs[name], _ = measure(get_config(name), args, pg, device, rank, world, full=False)
+    t = x["t"]
+    traffic = main_rec["roofline"]["traffic"]
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "metric": METRIC, "value": x["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": x["total_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.kv_dtype, "data": "synthetic",
         "config": {"workload": cfg.name, "batch": cfg.B, "q_heads": cfg.Hq, "kv_heads": cfg.Hkv,
                    "head_dim": cfg.D, "context": list(cfg.ctx), "gamma": cfg.gamma, "window": cfg.window,
@@ -855,30 +1000,33 @@ def main():
                    "parallelism": f"replicas x{world}",
                    "launch": "one CUDA graph per op (captured through the binding), replayed" if t["graphs"]
                              else "eager calls through the binding",
-                   "l2": ("L2 flushed (512 MB write) before every timed step; flush time excluded" if t["l2_flush"] else
-                          f"inputs larger than L2: the {nb['verify_kv'] / 1e9:.2f} GB verify cache streamed each step "
-                          "evicts L2" + ("; draft steps 2-4 of a round re-read the ring (may be L2-resident)"
-                                         if cfg.window else ""))},
-        "hbm_frac_verify": value / world / peak,
-        "spec_sample_rounds_per_s": world * cfg.B / (smp_ms * 1e-3),
-        "tokens_verified_per_s": world * cfg.B * cfg.nq / (ver_ms * 1e-3),
-        "draft_window_gbs": (world * nb["window"] * (cfg.draft_steps or 1) / (win_ms * 1e-3) / 1e9) if cfg.window else None,
-        "sample_gbs": world * nb["sample"] / (smp_ms * 1e-3) / 1e9,
-        "step_breakdown_ms": {"draft_window_x%d" % cfg.draft_steps: win_ms, "verify": ver_ms, "sample": smp_ms},
-        "commit": commit,
-        "verify_with_append": verify_append,
-        "tree_stochastic_sample": tree_sto,
-        "lmhead_greedy_sample": lmhead,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "spec_verify_attn (split-KV partial + merge, one call)",
-                     "peak_source": peak_kind},
-        "gpu_launches": (t["kernels_per_step"] if t["kernels_per_step"] is not None
-                         else runner.launches_per_step()) * args.steps,
+                   "l2": main_rec["l2"]},
+        "hbm_frac_verify": main_rec["hbm_frac_verify"],
+        "spec_sample_rounds_per_s": main_rec["spec_sample_rounds_per_s"],
+        "tokens_verified_per_s": main_rec["tokens_verified_per_s"],
+        "draft_window_gbs": main_rec["draft_window_gbs"],
+        "draft_window_gbs_note": "in-round figure: steps 2-4 re-read a ring the step before left in L2 "
+                                 "(see draft_window_cold for the L2-flushed call)" if cfg.window else None,
+        "draft_window_cold": main_rec.get("draft_window_cold"),
+        "sample_gbs": main_rec["sample_gbs"],
+        "sample_hbm_frac": main_rec["sample_hbm_frac"],
+        "sample_near_threshold": main_rec.get("sample_near_threshold"),
+        "step_breakdown_ms": main_rec["step_breakdown_ms"],
+        "commit": main_rec["commit"],
+        "verify_with_append": main_rec["verify_with_append"],
+        "tree_stochastic_sample": main_rec["tree_stochastic_sample"],
+        "lmhead_greedy_sample": main_rec["lmhead_greedy_sample"],
+        "roofline": {"bound": "hbm", "achieved": x["achieved"], "peak": x["peak"], "unit": "GB/s",
+                     "frac": x["achieved"] / x["peak"], "traffic": traffic,
+                     "kernel": "spec_verify_attn (split-KV partial + merge, one call)", "peak_source": x["peak_kind"]},
+        "tensor_roofline": main_rec["tensor_roofline"],
+        "workloads": subs,
+        "gpu_launches": x["launches_per_step"] * args.steps,
         "gpu_launches_source": "kernel nodes of the captured step graphs" if t["kernels_per_step"] is not None
                                else "launch rule of the library",
         "clocks": t["clocks"],
         "wall_s_timed": t["wall_s"],
-        "e2e": e2e,
+        "e2e": x.get("e2e"),
     }
     if rank == 0 and not args.no_cpu_baseline:
         r = oracle_sample_run(cfg, 11, budget_s=15.0)
@@ -894,8 +1042,10 @@ def main():
     return 0
 
 
-# Revision tag of the verify kernel that profiles/verify_traffic.json was measured on.
-KERNEL_REV = "mma8w-kt128-v3"
+# Revision tag of each verify kernel that profiles/roofline_counters.json was measured on; a
+# counter taken on another revision is not reported.
+KERNEL_REVS = {"magicdec-64k": "mma8w-kt128-v3", "llama3-70b-layer": "tc2wg-kt128-v2",
+               "llama3-8b-layer": "mma8w-kt128-v3", "medusa-tree-8k": "pair-kt64-v4"}
 
 if __name__ == "__main__":
     sys.exit(main())

@@ -101,7 +101,9 @@ def test_large_vocab_configs(sv, name, B):
 
 @pytest.mark.parametrize("name,B,cs,rereads", [
     ("magicdec-64k", 32, 4, False),      # the MagicDec bench batch: 4 CTAs per sequence, values kept
-    ("llama3-70b-layer", 16, 8, False),  # the 70B bench batch (gamma 6, correlated draft): 8 CTAs
+    ("llama3-70b-layer", 16, 4, False),  # the 70B bench batch (gamma 6, correlated draft): sixteen
+                                         # 8-CTA clusters are not all resident at once, so 4 CTAs
+    ("llama3-8b-layer", 50, 2, True),    # 2 CTAs per sequence, 126 slabs each: re-reads the row
     ("llama3-8b-layer", 100, 1, True),   # more sequences than 152 / 2 SMs: one CTA per sequence,
                                          # 251 slabs, the draw re-reads the residual row
 ])

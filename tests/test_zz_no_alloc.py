@@ -46,7 +46,7 @@ def test_noalloc_matches_workspace_entry_and_oracle_on_two_calls():
     torch = torch_mod()
     import speculative_decoding_verify_attn_gb300 as sv
     tree = np.array([-1, 0, 0, 1, 2, 2, 3], dtype=np.int32)
-    cases = [(_inputs(101, [1300, 2049, 640]), None), (_inputs(202, [777, 96]), tree)]
+    cases = [(_inputs(101, [1300, 2049, 640]), None), (_inputs(202, [777, 96], tree), tree)]
     refs = []
     for (_, d), par in cases:
         o_ref = torch.full(d["q"].shape, float("nan"), dtype=torch.float32, device=d["q"].device)
