@@ -17,7 +17,9 @@
 // P.V of tile t, so the warpgroup's next scores are ready when it finishes a tile.  mu is the
 // lazily updated row max of the other tensor-core kernel (O_w rescaled in TMEM only when a tile's
 // max exceeds it by more than 2^8).  A stage is free once both issuers' P.V of its tile completed
-// (two commits on its `empty` barrier).
+// (two commits on its `empty` barrier).  P.V completions are signalled per S buffer (pvdone[w][t & 1]:
+// phase t >> 1 of that barrier is P.V(t)), so a warpgroup waits for one only where it touches O (a
+// rescale, the part's epilogue) and never needs to observe each of them to keep count.
 // TMEM columns (512): block w at 256 w: S buffers [0,64) and [64,128), O [128,256).
 // Query row m of a block is TMEM lane m and row m of the Q tile.
 #include <cuda.h>
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   pdl_launch_dependents();  // the merge may be scheduled as SMs free up
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kPStages], empty[kPStages];
-  __shared__ uint64_t sfull[2][2], pfull[2][2], pvdone[2], ofree[2], qfull[2], drain[2];
+  __shared__ uint64_t sfull[2][2], pfull[2][2], pvdone[2][2], ofree[2], qfull[2], drain[2];
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
@@ -162,7 +164,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&sfull[w][1], 1);
       mbar_init(&pfull[w][0], 4);
       mbar_init(&pfull[w][1], 4);
-      mbar_init(&pvdone[w], 1);
+      mbar_init(&pvdone[w][0], 1);
+      mbar_init(&pvdone[w][1], 1);
       mbar_init(&ofree[w], 4);
       mbar_init(&qfull[w], 4);
       mbar_init(&drain[w], 1);
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const uint64_t bdesc = tc::smem_desc(vb + ks * 2048, kPHalf, 1024);
           tc::mma_ts(od, pa + ks * 8, bdesc, kPIdescPV, (ks > 0 || T.i > 0) ? 1u : 0u);
         }
-        tc::commit(&pvdone[wm]);
+        tc::commit(&pvdone[wm][t & 1]);
         tc::commit(&empty[t % kPStages]);
         return true;
       };
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           if (__any_sync(0xffffffffu, need)) {
             // O may only be touched once the previous P.V has completed
             if (pv_seen < t) {
-              if (!warp_wait(&pvdone[wg], (t - 1) & 1)) { ok = false; break; }
+              if (!warp_wait(&pvdone[wg][(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
               pv_seen = t;
               tc::fence_after();
             }
@@ -434,12 +437,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
           tc::st_wait();
           l += real ? (sums[0] + sums[1]) + (sums[2] + sums[3]) : 0.f;
         }
-        // observe the previous P.V completion before this tile's P is handed over, so that the
-        // P.V barrier never runs two phases ahead of this warpgroup
-        if (pv_seen < t) {
-          if (!warp_wait(&pvdone[wg], (t - 1) & 1)) { ok = false; break; }
-          pv_seen = t;
-        }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[wg][t & 1]);
@@ -447,7 +444,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (!ok) break;
       // ---- epilogue: the part's (m, l, o) record of this row block, once its last P.V is done
       if (pv_seen < t) {
-        if (!warp_wait(&pvdone[wg], (t - 1) & 1)) { ok = false; break; }
+        if (!warp_wait(&pvdone[wg][(t - 1) & 1], ((t - 1) >> 1) & 1)) { ok = false; break; }
         pv_seen = t;
       }
       __syncwarp();
