@@ -295,7 +295,7 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   specv::attn_workspace_carve(a->workspace, p.B * p.Hkv, p.rows, p.D, &p);
   CUtensorMap tmK, tmV;
   if (bf16) {
-    const int box = specv::attn_tile_keys(p.rows, a->D);
+    const int box = specv::window_tile_keys(p.rows, a->D, bf16);
     if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box) ||
         !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box))
       return SPEC_ERR_CUDA;

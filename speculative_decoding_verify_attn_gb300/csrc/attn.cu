@@ -479,6 +479,308 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   consumer_loop<D, MASK, NKS>(p, stages, sQ, sML, full, empty, warp, lane, row0, rows_here, &s_abort);
 }
 
+// ------------------------------------------------------------------ draft window kernel
+// The draft's single-query attention over its ring, for up to 16 query rows per kv head (the GQA
+// group): one small CTA per (sequence, kv head) segment, so every segment of the batch is resident
+// at once (several CTAs per SM) and no segment waits for another's latency.  One producer warp
+// streams the ring through a 3-stage TMA ring of 64-key K and V tiles; four consumer warps take
+// 16 keys of each tile (mma.sync m16n8k16, the group's rows padded to 16) with an fp32 online
+// softmax, then combine their partials through shared memory (the stage buffers, free by then),
+// add the new key (the current token, whose slot is masked in the ring) and write the output and
+// the ring slot.
+constexpr int kWinKeys = 64;
+constexpr int kWinStages = 3;
+constexpr int kWinWarps = 4;
+
+size_t window_smem_bytes(int D) { return 1024 + (size_t)kWinStages * 2 * kWinKeys * D * 2 + 16 * (size_t)D * 2; }
+
+template <int D>
+__global__ void __launch_bounds__((kWinWarps + 1) * 32)
+    attn_window_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ AttnParams p) {
+  constexpr int KT = kWinKeys;
+  constexpr int TILE = KT * D * 2;   // bytes of one K (or V) tile
+  constexpr int KSTEPS = D / 16;
+  constexpr int DT = D / 8;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kWinStages], empty[kWinStages];
+  __shared__ float2 sML[kWinWarps][16];
+  __shared__ int s_abort;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* stages = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* sQ = stages + kWinStages * 2 * TILE;  // 16 rows x D bf16, 128-byte swizzle
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x, b = seg / p.Hkv, g = seg % p.Hkv;
+  const int len = seg_len(p, b);               // valid ring slots (0: bad pos)
+  const int ntiles = (len + KT - 1) / KT;
+  const int skip = (p.has_new && len > 0) ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWinStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kWinWarps);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kWinWarps) {
+    // ---------------- producer: every tile of the segment through the ring
+    if (lane == 0 && !p.debug_no_loads) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kWinStages;
+        if (!mbar_wait_bounded(&empty[s], ((t / kWinStages) & 1) ^ 1u, &s_abort)) {
+          s_abort = 1;
+          atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+          for (int i = 1; i <= min(t, kWinStages); ++i) {  // copies still in flight
+            const int tt = t - i;
+            mbar_wait_bounded(&full[tt % kWinStages], (tt / kWinStages) & 1, nullptr);
+          }
+          break;
+        }
+        uint8_t* sK = stages + s * 2 * TILE;
+        mbar_arrive_expect_tx(&full[s], 2u * TILE);
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_4d(sK + h * (KT * 128), &tmK, &full[s], h * 64, t * KT, g, b);
+          tma_load_4d(sK + TILE + h * (KT * 128), &tmV, &full[s], h * 64, t * KT, g, b);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers: the group's rows (padded to 16) into shared memory
+  const int rows = p.rows;  // query rows of the segment (the GQA group)
+  const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  for (int idx = threadIdx.x; idx < 16 * (D / 8); idx += kWinWarps * 32) {
+    const int r = idx / (D / 8), c = idx % (D / 8);
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) val = *reinterpret_cast<const uint4*>(qbase + b * p.q_sb + (int64_t)(g * p.G + r) * p.q_sh + c * 8);
+    *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((c ^ (r & 7)) << 4)) = val;
+  }
+  // the new key (the current token) and its score for the rows this warp finalises (rows warp,
+  // warp + 4, ...), loaded and computed while the first tiles are in flight
+  constexpr int EPL = D / 32;
+  constexpr int RPW = 16 / kWinWarps;
+  const bool add_new = p.has_new && len > 0;
+  float knv[EPL], vnv[EPL], s_new[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) s_new[i] = neg_inf();
+  if (add_new) {
+    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + b * p.new_sb + g * p.new_sh;
+    const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + b * p.new_sb + g * p.new_sh;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      knv[e] = __bfloat162float(kn[lane * EPL + e]);
+      vnv[e] = __bfloat162float(vn[lane * EPL + e]);
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int rr = warp + i * kWinWarps;
+      if (rr < rows) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          dot = fmaf(__bfloat162float(qbase[b * p.q_sb + (int64_t)(g * p.G + rr) * p.q_sh + lane * EPL + e]), knv[e], dot);
+        s_new[i] = warp_sum(dot) * p.scale_log2;
+      }
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWinWarps * 32) : "memory");
+  float o[DT][4];
+#pragma unroll
+  for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+  float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
+  bool bad = false;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % kWinStages;
+    if (!mbar_wait_bounded(&full[s], (t / kWinStages) & 1, &s_abort)) {
+      s_abort = 1;
+      if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+      bad = true;
+      break;
+    }
+    const uint8_t* sK = stages + s * 2 * TILE;
+    const uint8_t* sV = sK + TILE;
+    const int key0 = t * KT;
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; kk += 2) {
+      uint32_t qa[4], qb[4];
+      {
+        const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int c0 = kk * 2 + (lane >> 4);
+        ldmatrix_x4(smem_u32(sQ + r * (D * 2) + ((c0 ^ (r & 7)) << 4)), qa[0], qa[1], qa[2], qa[3]);
+        const int c1 = c0 + 2;
+        ldmatrix_x4(smem_u32(sQ + r * (D * 2) + ((c1 ^ (r & 7)) << 4)), qb[0], qb[1], qb[2], qb[3]);
+      }
+      const int d0 = kk * 16 + (lane >> 3) * 8;
+      const int c = (d0 & 63) >> 3;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int r = warp * 16 + nt * 8 + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(smem_u32(sK + (d0 >> 6) * (KT * 128) + r * 128 + ((c ^ (r & 7)) << 4)), b0, b1, b2, b3);
+        mma_bf16_16816(sc[nt], qa, b0, b1);
+        mma_bf16_16816(sc[nt], qb, b2, b3);
+      }
+    }
+    // visible: slots below len, except the one the current token is about to take
+    const bool edge = key0 + KT > len || (unsigned)(skip - key0) < (unsigned)KT;
+    float mx_lo = neg_inf(), mx_hi = neg_inf();
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = sc[nt][e] * p.scale_log2;
+        if (edge) {
+          const int kk = key0 + warp * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
+          if (kk >= len || kk == skip) x = neg_inf();
+        }
+        sc[nt][e] = x;
+      }
+      mx_lo = fmaxf(mx_lo, fmaxf(sc[nt][0], sc[nt][1]));
+      mx_hi = fmaxf(mx_hi, fmaxf(sc[nt][2], sc[nt][3]));
+    }
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float mu_lo = mn_lo == neg_inf() ? 0.f : mn_lo, mu_hi = mn_hi == neg_inf() ? 0.f : mn_hi;
+    const float a_lo = exp2f(m_lo - mu_lo), a_hi = exp2f(m_hi - mu_hi);
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      sc[nt][0] = exp2f(sc[nt][0] - mu_lo);
+      sc[nt][1] = exp2f(sc[nt][1] - mu_lo);
+      sc[nt][2] = exp2f(sc[nt][2] - mu_hi);
+      sc[nt][3] = exp2f(sc[nt][3] - mu_hi);
+      sum_lo += sc[nt][0] + sc[nt][1];
+      sum_hi += sc[nt][2] + sc[nt][3];
+    }
+    l_lo = l_lo * a_lo + sum_lo;
+    l_hi = l_hi * a_hi + sum_hi;
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+      o[dt][0] *= a_lo; o[dt][1] *= a_lo;
+      o[dt][2] *= a_hi; o[dt][3] *= a_hi;
+    }
+    uint32_t a[4];
+    a[0] = pack_bf16(sc[0][0], sc[0][1]);
+    a[1] = pack_bf16(sc[0][2], sc[0][3]);
+    a[2] = pack_bf16(sc[1][0], sc[1][1]);
+    a[3] = pack_bf16(sc[1][2], sc[1][3]);
+    const int r = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int kf = key0 + warp * 16 + 2 * (lane & 3);  // keys of this thread's B-fragment halves
+#pragma unroll
+    for (int dn = 0; dn < DT; dn += 2) {
+      const int d0 = (dn + (lane >> 4)) * 8;
+      const int c = (d0 & 63) >> 3;
+      uint32_t v0, v1, v2, v3;
+      ldmatrix_x4_trans(smem_u32(sV + (d0 >> 6) * (KT * 128) + r * 128 + ((c ^ (r & 7)) << 4)), v0, v1, v2, v3);
+      if (edge) {  // V rows of hidden slots may hold anything (NaN): zeroed
+        auto okk = [&](int k) { return k < len && k != skip; };
+        const uint32_t m0 = (okk(kf) ? 0x0000ffffu : 0u) | (okk(kf + 1) ? 0xffff0000u : 0u);
+        const uint32_t m1 = (okk(kf + 8) ? 0x0000ffffu : 0u) | (okk(kf + 9) ? 0xffff0000u : 0u);
+        v0 &= m0; v1 &= m1; v2 &= m0; v3 &= m1;
+      }
+      mma_bf16_16816(o[dn], a, v0, v1);
+      mma_bf16_16816(o[dn + 1], a, v2, v3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  // ---------------- combine the four warps' key slices (their o columns through the stage
+  // buffers, free once every warp is past the last tile), add the new key, normalise, write
+  const int q = lane >> 2, tq = lane & 3;
+  if (tq == 0) {
+    sML[warp][q] = make_float2(m_lo, l_lo);
+    sML[warp][q + 8] = make_float2(m_hi, l_hi);
+  }
+  const int stop = [&] {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\tselp.b32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((int)(bad || s_abort)), "n"(kWinWarps * 32)
+        : "memory");
+    return r;
+  }();
+  if (stop) return;
+  float* scratch = reinterpret_cast<float*>(stages);  // [warp][16 rows][D] fp32
+#pragma unroll
+  for (int dt = 0; dt < DT; ++dt) {
+    const int col = dt * 8 + 2 * tq;
+    *reinterpret_cast<float2*>(scratch + (warp * 16 + q) * D + col) = make_float2(o[dt][0], o[dt][1]);
+    *reinterpret_cast<float2*>(scratch + (warp * 16 + q + 8) * D + col) = make_float2(o[dt][2], o[dt][3]);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWinWarps * 32) : "memory");
+  // warp w finalises rows w, w + 4, ... of the group; lane l owns columns l * D/32 ..
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const int rr = warp + i * kWinWarps;
+    if (rr >= rows) break;
+    float M = s_new[i];
+#pragma unroll
+    for (int w = 0; w < kWinWarps; ++w) M = fmaxf(M, sML[w][rr].x);
+    float L = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    if (M != neg_inf()) {
+#pragma unroll
+      for (int w = 0; w < kWinWarps; ++w) {
+        const float2 ml = sML[w][rr];
+        const float wk = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
+        L = fmaf(wk, ml.y, L);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, scratch[(w * 16 + rr) * D + lane * EPL + e], acc[e]);
+      }
+      if (add_new) {
+        const float wn = exp2f(s_new[i] - M);
+        L += wn;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wn, vnv[e], acc[e]);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t off = (int64_t)b * p.o_sb + (int64_t)(g * p.G + rr) * p.o_sh + lane * EPL;
+    if (p.o_bf16) {
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(p.o) + off;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) ob[e] = __float2bfloat16_rn(acc[e] * inv);
+    } else {
+      float* of = reinterpret_cast<float*>(p.o) + off;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) of[e] = acc[e] * inv;
+    }
+    if (add_new && rr == 0) {
+      // every read of the ring in this segment is done: the current token's K/V into its slot
+      const int64_t dst = (int64_t)b * p.kv_sb + (int64_t)g * p.kv_sh + (int64_t)skip * D + lane * EPL;
+      __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.k)) + dst;
+      __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.v)) + dst;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        kr[e] = __float2bfloat16_rn(knv[e]);  // exact: the values came from bf16
+        vr[e] = __float2bfloat16_rn(vnv[e]);
+      }
+    }
+  }
+  if (len == 0 && warp == 0 && lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
+}
+
 // ------------------------------------------------------------------ fp32 partial kernel
 template <int D, int MASK>
 __global__ void __launch_bounds__(128) attn_partial_f32(const __grid_constant__ AttnParams p) {
@@ -816,6 +1118,23 @@ static cudaError_t launch_partial(const AttnParams& p, const CUtensorMap* tmK, c
 
 int attn_tile_keys(int rows, int D) { return (D == 128 && rows > 128) ? kPairTileKeys : kKeyTile; }
 
+bool window_uses_small_kernel(int rows, int D, int kv_bf16) { return kv_bf16 && rows <= 16 && (D == 64 || D == 128); }
+
+int window_tile_keys(int rows, int D, int kv_bf16) {
+  return window_uses_small_kernel(rows, D, kv_bf16) ? kWinKeys : attn_tile_keys(rows, D);
+}
+
+template <int D>
+static cudaError_t launch_window_small(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                       cudaStream_t stream) {
+  const size_t smem = window_smem_bytes(D);
+  auto kern = attn_window_bf16<D>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<p.B * p.Hkv, (kWinWarps + 1) * 32, smem, stream>>>(*tmK, *tmV, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
                              cudaStream_t stream) {
   AttnParams p = p_in;
@@ -835,6 +1154,10 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   dim3 mgrid(p.B * p.Hkv, (p.rows + 3) / 4);
+  if (p.is_window && window_uses_small_kernel(p.rows, p.D, kv_bf16)) {
+    // the draft window with up to 16 rows per kv head: one small CTA per segment
+    return p.D == 64 ? launch_window_small<64>(p, tmK, tmV, stream) : launch_window_small<128>(p, tmK, tmV, stream);
+  }
   if (kv_bf16 && p.D == 128 && p.rows > 32) {
     // dense query blocks: tcgen05 tiles of 128 rows, one CTA per SM (range x row group)
     if (p.has_new) {

@@ -87,9 +87,12 @@ constexpr int kPairTileKeys = 64;
 cudaError_t launch_partial_tc_pair(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
                                    cudaStream_t stream);
 size_t attn_tc_pair_smem_bytes();
-// merge of the pair kernel's records (column-major o blocks)
-cudaError_t launch_merge_pair(const AttnParams& p, cudaStream_t stream);
 // Keys per TMA box the bf16 tensor maps of a launch need (rows = query rows per kv head).
 int attn_tile_keys(int rows, int D);
+// merge of the pair kernel's records (column-major o blocks)
+cudaError_t launch_merge_pair(const AttnParams& p, cudaStream_t stream);
+// The same for the draft window: 64-key boxes where the small per-segment window kernel runs.
+int window_tile_keys(int rows, int D, int kv_bf16);
+bool window_uses_small_kernel(int rows, int D, int kv_bf16);
 
 }  // namespace specv
