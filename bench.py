@@ -598,7 +598,9 @@ def time_lmhead(runner, K, device, plant=0.6):
     LM-head recipe of the input generator (hidden N(0, 1), weight N(0, 1/d), a fraction `plant`
     of the drafts made their row's argmax) but are drawn on the device from a seeded torch
     generator, the 1 GB weight being too slow to draw on the host.  CUDA graph replays; the weight
-    is larger than L2 and L2 is also flushed before each replay."""
+    is larger than L2 and L2 is also flushed before each replay.  The record's "stochastic" part
+    times the stochastic mode of the same call (SPEC_SAMPLE_CHAIN / SPEC_SAMPLE_TREE: logits
+    written to the workspace, sampled in the same call) beside cuBLAS + spec_sample."""
     import torch
     sv, cfg = runner.sv, runner.cfg
     tree = bool(cfg.tree_nodes)
@@ -683,6 +685,46 @@ def time_lmhead(runner, K, device, plant=0.6):
     rows = B * R
     nbytes = V * d * 2 + rows * d * 2 + 2 * rows * ((V + 127) // 128) * 8 + B * (R + cols + 1) * 4
     peak, _ = peaks()
+
+    # the stochastic mode of the same call: the GEMM writes the fp32 logits into the workspace
+    # (L2-sized at these shapes) and spec_sample's kernels read them back within the call; draft
+    # logits N(0, 4) fp32 and uniforms drawn on the device
+    smode = sv.SPEC_SAMPLE_TREE if tree else sv.SPEC_SAMPLE_CHAIN
+    nd = R if tree else R - 1
+    dl = 2.0 * torch.randn((B, nd, V), generator=g, device=device)
+    uni = torch.rand((B, R), generator=g, device=device)
+    out_s, nacc_s = torch.empty_like(out), torch.empty_like(nacc)
+    nodes_s = torch.empty_like(out) if tree else None
+    ws_s = torch.empty(sv.spec_lmhead_sample_workspace(smode, h, w), dtype=torch.uint8, device=device)
+    out_su, nacc_su = torch.empty_like(out), torch.empty_like(nacc)
+    nodes_su = torch.empty_like(out) if tree else None
+    ws_su = torch.empty(sv.spec_sample_workspace(smode, torch.empty((B, R, V), device="meta"), parent),
+                        dtype=torch.uint8, device=device)
+
+    def fused_s():
+        sv.spec_lmhead_sample(smode, h, w, out_s, nacc_s, draft_tokens=tok_d, tree_parent=parent,
+                              out_path_nodes=nodes_s, workspace=ws_s, stream=stream, draft_logits=dl, uniforms=uni)
+
+    def unfused_s():
+        if fp32_out:
+            logits = torch.mm(h2, w.t(), out_dtype=torch.float32).view(B, R, V)
+        else:
+            logits = torch.matmul(h2, w.t()).float().view(B, R, V)
+        sv.spec_sample(smode, logits, out_su, nacc_su, draft_logits=dl, draft_tokens=tok_d, uniforms=uni,
+                       tree_parent=parent, out_path_nodes=nodes_su, workspace=ws_su, stream=stream)
+
+    us_s = timed(fused_s)
+    us_su = timed(unfused_s)
+    # HBM bytes of the stochastic call: the weight once, the hidden rows, the draft logits and
+    # uniforms (the target logits stay in L2 between the GEMM and the sampler)
+    nbytes_s = V * d * 2 + rows * d * 2 + B * nd * V * 4 + B * R * 4 + B * (R + cols + 1) * 4
+    stochastic = {"us": us_s, "gbs": nbytes_s / (us_s * 1e-6) / 1e9,
+                  "hbm_frac": nbytes_s / (us_s * 1e-6) / 1e9 / peak, "algorithmic_bytes": int(nbytes_s),
+                  "mode": "tree" if tree else "chain", "mean_accepted": float(nacc_s.float().mean().item()),
+                  "unfused_us": us_su,
+                  "unfused": ("cuBLAS bf16 GEMM with fp32 output -> spec_sample" if fp32_out
+                              else "cuBLAS bf16 GEMM (bf16 output) -> fp32 copy -> spec_sample"),
+                  "logits_bytes": rows * V * 4}
     return {"us": us, "gbs": nbytes / (us * 1e-6) / 1e9, "hbm_frac": nbytes / (us * 1e-6) / 1e9 / peak,
             "algorithmic_bytes": int(nbytes), "rows": rows, "hidden": d, "vocab": V,
             "mode": "tree_greedy" if tree else "chain_greedy",
@@ -690,7 +732,8 @@ def time_lmhead(runner, K, device, plant=0.6):
             "unfused_us": us_u,
             "unfused": ("cuBLAS bf16 GEMM with fp32 output -> spec_sample greedy" if fp32_out
                         else "cuBLAS bf16 GEMM (bf16 output) -> fp32 copy -> spec_sample greedy"),
-            "unfused_same_tokens": agree}
+            "unfused_same_tokens": agree,
+            "stochastic": stochastic}
 
 
 def time_e2e(runner, K, W, device):

@@ -296,28 +296,39 @@ size_t spec_sample_workspace(const spec_sample_args* args);
 int spec_sample(const spec_sample_args* args, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
- * spec_lmhead_sample -- the LM-head projection fused with greedy verification
+ * spec_lmhead_sample -- the LM-head projection fused with verification
  *
  * The verified rows' logits are the target's final hidden states times the LM-head (unembedding)
  * matrix ("Speculative Decoding in LLM Serving Systems", The algorithm: one target pass gives a
- * next-token distribution per drafted position; "Guide to MagicDec", Implementation Step 3).  In
- * the greedy modes only each row's argmax is used, so this call never writes the logits: a GEMM
- * reduces its fp32 accumulators straight to one running (max, argmax) key per row, and the rule of
+ * next-token distribution per drafted position; "Guide to MagicDec", Implementation Step 3).
+ * Greedy modes only need each row's argmax, so they never write the logits: a tcgen05 GEMM reduces
+ * its fp32 accumulators straight to one running (max, argmax) key per row, and the rule of
  *   SPEC_SAMPLE_CHAIN_GREEDY (n = gamma: rows 0..gamma, draft_tokens [B, gamma]) or
  *   SPEC_SAMPLE_TREE_GREEDY  (n = N nodes: rows 0..N-1, node tokens [B, N], tree_parent HOST [N])
- * is applied to the argmaxes exactly as spec_sample does (ties to the smallest token id).
- * The stochastic modes are not offered: their residual draw needs a whole normalised target row
- * that is only known after every row's statistics, i.e. a second pass over the weights.
+ * is applied to the argmaxes exactly as spec_sample does (ties to the smaller token id).
+ * Stochastic modes need whole normalised rows (the residual draw), so the same GEMM writes the fp32
+ * target logits [B, R, V] -- into out_logits if given, else into the workspace, where at these
+ * sizes (20 MB for 40 rows of a 128K vocabulary) they are read back from L2 -- and the
+ * speculative-sampling kernels of spec_sample then run on them in the same call:
+ *   SPEC_SAMPLE_CHAIN (n = gamma >= 1: rows 0..gamma, draft_logits [B, gamma, V], uniforms
+ *                      [B, gamma + 1]) and
+ *   SPEC_SAMPLE_TREE  (n = N nodes: draft_logits [B, N, V], uniforms [B, N], tree_parent HOST [N]),
+ * with exactly the rules, outputs and numerics of spec_sample in that mode.
  *
  * Layout: hidden bf16 [B, R, d] contiguous (R = gamma + 1 or N), weight bf16 [V, d] contiguous,
  *   both 16-byte aligned; draft_tokens int32 with batch stride tok_stride_b; out_tokens /
- *   out_path_nodes [B, out_cols], out_num_accepted [B] as for spec_sample.
- * Limits: d a multiple of 64 (up to 65 536); 1 <= V <= 2^24; B * R <= 256; tree: N <= 64,
- *   out_cols >= max depth + 1; chain: 0 <= gamma <= 32, out_cols >= gamma + 1.
- * Floating point: bf16 products accumulated in fp32 on the tensor cores; the argmax compares those
- *   fp32 values (an exact tie goes to the smaller id; two logits within the fp32 rounding of a
- *   d-term sum of each other may come out in either order).
- * Workspace: 256 bytes (status word) + B * R * 8 bytes (one running (max, argmax) key per row).
+ *   out_path_nodes [B, out_cols], out_num_accepted [B] as for spec_sample.  Stochastic modes:
+ *   draft_logits fp32 with batch stride dl_stride_b (rows of V contiguous), uniforms fp32 with
+ *   batch stride u_stride_b, out_logits (optional) fp32 [B, R, V] contiguous, all 16-byte aligned.
+ * Limits: d a multiple of 64 (up to 65 536); 1 <= V <= 2^24 (stochastic: V % 4 == 0 and
+ *   V <= 2^20); B * R <= 256; tree: N <= 64, out_cols >= max depth + 1; chain: 0 <= gamma <= 32
+ *   (stochastic: >= 1), out_cols >= gamma + 1.
+ * Floating point: bf16 products accumulated in fp32 on the tensor cores; greedy argmaxes compare
+ *   those fp32 values (an exact tie goes to the smaller id; two logits within the fp32 rounding of
+ *   a d-term sum of each other may come out in either order); stochastic modes sample from those
+ *   fp32 logits as spec_sample does.
+ * Workspace: spec_lmhead_sample_workspace() bytes (the status word at byte 0, the row keys or the
+ *   logits and the sampling workspace), 256-byte aligned.
  * ---------------------------------------------------------------------------------------- */
 typedef struct spec_lmhead_args {
   int32_t mode, B, n, d, V;
@@ -326,12 +337,18 @@ typedef struct spec_lmhead_args {
   const void* weight;          /* bf16 [V, d], device */
   const int32_t* draft_tokens; /* device */
   int64_t tok_stride_b;
-  const int32_t* tree_parent;  /* HOST [N] (tree mode) */
+  const int32_t* tree_parent;  /* HOST [N] (tree modes) */
   int32_t* out_tokens;
   int32_t* out_num_accepted;
-  int32_t* out_path_nodes;     /* tree mode, optional */
+  int32_t* out_path_nodes;     /* tree modes, optional */
   void* workspace;
   size_t workspace_bytes;
+  /* stochastic modes only (NULL / 0 in greedy modes) */
+  const float* draft_logits;   /* device [B, gamma | N, V] */
+  int64_t dl_stride_b;
+  const float* uniforms;       /* device [B, gamma + 1 | N] */
+  int64_t u_stride_b;
+  float* out_logits;           /* device [B, R, V], optional: the projected target logits */
 } spec_lmhead_args;
 
 size_t spec_lmhead_sample_workspace(const spec_lmhead_args* args);

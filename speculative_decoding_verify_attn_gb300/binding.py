@@ -106,6 +106,9 @@ class SpecLmheadArgs(Structure):
         ("tree_parent", c_void_p),
         ("out_tokens", c_void_p), ("out_num_accepted", c_void_p), ("out_path_nodes", c_void_p),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("draft_logits", c_void_p), ("dl_stride_b", c_int64),
+        ("uniforms", c_void_p), ("u_stride_b", c_int64),
+        ("out_logits", c_void_p),
     ]
 
 
@@ -381,10 +384,10 @@ def spec_sample(mode, target_logits, out_tokens, out_num_accepted, *, draft_logi
 
 
 def lmhead_args(mode, hidden, weight, out_tokens, out_num_accepted, *, draft_tokens=None, tree_parent=None,
-                out_path_nodes=None, workspace=None):
+                out_path_nodes=None, workspace=None, draft_logits=None, uniforms=None, out_logits=None):
     B, rows, d = hidden.shape
     V = weight.shape[0]
-    n = rows if mode == SPEC_SAMPLE_TREE_GREEDY else rows - 1
+    n = rows if mode in (SPEC_SAMPLE_TREE_GREEDY, SPEC_SAMPLE_TREE) else rows - 1
     if not hidden.is_contiguous() or not weight.is_contiguous():
         raise ValueError("hidden [B, R, d] and weight [V, d] must be contiguous")
     if weight.shape[1] != d:
@@ -397,33 +400,42 @@ def lmhead_args(mode, hidden, weight, out_tokens, out_num_accepted, *, draft_tok
         tree_parent=parent_ptr,
         out_tokens=_ptr(out_tokens), out_num_accepted=_ptr(out_num_accepted), out_path_nodes=_ptr(out_path_nodes),
         workspace=_ptr(workspace), workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+        draft_logits=_ptr(draft_logits), dl_stride_b=0 if draft_logits is None else draft_logits.stride(0),
+        uniforms=_ptr(uniforms), u_stride_b=0 if uniforms is None else uniforms.stride(0),
+        out_logits=_ptr(out_logits),
     )
     return a, parent_arr
 
 
-def spec_lmhead_sample_workspace(mode, hidden, weight) -> int:
+def spec_lmhead_sample_workspace(mode, hidden, weight, out_logits=None) -> int:
     B, rows, d = hidden.shape
-    n = rows if mode == SPEC_SAMPLE_TREE_GREEDY else rows - 1
-    a = SpecLmheadArgs(mode=mode, B=B, n=n, d=d, V=weight.shape[0])
+    n = rows if mode in (SPEC_SAMPLE_TREE_GREEDY, SPEC_SAMPLE_TREE) else rows - 1
+    a = SpecLmheadArgs(mode=mode, B=B, n=n, d=d, V=weight.shape[0], out_logits=_ptr(out_logits))
     return lib().spec_lmhead_sample_workspace(byref(a))
 
 
 def spec_lmhead_sample(mode, hidden, weight, out_tokens, out_num_accepted, *, draft_tokens=None, tree_parent=None,
-                       out_path_nodes=None, workspace=None, stream=None):
-    """The LM-head projection fused with greedy verification: each row's logits hidden @ weight^T
-    reduced to its argmax on the GPU, then the greedy chain (SPEC_SAMPLE_CHAIN_GREEDY) or tree
-    (SPEC_SAMPLE_TREE_GREEDY) rule.
+                       out_path_nodes=None, workspace=None, stream=None, draft_logits=None, uniforms=None,
+                       out_logits=None):
+    """The LM-head projection fused with verification.  Greedy modes (SPEC_SAMPLE_CHAIN_GREEDY,
+    SPEC_SAMPLE_TREE_GREEDY): each row's logits hidden @ weight^T reduced to its argmax on the GPU,
+    then the greedy rule.  Stochastic modes (SPEC_SAMPLE_CHAIN, SPEC_SAMPLE_TREE): the GEMM writes
+    the fp32 logits (into out_logits if given, else the workspace) and spec_sample's kernels run on
+    them in the same call.
 
     hidden [B, gamma+1 | N, d] bf16; weight [V, d] bf16; draft_tokens [B, gamma] or node tokens
     [B, N] int32; tree_parent host [N] (tree); out_tokens [B, out_cols] int32;
-    out_num_accepted [B] int32."""
-    _check_cuda(hidden, weight, draft_tokens, out_tokens, out_num_accepted, out_path_nodes)
-    need = spec_lmhead_sample_workspace(mode, hidden, weight)
+    out_num_accepted [B] int32; stochastic: draft_logits [B, gamma | N, V] fp32, uniforms
+    [B, gamma+1 | N] fp32, out_logits [B, gamma+1 | N, V] fp32 (optional)."""
+    _check_cuda(hidden, weight, draft_tokens, out_tokens, out_num_accepted, out_path_nodes, draft_logits, uniforms,
+                out_logits)
+    need = spec_lmhead_sample_workspace(mode, hidden, weight, out_logits)
     if need == 0:
         raise SpecError(SPEC_ERR_INVALID_ARG, "spec_lmhead_sample_workspace")
     ws = _workspace(need, hidden.device, workspace)
     a, keep = lmhead_args(mode, hidden, weight, out_tokens, out_num_accepted, draft_tokens=draft_tokens,
-                          tree_parent=tree_parent, out_path_nodes=out_path_nodes, workspace=ws)
+                          tree_parent=tree_parent, out_path_nodes=out_path_nodes, workspace=ws,
+                          draft_logits=draft_logits, uniforms=uniforms, out_logits=out_logits)
     st = lib().spec_lmhead_sample(byref(a), _stream_handle(stream))
     del keep
     if st != SPEC_OK:

@@ -150,7 +150,7 @@ float resolve_scale(float scale, int D) { return scale != 0.f ? scale : 1.0f / s
 
 extern "C" {
 
-int spec_abi_version(void) { return 5; }
+int spec_abi_version(void) { return 6; }
 
 size_t spec_abi_struct_size(int which) {
   switch (which) {
@@ -385,19 +385,42 @@ int spec_sample(const spec_sample_args* a, spec_stream_t stream) {
 
 
 // ------------------------------------------------------------------ spec_lmhead_sample
+static bool lmhead_stochastic(int mode) { return mode == SPEC_SAMPLE_CHAIN || mode == SPEC_SAMPLE_TREE; }
+
 static int lmhead_rows(const spec_lmhead_args* a, int* R) {
-  if (a->mode == SPEC_SAMPLE_CHAIN_GREEDY) {
-    if (a->n < 0 || a->n > specv::kMaxGamma) return SPEC_ERR_UNSUPPORTED;
+  if (a->mode == SPEC_SAMPLE_CHAIN_GREEDY || a->mode == SPEC_SAMPLE_CHAIN) {
+    const int lo = a->mode == SPEC_SAMPLE_CHAIN ? 1 : 0;
+    if (a->n < lo || a->n > specv::kMaxGamma) return SPEC_ERR_UNSUPPORTED;
     *R = a->n + 1;
     return SPEC_OK;
   }
-  if (a->mode == SPEC_SAMPLE_TREE_GREEDY) {
+  if (a->mode == SPEC_SAMPLE_TREE_GREEDY || a->mode == SPEC_SAMPLE_TREE) {
     if (a->n < 1 || a->n > specv::kLmMaxNodes) return SPEC_ERR_UNSUPPORTED;
     *R = a->n;
     return SPEC_OK;
   }
-  if (a->mode == SPEC_SAMPLE_CHAIN || a->mode == SPEC_SAMPLE_TREE) return SPEC_ERR_UNSUPPORTED;
   return SPEC_ERR_INVALID_ARG;
+}
+
+// Workspace of the fused LM-head: the status word and the row keys; in stochastic modes then the
+// logits (unless the caller takes them in out_logits) and the sampling kernels' workspace.
+struct LmWs {
+  size_t keys, logits, sample, total;
+};
+static bool lmhead_ws(const spec_lmhead_args* a, int R, LmWs* w) {
+  const int nrows = a->B * R;
+  w->keys = specv::lmhead_workspace_bytes(nrows);
+  w->logits = 0;
+  w->sample = 0;
+  if (lmhead_stochastic(a->mode)) {
+    w->keys = (w->keys + 255) / 256 * 256;
+    if (a->V > (1 << 20) || (a->V % 4) != 0) return false;
+    if (!a->out_logits) w->logits = ((size_t)nrows * a->V * sizeof(float) + 255) / 256 * 256;
+    // target rows R, draft rows n (chain: gamma, tree: N)
+    w->sample = specv::sample_workspace_bytes(a->mode, a->B, R, a->n, a->V);
+  }
+  w->total = w->keys + w->logits + w->sample;
+  return true;
 }
 
 size_t spec_lmhead_sample_workspace(const spec_lmhead_args* a) {
@@ -405,7 +428,9 @@ size_t spec_lmhead_sample_workspace(const spec_lmhead_args* a) {
   int R;
   if (lmhead_rows(a, &R) != SPEC_OK) return 0;
   if (a->B < 1 || a->V < 1 || a->V > (1 << 24) || (int64_t)a->B * R > specv::kLmMaxRows) return 0;
-  return specv::lmhead_workspace_bytes(a->B * R);
+  LmWs w;
+  if (!lmhead_ws(a, R, &w)) return 0;
+  return w.total;
 }
 
 int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
@@ -417,19 +442,33 @@ int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
   if (a->V > (1 << 24) || (int64_t)a->B * R > specv::kLmMaxRows) return SPEC_ERR_UNSUPPORTED;
   if (!a->hidden || !a->weight || !aligned(a->hidden, 16) || !aligned(a->weight, 16)) return SPEC_ERR_INVALID_ARG;
   if (!a->out_tokens || !a->out_num_accepted) return SPEC_ERR_INVALID_ARG;
-  const bool tree = a->mode == SPEC_SAMPLE_TREE_GREEDY;
+  const bool stochastic = lmhead_stochastic(a->mode);
+  const bool tree = a->mode == SPEC_SAMPLE_TREE_GREEDY || a->mode == SPEC_SAMPLE_TREE;
   if ((tree || a->n > 0) && (!a->draft_tokens || a->tok_stride_b < 0)) return SPEC_ERR_INVALID_ARG;
+  if (stochastic) {
+    if (a->V > (1 << 20) || (a->V % 4) != 0) return SPEC_ERR_UNSUPPORTED;
+    if (!a->draft_logits || !aligned(a->draft_logits, 16) || a->dl_stride_b < 0 || (a->dl_stride_b % 4))
+      return SPEC_ERR_INVALID_ARG;
+    if (!a->uniforms || a->u_stride_b < 0) return SPEC_ERR_INVALID_ARG;
+    if (a->out_logits && !aligned(a->out_logits, 16)) return SPEC_ERR_INVALID_ARG;
+  }
   specv::LmheadParams p;
   memset(&p, 0, sizeof(p));
+  SampleParams sp;
+  memset(&sp, 0, sizeof(sp));
+  int maxd = 0;
   if (tree) {
-    const int maxd = build_tree(a->tree_parent, a->n, nullptr, p.parent, p.depth);
+    maxd = build_tree(a->tree_parent, a->n, nullptr, p.parent, p.depth);
     if (maxd < 0) return SPEC_ERR_INVALID_ARG;
     if (a->out_cols < maxd + 1) return SPEC_ERR_INVALID_ARG;
+    memcpy(sp.parent, p.parent, sizeof(sp.parent));
+    memcpy(sp.depth, p.depth, sizeof(sp.depth));
   } else if (a->out_cols < a->n + 1) {
     return SPEC_ERR_INVALID_ARG;
   }
-  const size_t need = spec_lmhead_sample_workspace(a);
-  if ((st = check_workspace(a->workspace, a->workspace_bytes, need)) != SPEC_OK) return st;
+  LmWs w;
+  if (!lmhead_ws(a, R, &w)) return SPEC_ERR_UNSUPPORTED;
+  if ((st = check_workspace(a->workspace, a->workspace_bytes, w.total)) != SPEC_OK) return st;
   const int sms = num_sms();
   if (sms <= 0) return SPEC_ERR_CUDA;
   p.mode = a->mode; p.B = a->B; p.R = R; p.d = a->d; p.V = a->V;
@@ -445,7 +484,35 @@ int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
   CUtensorMap tmW, tmH;
   if (!encode_2d_map(&tmW, a->weight, a->d, a->V, 128) || !encode_2d_map(&tmH, a->hidden, a->d, p.nrows, p.npad))
     return SPEC_ERR_CUDA;
-  cudaError_t e = specv::launch_lmhead(p, &tmW, &tmH, sms, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!stochastic) {
+    cudaError_t e = specv::launch_lmhead(p, &tmW, &tmH, sms, cs);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  // stochastic: the GEMM writes the target logits, then the kernels of spec_sample in that mode;
+  // both flag into the one status word at byte 0, cleared once here
+  uint8_t* base = reinterpret_cast<uint8_t*>(a->workspace);
+  p.logits = a->out_logits ? a->out_logits : reinterpret_cast<float*>(base + w.keys);
+  cudaError_t e = cudaMemsetAsync(p.status, 0, 256, cs);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  e = specv::launch_lmhead_logits(p, &tmW, &tmH, sms, cs);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  sp.mode = a->mode; sp.B = a->B; sp.V = a->V;
+  sp.gamma = tree ? 0 : a->n;
+  sp.rows_t = R;
+  sp.rows_d = a->n;
+  sp.N = tree ? a->n : 0;
+  sp.tl = p.logits; sp.tl_sb = (int64_t)R * a->V;
+  sp.dl = a->draft_logits; sp.dl_sb = a->dl_stride_b;
+  sp.tok = a->draft_tokens; sp.tok_sb = a->tok_stride_b;
+  sp.u = a->uniforms; sp.u_sb = a->u_stride_b;
+  sp.out_cols = a->out_cols; sp.out_tok = a->out_tokens; sp.out_nacc = a->out_num_accepted;
+  sp.out_nodes = a->out_path_nodes;
+  // the sampling workspace follows; its kernels report into the call's status word
+  specv::sample_workspace_carve(base + w.keys + w.logits, &sp);
+  sp.status = p.status;
+  sp.status_zeroed = 1;
+  e = specv::launch_sample(sp, sms, cs);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

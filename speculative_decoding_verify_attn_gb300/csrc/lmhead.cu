@@ -1,9 +1,10 @@
-// The LM-head projection fused with greedy verification (spec_lmhead_sample): the verified rows'
-// logits are the target's final hidden states times the LM-head matrix ("Speculative Decoding in
-// LLM Serving Systems", The algorithm; "Guide to MagicDec", Implementation Step 3), and the greedy
-// rules only need each row's argmax, so the logits never leave the SM: a tcgen05 GEMM reduces its
+// The LM-head projection fused with verification (spec_lmhead_sample): the verified rows' logits
+// are the target's final hidden states times the LM-head matrix ("Speculative Decoding in LLM
+// Serving Systems", The algorithm; "Guide to MagicDec", Implementation Step 3).  The greedy rules
+// only need each row's argmax, so there the logits never leave the SM: a tcgen05 GEMM reduces its
 // accumulators straight to one 64-bit (value, id) key per hidden row, and a small kernel reads the
-// keys and applies the chain or tree rule.
+// keys and applies the chain or tree rule.  The stochastic rules need whole normalised rows: the
+// same GEMM then stores its accumulators as fp32 logits, and the sampling kernels follow.
 //
 // GEMM (D[v, n] = sum_k W[v, k] H[n, k]): the vocabulary is M (128 rows of W per tile, K-major,
 // 128-byte swizzle), the B*R hidden rows are N (padded to a multiple of 16, at most 256).  A CTA
@@ -165,9 +166,13 @@ __device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt,
   }
 }
 
+// STORE: write the fp32 logits [nrows][V] instead of reducing them to argmax keys (stochastic
+// modes); for a fixed hidden row a warp's 32 lanes hold 32 consecutive vocabulary rows, so each
+// column of a TMEM load is one 128-byte store.
+template <bool STORE>
 __global__ void __launch_bounds__(kLmThreads, 1)
-    lmhead_argmax(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-                  const __grid_constant__ LmheadParams p) {
+    lmhead_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                const __grid_constant__ LmheadParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t wfull[kLmWStagesMax], wempty[kLmWStagesMax], hfull[kLmHStagesMax], hempty[kLmHStagesMax];
   __shared__ uint64_t acc_full, acc_empty, drain;
@@ -332,31 +337,56 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       tc::fence_after();
       const uint32_t vm0 = (uint32_t)((W.tile0 + ps * W.tpp) * 128 + sub * 32 + lane);  // tile 0's vocabulary id
       const uint32_t tb = tmem + ((uint32_t)(sub * 32) << 16);
+      if constexpr (STORE) {
+        for (int t = 0; t < nt; ++t) {
+          const uint32_t vm = vm0 + 128u * (uint32_t)t;
+          for (int cc = 0; cc * 32 < p.npad; ++cc) {
+            uint32_t u[32];
+            if (cc * 32 + 32 <= p.npad) {
+              tc::ld32(tb + (uint32_t)(t * p.npad + cc * 32), u);
+              tc::ld_wait(u);
+            } else {
+              lm_ld16(tb + (uint32_t)(t * p.npad + cc * 32), *reinterpret_cast<uint32_t(*)[16]>(u));
+            }
+            const int nc = min(32, p.npad - cc * 32);
+            if (vm < (uint32_t)p.V) {
+              for (int e = 0; e < nc; ++e) {
+                const int n = cc * 32 + e;
+                if (n < p.nrows) p.logits[(int64_t)n * p.V + vm] = __uint_as_float(u[e]);
+              }
+            }
+          }
+        }
+      } else {
 #pragma unroll
-      for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
-        if (cc * 32 >= p.npad) break;
-        uint32_t bo = 0, bi = 0xffffffffu;
-        if (cc * 32 + 32 <= p.npad)
-          lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
-        else
-          lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
-        const unsigned long long key = bi < (uint32_t)p.V ? (((unsigned long long)bo << 32) | (uint32_t)~bi) : 0ull;
-        kbest[cc] = key > kbest[cc] ? key : kbest[cc];
+        for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
+          if (cc * 32 >= p.npad) break;
+          uint32_t bo = 0, bi = 0xffffffffu;
+          if (cc * 32 + 32 <= p.npad)
+            lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
+          else
+            lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
+          const unsigned long long key =
+              bi < (uint32_t)p.V ? (((unsigned long long)bo << 32) | (uint32_t)~bi) : 0ull;
+          kbest[cc] = key > kbest[cc] ? key : kbest[cc];
+        }
       }
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty);
     }
-    // the four warps' keys into the CTA's, then one global atomic per row
+    if constexpr (!STORE) {
+      // the four warps' keys into the CTA's, then one global atomic per row
 #pragma unroll
-    for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
-      const int row = cc * 32 + lane;
-      if (row < p.nrows && kbest[cc] != 0ull) atomicMax(&s_key[row], kbest[cc]);
+      for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
+        const int row = cc * 32 + lane;
+        if (row < p.nrows && kbest[cc] != 0ull) atomicMax(&s_key[row], kbest[cc]);
+      }
+      lm_epi_sync();
+      unsigned long long* keys = reinterpret_cast<unsigned long long*>(p.rec);
+      for (int r = threadIdx.x - 64; r < p.nrows; r += 128)
+        if (s_key[r] != 0ull) atomicMax(&keys[r], s_key[r]);
     }
-    lm_epi_sync();
-    unsigned long long* keys = reinterpret_cast<unsigned long long*>(p.rec);
-    for (int r = threadIdx.x - 64; r < p.nrows; r += 128)
-      if (s_key[r] != 0ull) atomicMax(&keys[r], s_key[r]);
   }
   tc::fence_before();
   __syncthreads();
@@ -438,12 +468,25 @@ cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const C
   lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
   if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup) return cudaErrorInvalidValue;
   // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
-  e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_argmax), kLmSmemCap - 2560);
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<false>), kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
   const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
-  lmhead_argmax<<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  lmhead_gemm<false><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_dependent(lmhead_finalize, dim3(p.B), dim3(256), 0, stream, 0u, p);
+}
+
+cudaError_t launch_lmhead_logits(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
+                                 cudaStream_t stream) {
+  int ws, hs, kg;
+  size_t smem;
+  lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
+  if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup || !p.logits) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<true>), kLmSmemCap - 2560);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
+  lmhead_gemm<true><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  return cudaGetLastError();
 }
 
 }  // namespace specv

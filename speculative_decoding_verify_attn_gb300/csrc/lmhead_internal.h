@@ -12,7 +12,7 @@ constexpr int kLmMaxRows = 256;     // B * R hidden rows per call (N of one MMA)
 constexpr int kLmMaxNodes = 64;
 
 struct LmheadParams {
-  int mode;               // SPEC_SAMPLE_CHAIN_GREEDY or SPEC_SAMPLE_TREE_GREEDY
+  int mode;               // SPEC_SAMPLE_* (greedy: argmax keys; stochastic: logits)
   int B, R, d, V;         // R rows per sequence (gamma + 1 or N)
   int nrows, npad;        // B * R, padded to a multiple of 16
   int n_vtiles;           // ceil(V / 128)
@@ -27,6 +27,7 @@ struct LmheadParams {
   int32_t* out_nodes;
   uint32_t* status;
   void* rec;              // [nrows] 64-bit (value, id) keys of the running row maxima
+  float* logits;          // stochastic modes: [nrows][V] fp32 target logits written by the GEMM
   int8_t parent[kLmMaxNodes];
   int8_t depth[kLmMaxNodes];
 };
@@ -36,5 +37,8 @@ size_t lmhead_workspace_bytes(int nrows);
 void lmhead_workspace_carve(void* ws, LmheadParams* p);
 cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
                           cudaStream_t stream);
+// Stochastic modes: the GEMM alone, writing p.logits (the sampling kernels follow).
+cudaError_t launch_lmhead_logits(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
+                                 cudaStream_t stream);
 
 }  // namespace specv

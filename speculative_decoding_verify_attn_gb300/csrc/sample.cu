@@ -951,7 +951,7 @@ void sample_workspace_carve(void* ws, SampleParams* p) {
 
 static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const int rows = p.rows_t + p.rows_d;
-  cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
+  cudaError_t e = p.status_zeroed ? cudaSuccess : cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   const long long items = (long long)p.schunks * rows * p.B;
   // persistent statistics grid: one CTA per SM (its shared-memory rings fill the SM)
@@ -999,7 +999,7 @@ static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
 cudaError_t launch_sample(SampleParams& p, int num_sms, cudaStream_t stream) {
   if (p.mode == SPEC_SAMPLE_TREE) return launch_sample_tree(p, stream);
   if (p.V <= kSmallVocab) {
-    cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
+    cudaError_t e = p.status_zeroed ? cudaSuccess : cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
     const int per_block = kSampleThreads / 32;
     sample_small<<<(p.B + per_block - 1) / per_block, kSampleThreads, 0, stream>>>(p);

@@ -35,6 +35,7 @@ struct SampleParams {
   int num_sms;
   // workspace
   uint32_t* status;
+  int status_zeroed;  // the caller has already cleared *status for this call (no reset here)
   float* st_m;      // [B][rows_t + rows_d][schunks] item maxima
   float2* st_s;     // [B][rows][schunks] sum of exp(x - item max) as a float-float (hi, lo) pair
   int32_t* st_arg;  // [B][rows][schunks] item argmax (greedy)

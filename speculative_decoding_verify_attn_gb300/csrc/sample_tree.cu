@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sample_tree_stochastic(const 
 }
 
 cudaError_t launch_sample_tree(const SampleParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
+  cudaError_t e = p.status_zeroed ? cudaSuccess : cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

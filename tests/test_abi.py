@@ -46,7 +46,7 @@ def test_struct_layouts_match(L):
     assert L.spec_abi_struct_size(3) == ctypes.sizeof(b.SpecCommitArgs)
     assert L.spec_abi_struct_size(4) == ctypes.sizeof(b.SpecLmheadArgs)
     assert L.spec_abi_struct_size(5) == 0
-    assert L.spec_abi_version() == 5
+    assert L.spec_abi_version() == 6
     assert L.spec_status_string(-3).decode().startswith("workspace")
 
 
@@ -207,9 +207,25 @@ def test_lmhead_host_validation(L):
     ws = L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args()))
     assert ws == 256 + 8 * 5 * 8                          # status + one 64-bit key per hidden row
     assert call(lmhead_args(mode=7)) == -1
-    assert call(lmhead_args(mode=0)) == -2                 # stochastic chain: not fused
-    assert call(lmhead_args(mode=3, n=6)) == -2            # stochastic tree: not fused
-    assert L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(mode=0))) == 0
+    # stochastic modes: the logits (unless the caller takes them) and the sampling workspace follow
+    sto = dict(mode=0, draft_logits=FAKE, dl_stride_b=4 * 128256, uniforms=FAKE, u_stride_b=5)
+    ws0 = L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(**sto)))
+    logits = 8 * 5 * 128256 * 4
+    ws0_own = L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(**sto, out_logits=FAKE)))
+    assert ws0 - ws0_own == logits and ws0_own > 768
+    assert call(lmhead_args(**dict(sto, draft_logits=None))) == -1
+    assert call(lmhead_args(**dict(sto, draft_logits=FAKE + 4))) == -1     # 16-byte aligned
+    assert call(lmhead_args(**dict(sto, dl_stride_b=4 * 128256 + 2))) == -1
+    assert call(lmhead_args(**dict(sto, uniforms=None))) == -1
+    assert call(lmhead_args(**sto, out_logits=FAKE + 8)) == -1
+    assert call(lmhead_args(**dict(sto, n=0), out_cols=1)) == -2           # a stochastic chain drafts
+    assert call(lmhead_args(**dict(sto, V=1001))) == -2                    # V % 4
+    assert call(lmhead_args(**dict(sto, V=(1 << 20) + 4))) == -2
+    assert L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(**dict(sto, V=1001)))) == 0
+    assert call(lmhead_args(**sto, workspace_bytes=ws0 - 1)) == -3
+    ptree = np.array([-1, 0, 0, 1, 1, 2], dtype=np.int32)
+    assert L.spec_lmhead_sample_workspace(ctypes.byref(lmhead_args(**dict(sto, mode=3, n=6)))) > 8 * 6 * 128256 * 4
+    assert call(lmhead_args(**dict(sto, mode=3, n=6, tree_parent=ptree.ctypes.data), out_cols=2)) == -1
     assert call(lmhead_args(n=33)) == -2
     assert call(lmhead_args(B=52, n=4)) == -2              # 260 hidden rows > 256
     assert call(lmhead_args(d=4000)) == -1                 # d a multiple of 64

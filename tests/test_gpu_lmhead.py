@@ -1,10 +1,15 @@
-"""GPU parity: spec_lmhead_sample -- the LM-head projection fused with greedy chain / tree
-verification -- against the oracle.
+"""GPU parity: spec_lmhead_sample -- the LM-head projection fused with greedy or stochastic chain /
+tree verification -- against the oracle.
 
 The GPU accumulates bf16 products in fp32; the oracle takes the exact float64 dot products.  Token
 decisions are compared exactly on every sequence none of whose consulted rows the oracle marks as
 near-tied (top two logits within the fp32 accumulation bound of a d-term dot product of each
-other); the near-tied ones are only checked for validity."""
+other); the near-tied ones are only checked for validity.
+
+The stochastic modes run on exact-grid inputs (``workloads.gen.lmhead_grid_inputs``): every fp32
+partial sum of those dot products is exact, so the GPU's logits must equal the oracle's bit for
+bit, and the sampled outcomes are then held to spec_sample's own bar (exact wherever no decision
+lies within 1e-6 of its threshold, valid elsewhere)."""
 
 import numpy as np
 import pytest
@@ -211,12 +216,120 @@ def test_bad_token_flagged(sv):
     del torch
 
 
-def test_stochastic_modes_refused(sv):
+def _stochastic(sv, mode, inp, parent=None, take_logits=True):
+    """One stochastic fused call on the grid inputs; returns the outputs, the status word and the
+    logits the GEMM wrote (None unless taken through out_logits)."""
     torch = torch_mod()
-    h = torch.zeros((1, 3, 64), dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros((100, 64), dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros((1, 3), dtype=torch.int32, device="cuda")
-    nacc = torch.zeros((1,), dtype=torch.int32, device="cuda")
-    with pytest.raises(sv.SpecError):
-        sv.spec_lmhead_sample(sv.SPEC_SAMPLE_CHAIN, h, w, out, nacc,
-                              draft_tokens=torch.zeros((1, 2), dtype=torch.int32, device="cuda"))
+    B, R, _ = inp["hidden"].shape
+    V = inp["weight"].shape[0]
+    tree = parent is not None
+    cols = int(osm.tree_depths(parent).max()) + 1 if tree else R
+    h, w = to_dev(inp["hidden"], "bf16"), to_dev(inp["weight"], "bf16")
+    out = torch.full((B, cols), -7, dtype=torch.int32, device="cuda")
+    nodes = torch.full((B, cols), -7, dtype=torch.int32, device="cuda")
+    nacc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    lg = torch.full((B, R, V), float("nan"), dtype=torch.float32, device="cuda") if take_logits else None
+    need = sv.spec_lmhead_sample_workspace(mode, h, w, lg)
+    ws = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")   # stale bytes: the call clears what it needs
+    sv.spec_lmhead_sample(mode, h, w, out, nacc, draft_tokens=to_dev(inp["tokens"], "i32"), tree_parent=parent,
+                          out_path_nodes=nodes if tree else None, workspace=ws,
+                          draft_logits=to_dev(inp["draft_logits"]), uniforms=to_dev(inp["uniforms"]), out_logits=lg)
+    torch.cuda.synchronize()
+    return to_np(out), to_np(nodes), to_np(nacc), sv.read_status(ws), None if lg is None else to_np(lg)
+
+
+def _stochastic_chain(sv, inp, min_ok, take_logits=True):
+    """Grid inputs make every fp32 logit exact, so the GPU's logits equal the oracle's float64 ones
+    bit for bit and the sampling decisions must agree wherever the oracle marks none near."""
+    out, _, nacc, st, lg = _stochastic(sv, sv.SPEC_SAMPLE_CHAIN, inp, take_logits=take_logits)
+    ref = ol.lmhead_logits(inp["hidden"], inp["weight"])
+    if lg is not None:
+        assert np.array_equal(lg.astype(np.float64), ref)
+    t = ref.astype(np.float32)
+    r_out, r_k, near = osm.spec_sample_chain(t, inp["draft_logits"], inp["tokens"], inp["uniforms"])
+    ok = ~near
+    assert st == 0
+    assert ok.sum() >= min_ok
+    assert np.array_equal(nacc[ok], r_k[ok]) and np.array_equal(out[ok], r_out[ok])
+    if near.any():
+        assert osm.chain_outcome_valid(t[near], inp["draft_logits"][near], inp["tokens"][near],
+                                       inp["uniforms"][near], out[near], nacc[near]).all()
+    return r_k
+
+
+def _stochastic_tree(sv, inp, parent, min_ok, take_logits=True):
+    out, nodes, nacc, st, lg = _stochastic(sv, sv.SPEC_SAMPLE_TREE, inp, parent, take_logits=take_logits)
+    ref = ol.lmhead_logits(inp["hidden"], inp["weight"])
+    if lg is not None:
+        assert np.array_equal(lg.astype(np.float64), ref)
+    cols = out.shape[1]
+    r_out, r_nodes, r_k, near = osm.tree_stochastic(ref.astype(np.float32), inp["draft_logits"], inp["tokens"],
+                                                    parent, inp["uniforms"], cols)
+    ok = ~near
+    assert st == 0
+    assert ok.sum() >= min_ok
+    assert np.array_equal(nacc[ok], r_k[ok])
+    assert np.array_equal(out[ok], r_out[ok]) and np.array_equal(nodes[ok], r_nodes[ok])
+    for b in np.nonzero(near)[0]:       # near: the path must still be a parent chain of drafts
+        k = int(nacc[b])
+        assert 0 <= k < cols
+        prev = 0
+        for j in range(k):
+            n = int(nodes[b, j])
+            assert parent[n] == prev and out[b, j] == inp["tokens"][b, n]
+            prev = n
+    return r_k
+
+
+def test_stochastic_chain_llama3_8b_lm_head(sv):
+    """LLaMA-3-8B's LM head (d 4096, V 128 256), batch 8, gamma 4, on exact-grid inputs: the
+    projected logits match bit for bit and the sampled outcome matches the oracle's."""
+    cfg = CONFIGS["llama3-8b-layer"]
+    inp = gen.lmhead_grid_inputs(cfg.B, cfg.gamma + 1, 4096, cfg.vocab, cfg.seed)
+    k = _stochastic_chain(sv, inp, cfg.B - 1)
+    assert k.max() >= 1
+
+
+@pytest.mark.parametrize("B,gamma,d,V,take", [(50, 4, 256, 3000, True), (40, 5, 128, 1004, False),
+                                              (7, 32, 64, 2048, True), (3, 1, 192, 2052, False)])
+def test_stochastic_chain_shapes(sv, B, gamma, d, V, take):
+    """Both sampling paths (V <= 2048: one warp per sequence; above: the statistics pass), a
+    ragged last vocabulary tile, the longest chain, logits kept in the workspace or handed out."""
+    inp = gen.lmhead_grid_inputs(B, gamma + 1, d, V, 320 + gamma)
+    k = _stochastic_chain(sv, inp, B - 2, take_logits=take)
+    if B >= 40:
+        assert k.min() == 0 and k.max() >= 2
+
+
+def test_stochastic_tree_medusa_lm_head(sv):
+    """Vicuna-7B-sized LM head (d 4096, V 32 000) over the Medusa tree (64 nodes), batch 4: the
+    256-row accumulator, logits bit for bit, the tree walk against the oracle."""
+    cfg = CONFIGS["medusa-tree-8k"]
+    parent = gen.random_tree(cfg.tree_nodes, cfg.tree_max_depth, cfg.tree_max_children, cfg.seed)
+    inp = gen.lmhead_grid_inputs(cfg.B, len(parent), 4096, cfg.vocab, cfg.seed, parent=parent)
+    _stochastic_tree(sv, inp, parent, cfg.B - 1)
+
+
+@pytest.mark.parametrize("N,B,d,V,take", [(20, 12, 128, 1004, True), (9, 25, 64, 4100, False), (1, 3, 64, 96, True)])
+def test_stochastic_tree_shapes(sv, N, B, d, V, take):
+    parent = gen.random_tree(N, 4, 3, 330 + N) if N > 1 else np.array([-1], dtype=np.int32)
+    inp = gen.lmhead_grid_inputs(B, N, d, V, 331 + N, parent=parent)
+    k = _stochastic_tree(sv, inp, parent, B - 2, take_logits=take)
+    if N > 1:
+        assert k.max() >= 1
+
+
+def test_stochastic_bad_token_flagged(sv):
+    """A draft token outside [0, V) in one sequence: that sequence reports -1, the others match."""
+    inp = gen.lmhead_grid_inputs(4, 4, 64, 500, 340)
+    inp["tokens"][2, 1] = 500
+    out, _, nacc, st, lg = _stochastic(sv, sv.SPEC_SAMPLE_CHAIN, inp)
+    assert st == sv.SPEC_STATUS_BAD_TOKEN
+    assert nacc[2] == -1 and np.all(out[2] == -1)
+    keep = [0, 1, 3]
+    ref = ol.lmhead_logits(inp["hidden"], inp["weight"]).astype(np.float32)
+    r_out, r_k, near = osm.spec_sample_chain(ref[keep], inp["draft_logits"][keep], inp["tokens"][keep],
+                                             inp["uniforms"][keep])
+    for i, b in enumerate(keep):
+        if not near[i]:
+            assert nacc[b] == r_k[i] and list(out[b]) == list(r_out[i])

@@ -73,3 +73,33 @@ def test_near_band_grows_with_the_hidden_size():
         w[0, 0], w[1, 0] = 1.0, 1.0 - 1e-3        # logits 1 and 0.999, sum |terms| = 1.999
         lg = ol.lmhead_logits(h, w)
         assert bool(ol.near_rows(h, w, lg)[0, 0]) is expect
+
+
+def test_grid_inputs_give_order_free_fp32_logits():
+    """The exact-grid inputs of the stochastic LM-head tests: any summation order of the fp32
+    products gives the same logits as the float64 product, so a GPU kernel's fp32 logits must
+    equal the oracle's bit for bit.  Checked here with two unrelated orders (a float32 matmul and
+    a reversed running float32 sum) for the largest and smallest hidden sizes used."""
+    for d, V in ((4096, 64), (64, 96)):
+        inp = gen.lmhead_grid_inputs(2, 3, d, V, 41)
+        ref = ol.lmhead_logits(inp["hidden"], inp["weight"])
+        mm = (inp["hidden"] @ inp["weight"].T).astype(np.float64)
+        assert np.array_equal(mm, ref)
+        h, w = inp["hidden"][1, 2], inp["weight"][V - 1]
+        acc = np.float32(0)
+        for k in range(d - 1, -1, -1):
+            acc = np.float32(acc + h[k] * w[k])
+        assert float(acc) == ref[1, 2, V - 1]
+        assert 1.0 < ref.std() < 3.0
+        assert np.all(gen.round_bf16(inp["hidden"]) == inp["hidden"])
+        assert np.all(gen.round_bf16(inp["weight"]) == inp["weight"])
+
+
+def test_grid_inputs_planted_drafts_have_mass_in_both_models():
+    """The planted draft tokens of the grid inputs sit where both softmaxes put real mass, so the
+    accept test is exercised both ways (the chain is then a non-trivial sample of the rule)."""
+    inp = gen.lmhead_grid_inputs(40, 5, 256, 3000, 7)
+    lg = ol.lmhead_logits(inp["hidden"], inp["weight"])
+    _, k, _ = osm.spec_sample_chain(lg.astype(np.float32), inp["draft_logits"], inp["tokens"], inp["uniforms"])
+    counts = np.bincount(k, minlength=5)
+    assert counts[0] > 0 and counts[4] > 0 and counts[1:4].sum() > 0

@@ -270,3 +270,79 @@ def lmhead_inputs(B: int, R: int, d: int, V: int, seed: int, dtype: str = "bf16"
                 w[t] = h[b, src] * np.float32(3.0 / np.sqrt(d))
                 tok[b, dst] = t
     return dict(hidden=h, weight=store(w, dtype), tokens=tok)
+
+
+def lmhead_grid_inputs(B: int, R: int, d: int, V: int, seed: int, parent=None, plant: float = 0.85,
+                       draft_sigma: float = 2.0) -> dict:
+    """Inputs of the stochastic fused LM-head on an exact grid: every stored value is a small
+    integer times a power of two, hidden = h_int * 2^-2 and weight = w_int * 2^-(s-2) with
+    |h_int|, |w_int| <= 4 and s = floor(log2(4 sqrt(d))), so a logit is an integer times 2^-s of
+    magnitude at most 16 d * 2^-s: every partial sum of a d-term dot product is exact in fp32
+    (16 d < 2^24 for d <= 65 536), in any order.  The logits then spread about N(0, 1.7^2 .. 2.4^2).
+
+    With probability ``plant`` the token of each chain row i + 1 (tree: each node's first child)
+    is planted: a fresh vocabulary id whose weight row is +-4 on a random subset of coordinates
+    (the signs of the source hidden row there, zero elsewhere) sized for a target logit near
+    ln(V) + sigma_t^2 / 2 +- 2 (sigma_t the logits' spread), and whose draft logit in the source
+    row is set near ln(V) + draft_sigma^2 / 2 +- 2, so that both distributions put real mass on
+    it and the accept ratio spreads around 1.  Other draft
+    tokens are drawn from their draft row by Gumbel-max.  Draft logits ~ N(0, draft_sigma^2)
+    fp32.  Returns hidden [B, R, d], weight [V, d] (float32 holding bf16-exact values),
+    draft_logits [B, R - 1 | R, V], tokens [B, R - 1 | R] (draft tokens; tree: node tokens with
+    node 0's arbitrary), uniforms [B, R] (uniforms in [0, 1), fp32)."""
+    s = int(np.floor(np.log2(4.0 * np.sqrt(d))))
+    hi = rng_for(seed, "q").integers(-4, 5, size=(B, R, d), dtype=np.int8)
+    wi = rng_for(seed, "k").integers(-4, 5, size=(V, d), dtype=np.int8)
+    tree = parent is not None
+    nd = R if tree else R - 1
+    dl = (draft_sigma * rng_for(seed, "draft").standard_normal((B, nd, V), dtype=np.float32)).astype(np.float32)
+    pr = rng_for(seed, "tree_tok")
+    if tree:
+        first = {}
+        for c in range(1, R):
+            first.setdefault(int(parent[c]), c)
+        pairs = sorted((p_, c) for p_, c in first.items())
+    else:
+        pairs = [(i, i + 1) for i in range(R - 1)]
+    planted = {}
+    used = set()
+    # ln V + sigma^2 / 2 is about the log of the softmax denominator of V N(0, sigma^2) logits
+    sigma_t = (20.0 / 3.0) * np.sqrt(d) * 2.0 ** -s
+    base_t, base_d = np.log(V) + sigma_t ** 2 / 2, np.log(V) + draft_sigma ** 2 / 2
+    for b in range(B):
+        for src, dst in pairs:
+            if pr.random() >= plant:
+                continue
+            t = int(pr.integers(V))
+            if t in used:
+                continue
+            used.add(t)
+            # E|h_int| = 20/9: m coordinates at +-4 give a logit of about m * 4 * 20/9 * 2^-s
+            want = base_t + pr.uniform(-2.0, 2.0)
+            m = int(min(d, max(1, round(want * 2.0 ** s / (4.0 * 20.0 / 9.0)))))
+            idx = pr.choice(d, size=m, replace=False)
+            row = np.zeros(d, dtype=np.int8)
+            row[idx] = 4 * np.sign(hi[b, src, idx]).astype(np.int8)
+            wi[t] = row
+            dl[b, src, t] = np.float32(base_d + pr.uniform(-2.0, 2.0))
+            planted[(b, dst)] = t
+    r = rng_for(seed, "gumbel")
+    tok = np.zeros((B, nd), dtype=np.int32)
+    for b in range(B):
+        for j in range(nd):
+            node = j if tree else j + 1          # the row whose token this is
+            if tree and node == 0:
+                tok[b, 0] = int(r.integers(V))
+                continue
+            src = int(parent[node]) if tree else node - 1
+            if (b, node) in planted:
+                tok[b, j] = planted[(b, node)]
+            else:
+                tok[b, j] = int(gumbel_max_draw(dl[b, src][None], r)[0])
+    h = hi.astype(np.float32) * np.float32(0.25)
+    w = np.empty((V, d), dtype=np.float32)
+    step = 8192
+    for v0 in range(0, V, step):
+        w[v0:v0 + step] = wi[v0:v0 + step].astype(np.float32) * np.float32(2.0 ** -(s - 2))
+    u = rng_for(seed, "uniforms").random((B, R), dtype=np.float32)
+    return dict(hidden=h, weight=w, draft_logits=dl, tokens=tok, uniforms=u)
