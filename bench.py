@@ -42,6 +42,26 @@ L2_BYTES = 126 << 20
 SUB_WORKLOADS = ("llama3-70b-layer", "llama3-8b-layer", "medusa-tree-8k", "magicdec-64k")
 
 
+class L2Flush:
+    """Evicts L2 between timed replays: a 512 MB write replaces every line, then a 512 MB read
+    replaces the written lines with clean ones.  Without the read the timed kernel would also pay
+    for writing back the flush's own ~126 MB of dirty lines, a cost no kernel of the round leaves
+    behind (the steps before a verify or sampling call read caches and weights)."""
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(128 << 20, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self, k: int = 1):
+        self.w.fill_(k & 0xFF)
+        self.sink.copy_(self.r.sum())
+
+
+L2_NOTE = "L2 flushed (512 MB write, then a 512 MB read so the lines left are clean) before every"
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -52,6 +72,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling a small case)")
+    ap.add_argument("--context", type=int, default=0,
+                    help="override the verify context length (profiling the draft-window and sampling kernels at "
+                         "full size beside a small verify cache)")
     ap.add_argument("--clocks-csv", default=None, help="write the raw nvidia-smi clock samples of the timed region here")
     ap.add_argument("--no-graphs", action="store_true", help="issue every call eagerly instead of graph replays")
     ap.add_argument("--sinks", type=int, default=0, help="attention-sink slots at the front of the draft ring")
@@ -419,11 +442,11 @@ def time_steps(runner, K, W, pg, device, use_graphs=True, clocks_csv=None):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    # working sets that L2 (~126 MB) could hold between steps are flushed by a 512 MB write
+    # working sets that L2 (~126 MB) could hold between steps are flushed (L2Flush)
     nb = step_bytes(cfg, runner.inp)
     flush = None
     if nb["verify_total"] + nb["sample"] < 4 * L2_BYTES:
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+        flush = L2Flush(device)
     barrier(pg, device)
     torch.cuda.synchronize()
     clocks = ClockSampler(device.index, clocks_csv)
@@ -433,7 +456,7 @@ def time_steps(runner, K, W, pg, device, use_graphs=True, clocks_csv=None):
     for k in range(K):
         e = evs[k]
         if flush is not None:
-            flush.fill_(k & 0xFF)
+            flush(k)
         e[0].record(stream)
         do_draft()
         e[1].record(stream)
@@ -521,7 +544,7 @@ def time_verify_append(runner, K, device):
     def op():
         sv.spec_verify_attn(inp["q"], inp["k"], inp["v"], inp["kv_len"], inp["o"], tree_parent=inp["tree"],
                             workspace=runner.ws_v, stream=stream, k_new=k_new, v_new=v_new)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     with torch.cuda.stream(stream):
         op()
         stream.synchronize()
@@ -532,7 +555,7 @@ def time_verify_append(runner, K, device):
             g.replay()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for e0, e1 in evs:
-            flush.fill_(1)
+            flush(1)
             e0.record(stream)
             g.replay()
             e1.record(stream)
@@ -566,7 +589,7 @@ def time_tree_stochastic(runner, K, device):
     def op():
         sv.spec_sample(sv.SPEC_SAMPLE_TREE, tl, out, nacc, draft_logits=dl, draft_tokens=tok, uniforms=u,
                        tree_parent=parent, out_path_nodes=nodes, workspace=ws, stream=stream)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     with torch.cuda.stream(stream):
         op()
         stream.synchronize()
@@ -577,7 +600,7 @@ def time_tree_stochastic(runner, K, device):
             g.replay()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for e0, e1 in evs:
-            flush.fill_(1)
+            flush(1)
             e0.record(stream)
             g.replay()
             e1.record(stream)
@@ -659,7 +682,7 @@ def time_lmhead(runner, K, device, plant=0.6):
         sv.spec_sample(mode, logits, out_u, nacc_u, draft_tokens=tok_d, tree_parent=parent, out_path_nodes=nodes_u,
                        workspace=ws_u, stream=stream)
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
 
     def timed(op):
         with torch.cuda.stream(stream):
@@ -672,7 +695,7 @@ def time_lmhead(runner, K, device, plant=0.6):
                 gr.replay()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
             for e0, e1 in evs:
-                flush.fill_(1)
+                flush(1)
                 e0.record(stream)
                 gr.replay()
                 e1.record(stream)
@@ -877,7 +900,7 @@ def time_draft_cold(runner, K, device):
     import torch
     cfg, inp = runner.cfg, runner.inp
     stream = torch.cuda.Stream(device=device)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     with torch.cuda.stream(stream):
         runner.draft(0)
         stream.synchronize()
@@ -888,14 +911,14 @@ def time_draft_cold(runner, K, device):
             g.replay()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         for e0, e1 in evs:
-            flush.fill_(1)
+            flush(1)
             e0.record(stream)
             g.replay()
             e1.record(stream)
         stream.synchronize()
     us = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
     nb = step_bytes(cfg, inp)["window"]
-    return {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "bytes": nb, "l2": "flushed (512 MB write) before every call"}
+    return {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "bytes": nb, "l2": L2_NOTE.replace("L2 flushed", "flushed") + " call"}
 
 
 def oracle_check_sampling(cfg, runner):
@@ -972,7 +995,7 @@ def measure(cfg, args, pg, device, rank, world, full):
                             "flops": "4 * sum(kv_len) * Hq * nq * D (dense over the context)",
                             "peak_source": tpeak_kind,
                             "ncu_tensor_pipe_active_pct": counters.get("tensor_pipe_active_pct") if counters else None},
-        "l2": ("L2 flushed (512 MB write) before every timed step; flush time excluded" if t["l2_flush"] else
+        "l2": (L2_NOTE + " timed step; flush time excluded" if t["l2_flush"] else
                f"inputs larger than L2: the {nb['verify_kv'] / 1e9:.2f} GB verify cache streamed each step evicts L2"
                + ("; draft steps 2-4 of a round re-read the ring (may be L2-resident)" if cfg.window else "")),
         "clocks": t["clocks"],
@@ -1010,9 +1033,9 @@ def measure(cfg, args, pg, device, rank, world, full):
 def main():
     args = parse()
     cfg = get_config(args.workload)
-    if args.batch:
+    if args.batch or args.context:
         from workloads.configs import scaled
-        cfg = scaled(cfg, B=args.batch)
+        cfg = scaled(cfg, B=args.batch or None, ctx=(args.context, args.context) if args.context else None)
     if args.impl == "reference":
         return run_reference(args, cfg)
     import torch
@@ -1027,7 +1050,7 @@ def main():
 
     main_rec, x = measure(cfg, args, pg, device, rank, world, full=True)
     subs = {}
-    if not args.no_sub_configs and not args.batch:
+    if not args.no_sub_configs and not args.batch and not args.context:
         for name in SUB_WORKLOADS:
             if name != cfg.name:
                 subs[name], _ = measure(get_config(name), args, pg, device, rank, world, full=False)

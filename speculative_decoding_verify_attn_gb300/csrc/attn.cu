@@ -481,101 +481,113 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
 
 // ------------------------------------------------------------------ draft window kernel
 // The draft's single-query attention over its ring, for up to 16 query rows per kv head (the GQA
-// group): one small CTA per (sequence, kv head) segment, so every segment of the batch is resident
-// at once (several CTAs per SM) and no segment waits for another's latency.  One producer warp
-// streams the ring through a 3-stage TMA ring of 64-key K and V tiles; four consumer warps take
-// 16 keys of each tile (mma.sync m16n8k16, the group's rows padded to 16) with an fp32 online
-// softmax, then combine their partials through shared memory (the stage buffers, free by then),
-// add the new key (the current token, whose slot is masked in the ring) and write the output and
-// the ring slot.
+// group): one CTA per (sequence, kv head) segment, so every segment of the batch is resident at
+// once (two CTAs per SM) and no segment waits for another's latency.  The ring streams through a
+// 3-stage TMA ring of 64-key K and V tiles; the first tiles are issued by thread 0 right after the
+// barriers are set up, before the segment's length is read (every tile lies inside the ring, so
+// the copies are in bounds whatever the length; those past it are only waited for).  Two groups
+// of four warps take alternate tiles, so two tiles are in compute at once; within a group each
+// warp takes 16 keys of its tile (mma.sync m16n8k16, the group's rows padded to 16, Q.K^T as four
+// independent accumulator chains) with an fp32 online softmax.  There is no producer warp (its
+// registers would cost the second CTA per SM): the last of a group's four warps to finish a tile
+// (a shared counter per stage) refills that stage with the tile three ahead.  A stage's tiles
+// alternate between the groups, so each (group, stage) pair has its own full barrier: a group
+// then waits on consecutive phases of it (on a shared barrier it would skip the other group's
+// phases, and a parity wait could pass on an older phase).  The eight partial
+// states are combined through shared memory (the stage buffers, once every copy has landed) with
+// the new key (the current token, whose slot is masked in the ring), and the output and the ring
+// slot are written.
 constexpr int kWinKeys = 64;
 constexpr int kWinStages = 3;
-constexpr int kWinWarps = 4;
+constexpr int kWinGroups = 2;
+constexpr int kWinWarps = 4 * kWinGroups;
+constexpr int kWinThreads = kWinWarps * 32;
 
 size_t window_smem_bytes(int D) { return 1024 + (size_t)kWinStages * 2 * kWinKeys * D * 2 + 16 * (size_t)D * 2; }
 
 template <int D>
-__global__ void __launch_bounds__((kWinWarps + 1) * 32)
+__global__ void __launch_bounds__(kWinThreads, 2)
     attn_window_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const __grid_constant__ AttnParams p) {
   constexpr int KT = kWinKeys;
   constexpr int TILE = KT * D * 2;   // bytes of one K (or V) tile
   constexpr int KSTEPS = D / 16;
   constexpr int DT = D / 8;
+  static_assert((size_t)kWinWarps * 16 * D * 4 <= (size_t)kWinStages * 2 * TILE, "combine scratch fits the stages");
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full[kWinStages], empty[kWinStages];
+  __shared__ uint64_t full[kWinGroups][kWinStages];  // tile t lands on full[t % 2][t % 3], phase t / 6
+  __shared__ int s_done[kWinStages];  // warp-tiles finished in the stage (four per tile, never reset)
+  __shared__ int s_last[kWinStages];  // the last tile copied into the stage (-1: none)
   __shared__ float2 sML[kWinWarps][16];
+  __shared__ float sNewK[D], sNewV[D], sNewS[16];  // the new key and value, its score per row
   __shared__ int s_abort;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* stages = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* sQ = stages + kWinStages * 2 * TILE;  // 16 rows x D bf16, 128-byte swizzle
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x, b = seg / p.Hkv, g = seg % p.Hkv;
-  const int len = seg_len(p, b);               // valid ring slots (0: bad pos)
-  const int ntiles = (len + KT - 1) / KT;
-  const int skip = (p.has_new && len > 0) ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
+  auto issue = [&](int t) {  // one thread: tile t into stage t % kWinStages
+    const int s = t % kWinStages;
+    uint8_t* sK = stages + s * 2 * TILE;
+    uint64_t* bar = &full[t % kWinGroups][s];
+    mbar_arrive_expect_tx(bar, 2u * TILE);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_4d(sK + h * (KT * 128), &tmK, bar, h * 64, t * KT, g, b);
+      tma_load_4d(sK + TILE + h * (KT * 128), &tmV, bar, h * 64, t * KT, g, b);
+    }
+    s_last[s] = t;
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kWinStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kWinWarps);
+      mbar_init(&full[0][i], 1);
+      mbar_init(&full[1][i], 1);
+      s_done[i] = 0;
+      s_last[i] = -1;
     }
     s_abort = 0;
     fence_mbar_init();
+    if (!p.debug_no_loads) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      // the first stages before the length is known: slots [0, W) are all inside the ring
+      const int pre = min(kWinStages, (p.Lmax + KT - 1) / KT);
+      for (int t = 0; t < pre; ++t) issue(t);
+    }
   }
   __syncthreads();
 
-  if (warp == kWinWarps) {
-    // ---------------- producer: every tile of the segment through the ring
-    if (lane == 0 && !p.debug_no_loads) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kWinStages;
-        if (!mbar_wait_bounded(&empty[s], ((t / kWinStages) & 1) ^ 1u, &s_abort)) {
-          s_abort = 1;
-          atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
-          for (int i = 1; i <= min(t, kWinStages); ++i) {  // copies still in flight
-            const int tt = t - i;
-            mbar_wait_bounded(&full[tt % kWinStages], (tt / kWinStages) & 1, nullptr);
-          }
-          break;
-        }
-        uint8_t* sK = stages + s * 2 * TILE;
-        mbar_arrive_expect_tx(&full[s], 2u * TILE);
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_4d(sK + h * (KT * 128), &tmK, &full[s], h * 64, t * KT, g, b);
-          tma_load_4d(sK + TILE + h * (KT * 128), &tmV, &full[s], h * 64, t * KT, g, b);
-        }
-      }
-    }
-    return;
-  }
-
   // ---------------- consumers: the group's rows (padded to 16) into shared memory
+  const int len = seg_len(p, b);               // valid ring slots (0: bad pos)
+  const int ntiles = (len + KT - 1) / KT;
+  const int skip = (p.has_new && len > 0) ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
+  const int grp = warp >> 2, wk = warp & 3;    // tile parity of this warp's group, key slice in the tile
   const int rows = p.rows;  // query rows of the segment (the GQA group)
   const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(p.q);
-  for (int idx = threadIdx.x; idx < 16 * (D / 8); idx += kWinWarps * 32) {
+  for (int idx = threadIdx.x; idx < 16 * (D / 8); idx += kWinThreads) {
     const int r = idx / (D / 8), c = idx % (D / 8);
     uint4 val = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) val = *reinterpret_cast<const uint4*>(qbase + b * p.q_sb + (int64_t)(g * p.G + r) * p.q_sh + c * 8);
     *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((c ^ (r & 7)) << 4)) = val;
   }
   // the new key (the current token) and its score for the rows this warp finalises (rows warp,
-  // warp + 4, ...), loaded and computed while the first tiles are in flight
+  // warp + 8), loaded and computed while the first tiles are in flight, kept in shared memory
+  // (the registers are the loop's)
   constexpr int EPL = D / 32;
   constexpr int RPW = 16 / kWinWarps;
   const bool add_new = p.has_new && len > 0;
-  float knv[EPL], vnv[EPL], s_new[RPW];
-#pragma unroll
-  for (int i = 0; i < RPW; ++i) s_new[i] = neg_inf();
   if (add_new) {
     const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + b * p.new_sb + g * p.new_sh;
     const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + b * p.new_sb + g * p.new_sh;
+    float knv[EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      knv[e] = __bfloat162float(kn[lane * EPL + e]);
-      vnv[e] = __bfloat162float(vn[lane * EPL + e]);
+    for (int e = 0; e < EPL; ++e) knv[e] = __bfloat162float(kn[lane * EPL + e]);
+    if (warp == 0) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        sNewK[lane * EPL + e] = knv[e];
+        sNewV[lane * EPL + e] = __bfloat162float(vn[lane * EPL + e]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < RPW; ++i) {
@@ -585,19 +597,20 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
 #pragma unroll
         for (int e = 0; e < EPL; ++e)
           dot = fmaf(__bfloat162float(qbase[b * p.q_sb + (int64_t)(g * p.G + rr) * p.q_sh + lane * EPL + e]), knv[e], dot);
-        s_new[i] = warp_sum(dot) * p.scale_log2;
+        dot = warp_sum(dot);
+        if (lane == 0) sNewS[rr] = dot * p.scale_log2;
       }
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kWinWarps * 32) : "memory");
+  __syncthreads();
   float o[DT][4];
 #pragma unroll
   for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
   float m_lo = neg_inf(), m_hi = neg_inf(), l_lo = 0.f, l_hi = 0.f;
   bool bad = false;
-  for (int t = 0; t < ntiles; ++t) {
+  for (int t = grp; t < ntiles; t += kWinGroups) {
     const int s = t % kWinStages;
-    if (!mbar_wait_bounded(&full[s], (t / kWinStages) & 1, &s_abort)) {
+    if (!mbar_wait_bounded(&full[grp][s], (t / (kWinGroups * kWinStages)) & 1, &s_abort)) {
       s_abort = 1;
       if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
       bad = true;
@@ -606,11 +619,16 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
     const uint8_t* sK = stages + s * 2 * TILE;
     const uint8_t* sV = sK + TILE;
     const int key0 = t * KT;
-    float sc[2][4];
+    // S = Q.K^T for this warp's 16 keys: two 8-key halves x two K-dimension halves, four
+    // independent accumulator chains
+    float sc4[2][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) sc4[nt][hh][0] = sc4[nt][hh][1] = sc4[nt][hh][2] = sc4[nt][hh][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; kk += 2) {
+      const int hh = kk < KSTEPS / 2 ? 0 : 1;
       uint32_t qa[4], qb[4];
       {
         const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -623,13 +641,18 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
       const int c = (d0 & 63) >> 3;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int r = warp * 16 + nt * 8 + (lane & 7);
+        const int r = wk * 16 + nt * 8 + (lane & 7);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(smem_u32(sK + (d0 >> 6) * (KT * 128) + r * 128 + ((c ^ (r & 7)) << 4)), b0, b1, b2, b3);
-        mma_bf16_16816(sc[nt], qa, b0, b1);
-        mma_bf16_16816(sc[nt], qb, b2, b3);
+        mma_bf16_16816(sc4[nt][hh], qa, b0, b1);
+        mma_bf16_16816(sc4[nt][hh], qb, b2, b3);
       }
     }
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = sc4[nt][0][e] + sc4[nt][1][e];
     // visible: slots below len, except the one the current token is about to take
     const bool edge = key0 + KT > len || (unsigned)(skip - key0) < (unsigned)KT;
     float mx_lo = neg_inf(), mx_hi = neg_inf();
@@ -639,7 +662,7 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
       for (int e = 0; e < 4; ++e) {
         float x = sc[nt][e] * p.scale_log2;
         if (edge) {
-          const int kk = key0 + warp * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
+          const int kk = key0 + wk * 16 + nt * 8 + 2 * (lane & 3) + (e & 1);
           if (kk >= len || kk == skip) x = neg_inf();
         }
         sc[nt][e] = x;
@@ -678,8 +701,8 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
     a[1] = pack_bf16(sc[0][2], sc[0][3]);
     a[2] = pack_bf16(sc[1][0], sc[1][1]);
     a[3] = pack_bf16(sc[1][2], sc[1][3]);
-    const int r = warp * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-    const int kf = key0 + warp * 16 + 2 * (lane & 3);  // keys of this thread's B-fragment halves
+    const int r = wk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+    const int kf = key0 + wk * 16 + 2 * (lane & 3);  // keys of this thread's B-fragment halves
 #pragma unroll
     for (int dn = 0; dn < DT; dn += 2) {
       const int d0 = (dn + (lane >> 4)) * 8;
@@ -695,19 +718,40 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
       mma_bf16_16816(o[dn], a, v0, v1);
       mma_bf16_16816(o[dn + 1], a, v2, v3);
     }
+    // the last of the group's warps to finish the tile refills its stage (its reads of the stage
+    // are done: every ldmatrix result was consumed by an MMA issued above)
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) {
+      __threadfence_block();
+      if ((atomicAdd(&s_done[s], 1) & 3) == 3) {
+        __threadfence_block();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (t + kWinStages < ntiles && !s_abort && !p.debug_no_loads) issue(t + kWinStages);
+      }
+    }
   }
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  // ---------------- combine the four warps' key slices (their o columns through the stage
-  // buffers, free once every warp is past the last tile), add the new key, normalise, write
+  // ---------------- combine the eight warps' partial states (their o columns through the stage
+  // buffers, once every warp is past its last tile and every copy issued has landed: tiles past
+  // the length, or after an abort, were never waited for), add the new key, normalise, write
   const int q = lane >> 2, tq = lane & 3;
   if (tq == 0) {
     sML[warp][q] = make_float2(m_lo, l_lo);
     sML[warp][q + 8] = make_float2(m_hi, l_hi);
+  }
+  __syncthreads();  // no copy is issued after this
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWinStages; ++i) {
+      // the stage's last tile: the one before it in the stage had been consumed when it was issued
+      const int tl = s_last[i];
+      if (tl >= 0 && !mbar_wait_bounded(&full[tl % kWinGroups][i], (tl / (kWinGroups * kWinStages)) & 1, nullptr)) {
+        s_abort = 1;
+        atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+      }
+    }
   }
   const int stop = [&] {
     int r;
@@ -715,7 +759,7 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
         "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
         "bar.red.or.pred q, 1, %2, p;\n\tselp.b32 %0, 1, 0, q;\n\t}\n"
         : "=r"(r)
-        : "r"((int)(bad || s_abort)), "n"(kWinWarps * 32)
+        : "r"((int)(bad || s_abort)), "n"(kWinThreads)
         : "memory");
     return r;
   }();
@@ -727,13 +771,14 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
     *reinterpret_cast<float2*>(scratch + (warp * 16 + q) * D + col) = make_float2(o[dt][0], o[dt][1]);
     *reinterpret_cast<float2*>(scratch + (warp * 16 + q + 8) * D + col) = make_float2(o[dt][2], o[dt][3]);
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kWinWarps * 32) : "memory");
-  // warp w finalises rows w, w + 4, ... of the group; lane l owns columns l * D/32 ..
+  asm volatile("bar.sync 1, %0;" ::"n"(kWinThreads) : "memory");
+  // warp w finalises rows w, w + 8 of the group; lane l owns columns l * D/32 ..
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
     const int rr = warp + i * kWinWarps;
     if (rr >= rows) break;
-    float M = s_new[i];
+    const float s_new = add_new ? sNewS[rr] : neg_inf();
+    float M = s_new;
 #pragma unroll
     for (int w = 0; w < kWinWarps; ++w) M = fmaxf(M, sML[w][rr].x);
     float L = 0.f, acc[EPL];
@@ -743,16 +788,16 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
 #pragma unroll
       for (int w = 0; w < kWinWarps; ++w) {
         const float2 ml = sML[w][rr];
-        const float wk = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
-        L = fmaf(wk, ml.y, L);
+        const float wk2 = ml.x == neg_inf() ? 0.f : exp2f(ml.x - M);
+        L = fmaf(wk2, ml.y, L);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, scratch[(w * 16 + rr) * D + lane * EPL + e], acc[e]);
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk2, scratch[(w * 16 + rr) * D + lane * EPL + e], acc[e]);
       }
       if (add_new) {
-        const float wn = exp2f(s_new[i] - M);
+        const float wn = exp2f(s_new - M);
         L += wn;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wn, vnv[e], acc[e]);
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wn, sNewV[lane * EPL + e], acc[e]);
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -773,8 +818,8 @@ __global__ void __launch_bounds__((kWinWarps + 1) * 32)
       __nv_bfloat16* vr = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.v)) + dst;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        kr[e] = __float2bfloat16_rn(knv[e]);  // exact: the values came from bf16
-        vr[e] = __float2bfloat16_rn(vnv[e]);
+        kr[e] = __float2bfloat16_rn(sNewK[lane * EPL + e]);  // exact: the values came from bf16
+        vr[e] = __float2bfloat16_rn(sNewV[lane * EPL + e]);
       }
     }
   }
@@ -1131,7 +1176,7 @@ static cudaError_t launch_window_small(const AttnParams& p, const CUtensorMap* t
   auto kern = attn_window_bf16<D>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.B * p.Hkv, (kWinWarps + 1) * 32, smem, stream>>>(*tmK, *tmV, p);
+  kern<<<p.B * p.Hkv, kWinThreads, smem, stream>>>(*tmK, *tmV, p);
   return cudaGetLastError();
 }
 

@@ -55,6 +55,28 @@ def test_window_with_append_many_positions(sv, dtype, D, Hq, Hkv):
         assert np.array_equal(vr_np[b][:, other], inp["v_ring"][b][:, other])
 
 
+@pytest.mark.parametrize("W", [64, 512, 1024])
+def test_window_full_batch_ring_sizes(sv, W):
+    """The MagicDec draft shape at its full batch (32 sequences x 8 kv heads = 256 segments, two
+    per SM) for rings of one, eight and sixteen 64-key tiles, with full rings and rings still
+    filling (fewer tiles than the ring holds, so some of the first copies are never consumed)."""
+    Hq, Hkv, D, B = 32, 8, 128, 32
+    pos = np.random.default_rng(W).integers(1, 3 * W, size=B).astype(np.int32)
+    pos[:4] = [1, W - 1, W, 70000]
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, pos, "bf16", seed=60 + W)
+    q, kr, vr = to_dev(inp["q"], "bf16"), to_dev(inp["k_ring"], "bf16"), to_dev(inp["v_ring"], "bf16")
+    kn, vn = to_dev(inp["k_new"], "bf16"), to_dev(inp["v_new"], "bf16")
+    o, st = _run(sv, q, kr, vr, to_dev(pos, "i32"), kn, vn, "bf16")
+    ref, k_after, v_after = oa.draft_window_attn(inp["q"], inp["k_ring"], inp["v_ring"], pos,
+                                                 inp["k_new"], inp["v_new"])
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what=f"window W={W}")
+    kr_np = to_np(kr)
+    for b in range(B):
+        s_ = (pos[b] - 1) % W
+        assert np.array_equal(kr_np[b, :, s_], k_after[b, :, s_].astype(np.float32))
+
+
 def test_magicdec_draft_round_four_steps(sv):
     """Four draft steps of a round, each appending one token, on the MagicDec window shape."""
     cfg = CONFIGS["magicdec-64k"]
