@@ -538,7 +538,41 @@ __global__ void __launch_bounds__(kWinThreads, 2)
     }
     s_last[s] = t;
   };
-  if (threadIdx.x == 0) {
+  // ---------------- every thread: the segment's length, the group's rows (padded to 16) and the
+  // new key.  Every global load is issued before any of them is used, so the prologue costs one
+  // round trip; the last warp's lane 0 sets up the ring meanwhile.
+  constexpr int EPL = D / 32;
+  constexpr int RPW = 16 / kWinWarps;
+  const int grp = warp >> 2, wk = warp & 3;    // tile parity of this warp's group, key slice in the tile
+  const int rows = p.rows;  // query rows of the segment (the GQA group)
+  const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  const int lraw = __ldg(p.lens + b);
+  static_assert(16 * (D / 8) <= kWinThreads, "one 16-byte chunk of Q per thread");
+  const int qr = threadIdx.x / (D / 8), qc = threadIdx.x % (D / 8);
+  uint4 qval = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x < 16 * (D / 8) && qr < rows)
+    qval = *reinterpret_cast<const uint4*>(qbase + b * p.q_sb + (int64_t)(g * p.G + qr) * p.q_sh + qc * 8);
+  // the new key (the current token), its value (warp 0 keeps both), and the rows this warp scores
+  // against it (rows warp, warp + 8)
+  __nv_bfloat16 kraw[EPL], vraw[EPL], qraw[RPW][EPL];
+  if (p.has_new) {
+    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + b * p.new_sb + g * p.new_sh;
+    const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + b * p.new_sb + g * p.new_sh;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kraw[e] = kn[lane * EPL + e];
+      vraw[e] = warp == 0 ? vn[lane * EPL + e] : __float2bfloat16_rn(0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+      const int rr = warp + i * kWinWarps;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        qraw[i][e] = rr < rows ? qbase[b * p.q_sb + (int64_t)(g * p.G + rr) * p.q_sh + lane * EPL + e]
+                               : __float2bfloat16_rn(0.f);
+    }
+  }
+  if (threadIdx.x == kWinThreads - 32) {
     for (int i = 0; i < kWinStages; ++i) {
       mbar_init(&full[0][i], 1);
       mbar_init(&full[1][i], 1);
@@ -555,38 +589,17 @@ __global__ void __launch_bounds__(kWinThreads, 2)
       for (int t = 0; t < pre; ++t) issue(t);
     }
   }
-  __syncthreads();
-
-  // ---------------- consumers: the group's rows (padded to 16) into shared memory
-  const int len = seg_len(p, b);               // valid ring slots (0: bad pos)
+  const int len = lraw >= 1 ? min(lraw, p.Lmax) : 0;  // valid ring slots (0: bad pos)
   const int ntiles = (len + KT - 1) / KT;
-  const int skip = (p.has_new && len > 0) ? window_slot(__ldg(p.lens + b) - 1, p.Lmax, p.n_sinks) : -1;
-  const int grp = warp >> 2, wk = warp & 3;    // tile parity of this warp's group, key slice in the tile
-  const int rows = p.rows;  // query rows of the segment (the GQA group)
-  const __nv_bfloat16* qbase = reinterpret_cast<const __nv_bfloat16*>(p.q);
-  for (int idx = threadIdx.x; idx < 16 * (D / 8); idx += kWinThreads) {
-    const int r = idx / (D / 8), c = idx % (D / 8);
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r < rows) val = *reinterpret_cast<const uint4*>(qbase + b * p.q_sb + (int64_t)(g * p.G + r) * p.q_sh + c * 8);
-    *reinterpret_cast<uint4*>(sQ + r * (D * 2) + ((c ^ (r & 7)) << 4)) = val;
-  }
-  // the new key (the current token) and its score for the rows this warp finalises (rows warp,
-  // warp + 8), loaded and computed while the first tiles are in flight, kept in shared memory
-  // (the registers are the loop's)
-  constexpr int EPL = D / 32;
-  constexpr int RPW = 16 / kWinWarps;
+  const int skip = (p.has_new && len > 0) ? window_slot(lraw - 1, p.Lmax, p.n_sinks) : -1;
+  if (threadIdx.x < 16 * (D / 8)) *reinterpret_cast<uint4*>(sQ + qr * (D * 2) + ((qc ^ (qr & 7)) << 4)) = qval;
   const bool add_new = p.has_new && len > 0;
-  if (add_new) {
-    const __nv_bfloat16* kn = reinterpret_cast<const __nv_bfloat16*>(p.k_new) + b * p.new_sb + g * p.new_sh;
-    const __nv_bfloat16* vn = reinterpret_cast<const __nv_bfloat16*>(p.v_new) + b * p.new_sb + g * p.new_sh;
-    float knv[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) knv[e] = __bfloat162float(kn[lane * EPL + e]);
+  if (p.has_new) {
     if (warp == 0) {
 #pragma unroll
       for (int e = 0; e < EPL; ++e) {
-        sNewK[lane * EPL + e] = knv[e];
-        sNewV[lane * EPL + e] = __bfloat162float(vn[lane * EPL + e]);
+        sNewK[lane * EPL + e] = __bfloat162float(kraw[e]);
+        sNewV[lane * EPL + e] = __bfloat162float(vraw[e]);
       }
     }
 #pragma unroll
@@ -595,14 +608,13 @@ __global__ void __launch_bounds__(kWinThreads, 2)
       if (rr < rows) {
         float dot = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-          dot = fmaf(__bfloat162float(qbase[b * p.q_sb + (int64_t)(g * p.G + rr) * p.q_sh + lane * EPL + e]), knv[e], dot);
+        for (int e = 0; e < EPL; ++e) dot = fmaf(__bfloat162float(qraw[i][e]), __bfloat162float(kraw[e]), dot);
         dot = warp_sum(dot);
         if (lane == 0) sNewS[rr] = dot * p.scale_log2;
       }
     }
   }
-  __syncthreads();
+  __syncthreads();  // barriers initialised, Q and the new key in shared memory
   float o[DT][4];
 #pragma unroll
   for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
@@ -747,7 +759,7 @@ __global__ void __launch_bounds__(kWinThreads, 2)
     for (int i = 0; i < kWinStages; ++i) {
       // the stage's last tile: the one before it in the stage had been consumed when it was issued
       const int tl = s_last[i];
-      if (tl >= 0 && !mbar_wait_bounded(&full[tl % kWinGroups][i], (tl / (kWinGroups * kWinStages)) & 1, nullptr)) {
+      if (tl >= 0 && (tl >= ntiles || s_abort) && !mbar_wait_bounded(&full[tl % kWinGroups][i], (tl / (kWinGroups * kWinStages)) & 1, nullptr)) {
         s_abort = 1;
         atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
       }
@@ -765,11 +777,15 @@ __global__ void __launch_bounds__(kWinThreads, 2)
   }();
   if (stop) return;
   float* scratch = reinterpret_cast<float*>(stages);  // [warp][16 rows][D] fp32
+  if (q < rows) {
 #pragma unroll
-  for (int dt = 0; dt < DT; ++dt) {
-    const int col = dt * 8 + 2 * tq;
-    *reinterpret_cast<float2*>(scratch + (warp * 16 + q) * D + col) = make_float2(o[dt][0], o[dt][1]);
-    *reinterpret_cast<float2*>(scratch + (warp * 16 + q + 8) * D + col) = make_float2(o[dt][2], o[dt][3]);
+    for (int dt = 0; dt < DT; ++dt)
+      *reinterpret_cast<float2*>(scratch + (warp * 16 + q) * D + dt * 8 + 2 * tq) = make_float2(o[dt][0], o[dt][1]);
+  }
+  if (q + 8 < rows) {
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt)
+      *reinterpret_cast<float2*>(scratch + (warp * 16 + q + 8) * D + dt * 8 + 2 * tq) = make_float2(o[dt][2], o[dt][3]);
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kWinThreads) : "memory");
   // warp w finalises rows w, w + 8 of the group; lane l owns columns l * D/32 ..

@@ -29,6 +29,12 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
   return FF{hi, __fsub_rn(t, __fsub_rn(hi, s))};
 }
 __device__ __forceinline__ FF ff_neg(FF a) { return FF{-a.hi, -a.lo}; }
+// The exact sum of two floats as a float-float (Knuth's TwoSum).
+__device__ __forceinline__ FF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float v = __fsub_rn(s, a);
+  return FF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, v)), __fsub_rn(b, v))};
+}
 // a * b for float-float a and float b: the exact product of the high parts (FMA) plus the low
 // part's product, renormalised
 __device__ __forceinline__ FF ff_mul_f(FF a, float b) {

@@ -505,11 +505,25 @@ __device__ __forceinline__ void keep_slab(float4* s_r, int sl, const float (&r)[
 #pragma unroll
   for (int j = 0; j < 4; ++j) s_r[(sl * 4 + j) * 32 + lane] = make_float4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
 }
-__device__ __forceinline__ void slab_resid(const float* tr, const float* dr, int base, int V, float Mt, float iZt,
-                                           float Md, float iZd, bool has_d, float (&r)[16]) {
-  SlabData D;
-  slab_load(tr, dr, base, V, has_d, D);
-  slab_compute(D, base, V, Mt, iZt, Md, iZd, has_d, r);
+// The residual values of the slab starting at `base` with lane l holding elements 16 l .. 16 l + 15
+// (0 past V; V % 4 == 0).
+__device__ __forceinline__ void slab_resid_lanes(const float* tr, const float* dr, int base, int V, float Mt,
+                                                 float iZt, float Md, float iZd, bool has_d, float (&r)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int idx = base + lane * 16 + m * 4;
+    float4 tv = make_float4(0.f, 0.f, 0.f, 0.f), dv = tv;
+    if (idx < V) {
+      tv = __ldcg(reinterpret_cast<const float4*>(tr + idx));
+      if (has_d) dv = __ldcg(reinterpret_cast<const float4*>(dr + idx));
+    }
+    const bool in = idx < V;
+    r[4 * m + 0] = in ? resid_fast(tv.x, dv.x, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * m + 1] = in ? resid_fast(tv.y, dv.y, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * m + 2] = in ? resid_fast(tv.z, dv.z, Mt, iZt, Md, iZd, has_d) : 0.f;
+    r[4 * m + 3] = in ? resid_fast(tv.w, dv.w, Mt, iZt, Md, iZd, has_d) : 0.f;
+  }
 }
 // One slab's residual mass (compensated fp32 per lane, float-float across the warp; lane 0).  It is
 // positive exactly when the slab holds a positive residual.
@@ -546,10 +560,13 @@ __device__ __forceinline__ void slab_scan(const FF* s_slab, int ns, FF& lsum, FF
 // merges the item statistics of the sequence's rows and decides k (identical in every CTA: same
 // inputs, same order); CTA `rank` then takes slabs [rank * per, (rank + 1) * per) of the residual
 // row and records each slab's mass in shared memory (compensated fp32 per lane, float-float across
-// the warp) and its own total.  After a cluster barrier one warp reads the CS totals through
-// distributed shared memory in rank order, so every CTA agrees on R and on each CTA's prefix; the
-// CTA whose [prefix, prefix + total) holds u * R scans its slab masses, re-reads the slab that
-// passes the threshold and scans it element by element.  All of it in float-float (no fp64).
+// the warp) and its own total, which it writes into every CTA of the cluster (distributed shared
+// memory) before a cluster barrier; each thread then sums the CS totals in rank order, so every
+// CTA agrees on R and on each CTA's prefix.  In the CTA whose [prefix, prefix + total) holds u * R,
+// warp 0 finds the slab from the scan of its slab masses, then the element: lane l takes the
+// slab's elements 16 l .. 16 l + 15 (kept in shared memory, else recomputed), one warp scan of
+// the lanes' sums picks the lane, which searches its four groups of four.  All of it in
+// float-float (no fp64).
 // Every CTA takes the same cluster barriers (the decisions that steer them are identical across
 // the cluster).
 __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __grid_constant__ SampleParams p) {
@@ -559,8 +576,8 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   __shared__ FF sZ[2 * kMaxGamma + 1];
   __shared__ int s_k;
   __shared__ int32_t s_x[kMaxGamma];  // the draft tokens (for the output row)
-  __shared__ FF s_total;              // this CTA's residual mass (read by the whole cluster)
-  __shared__ FF s_R, s_cum;           // the cluster's total and this CTA's prefix
+  __shared__ FF s_tot[8];             // the residual mass of every CTA of the cluster, by rank (each
+                                      // CTA writes its own into all of them)
   cg::cluster_group cl = cg::this_cluster();
   const int CS = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const int b = blockIdx.x / CS;
@@ -642,22 +659,28 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
   float Md = has_d ? sM[p.rows_t + k] : 0.f;
   float iZd = has_d ? __fdiv_rn(1.f, sZ[p.rows_t + k].hi) : 0.f;
 
-  FF R{0.f, 0.f}, cum{0.f, 0.f};
+  FF R{0.f, 0.f}, cum{0.f, 0.f}, mine{0.f, 0.f};
+  FF lsum{0.f, 0.f}, incl{0.f, 0.f};  // warp 0: lane-block sums and scan of the slab masses
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (k >= 0) {
-      // two slabs per step, both in flight before either is reduced
-      for (int s = s0 + warp; s < s1; s += 2 * kFinWarps) {
+      // this warp's slabs s0 + warp + j * kFinWarps, two buffers in a pipeline: the next slab of a
+      // buffer is loaded as soon as the buffer's slab has been reduced, while the other buffer's
+      // slab is reduced
+      SlabData D0, D1;
+      const int sa0 = s0 + warp;
+      if (sa0 < s1) slab_load(tr, dr, sa0 * kSlab, p.V, has_d, D0);
+      if (sa0 + kFinWarps < s1) slab_load(tr, dr, (sa0 + kFinWarps) * kSlab, p.V, has_d, D1);
+      for (int s = sa0; s < s1; s += 2 * kFinWarps) {
         const int s2 = s + kFinWarps;
-        SlabData D0, D1;
-        slab_load(tr, dr, s * kSlab, p.V, has_d, D0);
-        if (s2 < s1) slab_load(tr, dr, s2 * kSlab, p.V, has_d, D1);
         float r[16];
         slab_compute(D0, s * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+        if (s + 2 * kFinWarps < s1) slab_load(tr, dr, (s + 2 * kFinWarps) * kSlab, p.V, has_d, D0);
         if (keep) keep_slab(s_r, s - s0, r);
         const FF m0 = slab_mass(r);
         if (lane == 0) s_slab[s - s0] = m0;
         if (s2 < s1) {
           slab_compute(D1, s2 * kSlab, p.V, Mt, iZt, Md, iZd, has_d, r);
+          if (s2 + 2 * kFinWarps < s1) slab_load(tr, dr, (s2 + 2 * kFinWarps) * kSlab, p.V, has_d, D1);
           if (keep) keep_slab(s_r, s2 - s0, r);
           const FF m1 = slab_mass(r);
           if (lane == 0) s_slab[s2 - s0] = m1;
@@ -666,26 +689,22 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
     }
     __syncthreads();
     if (warp == 0) {
-      FF lsum{0.f, 0.f}, incl{0.f, 0.f};
+      // the CTA's total (lane 31 of the scan), pushed into every CTA of the cluster at this rank
+      lsum = FF{0.f, 0.f};
+      incl = FF{0.f, 0.f};
       if (k >= 0) slab_scan(s_slab, s1 - s0, lsum, incl);
-      if (lane == 31) s_total = incl;
+      const FF tot = shfl_ff(incl, 31);
+      if (lane < CS) *cl.map_shared_rank(&s_tot[rank], lane) = tot;
     }
     cl.sync();
-    // the cluster's totals in rank order (one remote read per lane, then a fixed-order sum), the
-    // same in every CTA
-    if (warp == 0) {
-      FF tc{0.f, 0.f};
-      if (lane < CS) tc = *cl.map_shared_rank(&s_total, lane);
-      FF run{0.f, 0.f}, mycum{0.f, 0.f};
-      for (int c = 0; c < CS; ++c) {
-        if (c == rank) mycum = run;
-        run = ff_add(run, shfl_ff(tc, c));
-      }
-      if (lane == 0) { s_R = run; s_cum = mycum; }
+    // the cluster's totals in rank order, summed in a fixed order: the same R in every thread of
+    // every CTA, and this CTA's prefix
+    R = FF{0.f, 0.f};
+    for (int c = 0; c < CS; ++c) {
+      if (c == rank) cum = R;
+      R = ff_add(R, s_tot[c]);
     }
-    __syncthreads();
-    R = s_R;
-    cum = s_cum;
+    mine = s_tot[rank];
     if (k >= 0 && R.hi == 0.f && has_d) {
       // residual identically zero: draw from P_{k+1} itself
       has_d = false;
@@ -698,17 +717,15 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
     break;
   }
 
-  if (k >= 0 && R.hi > 0.f) {
-    const float uu = __shfl_sync(0xffffffffu, u_draw, 0);   // meaningful in warp 0, the only user
+  if (k >= 0 && R.hi > 0.f && warp == 0) {
+    const float uu = __shfl_sync(0xffffffffu, u_draw, 0);
     const FF thr = ff_mul_f(R, uu);
-    const FF nxt = ff_add(cum, s_total);
-    if (warp == 0 && !ff_gt(cum, thr) && ff_gt(nxt, thr)) {
-      // this CTA holds the threshold: the same lane-block scan of its slab masses as for its total
-      // gives every slab's prefix in token order
+    const FF nxt = ff_add(cum, mine);
+    if (!ff_gt(cum, thr) && ff_gt(nxt, thr)) {
+      // this CTA holds the threshold: the scan of its slab masses (kept from the total) gives
+      // every slab's prefix in token order
       const int ns = s1 - s0;
       const int pp = (ns + 31) / 32;
-      FF lsum, incl;
-      slab_scan(s_slab, ns, lsum, incl);
       int my_sl = -1;
       FF my_acc{0.f, 0.f};
       {
@@ -741,63 +758,61 @@ __global__ void __launch_bounds__(kFinThreads, 1) sample_chain_finish(const __gr
       if (found) {
         const int src = __ffs(found) - 1;
         const int sl = __shfl_sync(0xffffffffu, my_sl, src);
-        FF base = at_end ? thr : shfl_ff(my_acc, src);
-        // the slab's residual values (kept from the mass pass, else recomputed from the rows), scanned
-        // in token order: quarter j holds lane l's elements 4l..4l+3
-        float r[16];
+        const FF base = shfl_ff(my_acc, src);
+        // the slab's residual values in token order, lane l holding elements 16 l .. 16 l + 15
+        // (kept from the mass pass, else recomputed from the rows)
         const int sbase = (s0 + sl) * kSlab;
+        float r[16];
         if (keep) {
+          // kept as quarters of 128: element 16 l + m sits in quarter l / 8 at position (l % 8) * 16 + m
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 v = s_r[(sl * 4 + j) * 32 + lane];
-            r[4 * j] = v.x;
-            r[4 * j + 1] = v.y;
-            r[4 * j + 2] = v.z;
-            r[4 * j + 3] = v.w;
+          for (int m = 0; m < 4; ++m) {
+            const float4 v = s_r[(sl * 4 + (lane >> 3)) * 32 + (lane & 7) * 4 + m];
+            r[4 * m] = v.x;
+            r[4 * m + 1] = v.y;
+            r[4 * m + 2] = v.z;
+            r[4 * m + 3] = v.w;
           }
         } else {
-          slab_resid(tr, dr, sbase, p.V, Mt, iZt, Md, iZd, has_d, r);
+          slab_resid_lanes(tr, dr, sbase, p.V, Mt, iZt, Md, iZd, has_d, r);
         }
-        int slab_last = -1;
+        int last = -1;  // this lane's last element with positive mass
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          if (r[e] > 0.f) slab_last = max(slab_last, sbase + (e >> 2) * 128 + lane * 4 + (e & 3));
+          if (r[e] > 0.f) last = sbase + lane * 16 + e;
+        // the lane's 16 values summed exactly in pairs, then in float-float: groups of 4 kept for
+        // the search inside the lane
+        FF gsum[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) slab_last = max(slab_last, __shfl_xor_sync(0xffffffffu, slab_last, o));
-        // the four quarters' lane sums and warp scans first (independent, so they overlap), then
-        // the quarters in order
-        FF qv[4], qiv[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          qv[j] = ff_add(ff_add(FF{r[4 * j], 0.f}, FF{r[4 * j + 1], 0.f}),
-                         ff_add(FF{r[4 * j + 2], 0.f}, FF{r[4 * j + 3], 0.f}));
-          qiv[j] = warp_scan_ff(qv[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (y >= 0 || at_end) break;
-          const int idx = sbase + j * 128 + lane * 4;
-          const FF q = qv[j];
-          const FF qi = qiv[j];
-          const unsigned hit = __ballot_sync(0xffffffffu, ff_gt(ff_add(base, qi), thr));
-          if (hit) {
-            const int hl = __ffs(hit) - 1;
-            int yy = -1;
-            if (lane == hl) {
-              FF run = ff_add(base, ff_add(qi, ff_neg(q)));
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                run = ff_add(run, FF{r[4 * j + e], 0.f});
-                if (yy < 0 && ff_gt(run, thr)) yy = idx + e;
-              }
-              if (yy < 0)
-                yy = r[4 * j + 3] > 0.f ? idx + 3 : (r[4 * j + 2] > 0.f ? idx + 2 : (r[4 * j + 1] > 0.f ? idx + 1 : idx));
+        for (int q = 0; q < 4; ++q)
+          gsum[q] = ff_add(two_sum(r[4 * q], r[4 * q + 1]), two_sum(r[4 * q + 2], r[4 * q + 3]));
+        const FF lt = ff_add(ff_add(gsum[0], gsum[1]), ff_add(gsum[2], gsum[3]));
+        const FF li = warp_scan_ff(lt);
+        const unsigned hit = at_end ? 0u : __ballot_sync(0xffffffffu, ff_gt(ff_add(base, li), thr));
+        if (hit) {
+          const int hl = __ffs(hit) - 1;
+          int yy = -1;
+          if (lane == hl) {
+            FF run = ff_add(base, ff_add(li, ff_neg(lt)));
+            int q = 0;
+            for (; q < 3; ++q) {
+              const FF nx = ff_add(run, gsum[q]);
+              if (ff_gt(nx, thr)) break;
+              run = nx;
             }
-            y = __shfl_sync(0xffffffffu, yy, hl);
+            for (int e = 0; e < 4 && yy < 0; ++e) {
+              run = ff_add(run, FF{r[4 * q + e], 0.f});
+              if (ff_gt(run, thr)) yy = sbase + lane * 16 + 4 * q + e;
+            }
+            if (yy < 0) yy = last;  // rounding: the lane's last positive element
           }
-          base = ff_add(base, shfl_ff(qi, 31));
+          y = __shfl_sync(0xffffffffu, yy, hl);
         }
-        if (y < 0) y = slab_last;  // rounding left the threshold at the slab end
+        if (y < 0) {  // rounding left the threshold at the slab end: its last positive element
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+          y = last;
+        }
       }
       if (lane == 0) write_chain_out(p, b, k, y, s_x);
     }
