@@ -1233,6 +1233,11 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
       const int pairs = (p.tc_groups + 1) / 2;
       p.nks = 1;
       p.grid_x = sms / pairs > 0 ? sms / pairs : 1;
+      // a whole number of CTAs per segment when every segment gets one: with equal lengths no
+      // CTA's range then spans two segments (a part change costs the CTA about five 64-key tiles:
+      // its records, the next part's Q rows and the refill), at the price of idle SMs
+      const int segs = p.B * p.Hkv;
+      if (segs <= p.grid_x) p.grid_x = segs * (p.grid_x / segs);
       if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
       e = launch_partial_tc_pair(p, tmK, tmV, stream);
       if (e != cudaSuccess) return e;

@@ -211,6 +211,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tma_load_4d_hint(sk + h * kPHalf, &tmK, &full[s], h * 64, key0, g, b, pol);
             tma_load_4d_hint(sk + kPTile + h * kPHalf, &tmV, &full[s], h * 64, key0, g, b, pol);
           }
+          // the first part's Q rows are plain loads by the softmax threads: with every CTA's
+          // K/V ring filling at once they would queue behind ~25 MB of copies, so after the first
+          // tile the rest of the ring waits until both row blocks' Q rows have landed
+          if (t == 0 && (!mbar_wait_bounded(&qfull[0], 0, &s_abort) || !mbar_wait_bounded(&qfull[1], 0, &s_abort))) {
+            fail();
+            ok = false;
+            ++t;
+            break;
+          }
         }
       }
       if (!ok || s_abort) {
