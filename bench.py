@@ -328,10 +328,11 @@ class Runner:
                                 draft_tokens=i["x"], uniforms=i["u"], workspace=self.ws_s)
 
     def launches_per_step(self):
-        """Our kernels per step by the library's launch rules (status/ticket memsets are not
-        counted); used only when the captured graphs cannot be inspected.  Verify: partial + merge.
-        Window: see below.  Sampling: one warp-per-sequence kernel for V <= 2048, else statistics +
-        finalize, plus the residual pass for the chain."""
+        """Our kernels per step by the library's launch rules (status memsets are not counted);
+        used only when the captured graphs cannot be inspected.  Verify: partial + merge.  Window:
+        one per-segment kernel for bf16 rings with <= 16 query rows per KV head and D 64/128, else
+        see below.  Sampling: one warp-per-sequence kernel for V <= 2048, else statistics + the
+        finishing kernel (cluster finish or greedy finalize)."""
         import torch
         cfg = self.cfg
         win = 0
@@ -339,17 +340,16 @@ class Runner:
             sms = torch.cuda.get_device_properties(0).multi_processor_count
             S, seg_tiles = cfg.B * cfg.Hkv, -(-cfg.window // 128)
             spc, even = -(-S // sms), -(-S * seg_tiles // sms)
-            if cfg.kv_dtype == "bf16" and cfg.D == 128 and cfg.G > 32:
+            if cfg.kv_dtype == "bf16" and cfg.G <= 16 and cfg.D in (64, 128):
+                per_call = 1                     # attn_window_bf16: one CTA per segment
+            elif cfg.kv_dtype == "bf16" and cfg.D == 128 and cfg.G > 32:
                 per_call = 3                     # append + tensor-core partial + merge
             elif cfg.kv_dtype == "bf16" and cfg.G <= 64 and spc * seg_tiles <= max(2 * even, 16):
                 per_call = 1                     # whole segments per CTA: partial writes o itself
             else:
                 per_call = 2                     # partial + merge (append fused into the merge)
             win = cfg.draft_steps * per_call
-        if cfg.vocab <= 2048:
-            samp = 1
-        else:
-            samp = 2 if cfg.tree_nodes else 3
+        samp = 1 if cfg.vocab <= 2048 else 2
         return win + 2 + samp
 
 
@@ -760,53 +760,77 @@ def time_lmhead(runner, K, device, plant=0.6):
 
 
 def time_e2e(runner, K, W, device):
-    """The same round through the public API with host buffers: per step, pinned host -> device
-    copies of the round's inputs, the six calls, and a device -> host read of the emitted tokens."""
+    """The same round through the public API with host buffers.  Per step: pinned host -> device
+    copies of the round's inputs (verify queries and the gamma+1 new K/V rows, the draft queries
+    and new K/V rows, target and draft logits, draft tokens, uniforms), the calls, and a
+    device -> host read of the emitted tokens and accepted counts, which the host waits for before
+    it issues the step's successor.  The copies of step k + 1 run on a second stream into the
+    other of two device input buffers while step k computes, as a serving loop overlaps its input
+    transfers with compute; the verify call appends the new K/V rows to the cache itself (k_new,
+    v_new, the fused append)."""
     import torch
-    cfg, inp = runner.cfg, runner.inp
+    cfg, inp, sv = runner.cfg, runner.inp, runner.sv
     B, nq = cfg.B, cfg.nq
-    host = {}
-    for name in ("q", "tl", "dl", "x", "u", "dq", "dk", "dv"):
-        if inp.get(name) is not None:
-            host[name] = inp[name].cpu().pin_memory()
+    names = [n for n in ("q", "tl", "dl", "x", "u", "dq", "dk", "dv") if inp.get(n) is not None]
+    saved = {n: inp[n] for n in names}
+    host = {n: inp[n].cpu().pin_memory() for n in names}
     L = inp["kv_len_h"]
-    newk = inp["k"].new_empty((B, cfg.Hkv, nq, cfg.D)).cpu().pin_memory()
-    newv = newk.clone().pin_memory()
-    for b in range(B):
-        newk[b] = inp["k"][b, :, L[b] - nq:L[b]].cpu()
-        newv[b] = inp["v"][b, :, L[b] - nq:L[b]].cpu()
+    # the verified positions' K/V rows, [B, nq, Hkv, D] as the append takes them
+    host["k_new"] = torch.stack([inp["k"][b, :, L[b] - nq:L[b]].transpose(0, 1) for b in range(B)]).cpu().pin_memory()
+    host["v_new"] = torch.stack([inp["v"][b, :, L[b] - nq:L[b]].transpose(0, 1) for b in range(B)]).cpu().pin_memory()
+    bufs = [{n: torch.empty(t.shape, dtype=t.dtype, device=device) for n, t in host.items()} for _ in range(2)]
     out_h = torch.empty(tuple(inp["out"].shape), dtype=torch.int32).pin_memory()
     nacc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + 2 * newk.numel() * newk.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * 4 + nacc_h.numel() * 4
-    same_len = bool(np.all(L == L[0]))
+    comp = torch.cuda.current_stream(device)
+    copy_s = torch.cuda.Stream(device=device)
+    ready = [torch.cuda.Event() for _ in range(2)]   # buffer i holds its step's inputs
+    free = [torch.cuda.Event() for _ in range(2)]    # the step that read buffer i is done
+    done = torch.cuda.Event()                        # the step's results are on the host
 
-    def one():
-        for name, t in host.items():
-            inp[name].copy_(t, non_blocking=True)
-        if same_len:
-            inp["k"][:, :, L[0] - nq:L[0]].copy_(newk, non_blocking=True)
-            inp["v"][:, :, L[0] - nq:L[0]].copy_(newv, non_blocking=True)
-        else:
-            for b in range(B):
-                inp["k"][b, :, L[b] - nq:L[b]].copy_(newk[b], non_blocking=True)
-                inp["v"][b, :, L[b] - nq:L[b]].copy_(newv[b], non_blocking=True)
-        for s in range(cfg.draft_steps if cfg.window else 0):
-            runner.draft(s)
-        runner.verify()
+    def copy_in(k):
+        i = k % 2
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(free[i])
+            for n, t in host.items():
+                bufs[i][n].copy_(t, non_blocking=True)
+            ready[i].record(copy_s)
+
+    def compute(k):
+        i = k % 2
+        comp.wait_event(ready[i])
+        b = bufs[i]
+        for n in names:
+            inp[n] = b[n]
+        for s_ in range(cfg.draft_steps if cfg.window else 0):
+            runner.draft(s_)
+        sv.spec_verify_attn(inp["q"], inp["k"], inp["v"], inp["kv_len"], inp["o"], tree_parent=inp["tree"],
+                            workspace=runner.ws_v, k_new=b["k_new"], v_new=b["v_new"])
         runner.sample()
+        free[i].record(comp)
         out_h.copy_(inp["out"], non_blocking=True)
         nacc_h.copy_(inp["nacc"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        done.record(comp)
 
-    for _ in range(W):
-        one()
+    def run(n):
+        copy_in(0)
+        compute(0)
+        for k in range(n):
+            if k + 1 < n:
+                copy_in(k + 1)    # overlaps step k
+            done.synchronize()    # step k's tokens and counts are on the host
+            if k + 1 < n:
+                compute(k + 1)
+
+    run(W)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(K):
-        one()
+    run(K)
     torch.cuda.synchronize()
-    return (time.perf_counter() - t0) / K, h2d, d2h
+    sec = (time.perf_counter() - t0) / K
+    inp.update(saved)
+    return sec, h2d, d2h
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
@@ -916,9 +940,27 @@ def time_draft_cold(runner, K, device):
             g.replay()
             e1.record(stream)
         stream.synchronize()
+        # the same measurement of a one-node graph holding a 16-byte fill: the part of the figure
+        # any single-call graph pays (launch of the graph and its node), for context
+        tiny = torch.empty(4, dtype=torch.int32, device=device)
+        gt = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gt, stream=stream, capture_error_mode="thread_local"):
+            tiny.fill_(1)
+        for _ in range(3):
+            gt.replay()
+        evt = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for e0, e1 in evt:
+            flush(1)
+            e0.record(stream)
+            gt.replay()
+            e1.record(stream)
+        stream.synchronize()
     us = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    floor = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evt]))
     nb = step_bytes(cfg, inp)["window"]
-    return {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "bytes": nb, "l2": L2_NOTE.replace("L2 flushed", "flushed") + " call"}
+    return {"us": us, "gbs": nb / (us * 1e-6) / 1e9, "bytes": nb,
+            "l2": L2_NOTE.replace("L2 flushed", "flushed") + " call",
+            "one_node_graph_floor_us": floor}
 
 
 def oracle_check_sampling(cfg, runner):
@@ -1111,7 +1153,7 @@ def main():
 # Revision tag of each verify kernel that profiles/roofline_counters.json was measured on; a
 # counter taken on another revision is not reported.
 KERNEL_REVS = {"magicdec-64k": "mma8w-kt128-v3", "llama3-70b-layer": "tc2wg-kt128-v2",
-               "llama3-8b-layer": "mma8w-kt128-v3", "medusa-tree-8k": "pair-kt64-v5"}
+               "llama3-8b-layer": "mma8w-kt128-v3", "medusa-tree-8k": "pair-kt64-v6"}
 
 if __name__ == "__main__":
     sys.exit(main())

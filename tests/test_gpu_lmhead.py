@@ -290,6 +290,15 @@ def test_stochastic_chain_llama3_8b_lm_head(sv):
     assert k.max() >= 1
 
 
+def test_stochastic_chain_magicdec_batch(sv):
+    """The MagicDec batch (32 sequences x 5 rows = 160 hidden rows: three accumulator passes) over
+    the LLaMA-3 vocabulary, logits handed out: the shape of the bench's LM-head record."""
+    cfg = CONFIGS["magicdec-64k"]
+    inp = gen.lmhead_grid_inputs(cfg.B, cfg.gamma + 1, 4096, cfg.vocab, cfg.seed)
+    k = _stochastic_chain(sv, inp, cfg.B - 2)
+    assert k.min() == 0 and k.max() >= 2
+
+
 @pytest.mark.parametrize("B,gamma,d,V,take", [(50, 4, 256, 3000, True), (40, 5, 128, 1004, False),
                                               (7, 32, 64, 2048, True), (3, 1, 192, 2052, False)])
 def test_stochastic_chain_shapes(sv, B, gamma, d, V, take):
