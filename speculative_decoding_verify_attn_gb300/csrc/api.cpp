@@ -77,6 +77,23 @@ bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int 
   return r == CUDA_SUCCESS;
 }
 
+// Q of the verify call as [B, nq, Hq, D] bf16 for the pair kernel: a box is one half of D (64
+// elements, 128-byte swizzle) of the G heads of one kv head over 128 / G consecutive positions,
+// i.e. 128 consecutive query rows of a row block in the kernel's row order.
+bool encode_q_map(CUtensorMap* m, const spec_attn_args* a) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int G = a->Hq / a->Hkv;
+  cuuint64_t dims[4] = {(cuuint64_t)a->D, (cuuint64_t)a->Hq, (cuuint64_t)a->nq, (cuuint64_t)a->B};
+  cuuint64_t strides[3] = {(cuuint64_t)a->q_stride_h * 2, (cuuint64_t)a->q_stride_t * 2, (cuuint64_t)a->q_stride_b * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a->q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D bf16 [rows, cols] row-major (cols contiguous), boxes of 64 columns x box_rows, 128B swizzle
 bool encode_2d_map(CUtensorMap* m, const void* base, int cols, int rows, int box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -242,8 +259,16 @@ int spec_verify_attn(const spec_attn_args* a, spec_stream_t stream) {
         !encode_kv_map(&tmV, a->v, a->D, a->Lmax, a->Hkv, a->B, a->kv_stride_h, a->kv_stride_b, box))
       return SPEC_ERR_CUDA;
   }
+  // the pair kernel (more than 128 query rows per kv head) takes its first Q rows by TMA when the
+  // rows of a block are whole GQA groups and the strides suit a tensor map; otherwise its threads
+  // load them
+  CUtensorMap tmQ;
+  bool qmap = false;
+  if (bf16 && a->q_dtype == SPEC_BF16 && specv::q_tma_possible(a->D, p.G, a->nq) && aligned(a->q, 16) &&
+      (a->q_stride_h * 2) % 16 == 0 && (a->q_stride_t * 2) % 16 == 0 && (a->q_stride_b * 2) % 16 == 0)
+    qmap = encode_q_map(&tmQ, a);
   cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16,
-                                          reinterpret_cast<cudaStream_t>(stream));
+                                          reinterpret_cast<cudaStream_t>(stream), qmap ? &tmQ : nullptr);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

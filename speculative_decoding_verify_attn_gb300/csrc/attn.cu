@@ -1196,8 +1196,12 @@ static cudaError_t launch_window_small(const AttnParams& p, const CUtensorMap* t
   return cudaGetLastError();
 }
 
+bool q_tma_possible(int D, int G, int nq) {
+  return D == 128 && G >= 1 && 128 % G == 0 && (nq * G) % 128 == 0 && nq * G > 128;
+}
+
 cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const CUtensorMap* tmQ) {
   AttnParams p = p_in;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1239,7 +1243,8 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
       const int segs = p.B * p.Hkv;
       if (segs <= p.grid_x) p.grid_x = segs * (p.grid_x / segs);
       if (p.grid_x > kMaxGridX) p.grid_x = kMaxGridX;
-      e = launch_partial_tc_pair(p, tmK, tmV, stream);
+      p.q_tma = (tmQ != nullptr && p.rows_per_group == 128 && q_tma_possible(p.D, p.G, p.nq)) ? 1 : 0;
+      e = launch_partial_tc_pair(p, tmK, tmV, p.q_tma ? tmQ : tmK, stream);
       if (e != cudaSuccess) return e;
       return launch_merge_pair(p, stream);
     }

@@ -62,6 +62,7 @@ struct AttnParams {
   int verify_append;
   int64_t new_st;
   int debug_no_loads;              // test hook: the producers issue no K/V copies (waits run out)
+  int q_tma;                       // pair kernel: the first part's Q rows come by TMA (tmQ)
   unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
 };
 
@@ -69,9 +70,14 @@ struct AttnParams {
 size_t attn_workspace_bytes(int segments, int rows, int D);
 void attn_workspace_carve(void* ws, int segments, int rows, int D, AttnParams* p);
 
-// Launch helpers; return a cudaError_t.  tmK/tmV are used by the bf16 path only.
+// Launch helpers; return a cudaError_t.  tmK/tmV are used by the bf16 path only; tmQ (may be
+// null) by the pair kernel only, over Q as [B, nq, Hq, D] with boxes of 64 x G heads x 128 / G
+// positions (see q_tma_possible).
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int kv_bf16,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const CUtensorMap* tmQ = nullptr);
+// Whether a Q tensor map for the pair kernel applies: D 128, every row block 128 rows of whole
+// GQA groups (G divides 128, nq * G a multiple of 128, more than 128 rows).
+bool q_tma_possible(int D, int G, int nq);
 
 // tcgen05 partial kernel (attn_tc.cu): D = 128, bf16, up to 128 query rows per row group; two
 // softmax warpgroups on alternate tiles, so each part leaves kTcSlices records.
@@ -85,7 +91,7 @@ size_t attn_tc_smem_bytes();
 // use 64-key boxes); one record per row and part, o as column-major [D][128] blocks.
 constexpr int kPairTileKeys = 64;
 cudaError_t launch_partial_tc_pair(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                   cudaStream_t stream);
+                                   const CUtensorMap* tmQ, cudaStream_t stream);
 size_t attn_tc_pair_smem_bytes();
 // Keys per TMA box the bf16 tensor maps of a launch need (rows = query rows per kv head).
 int attn_tile_keys(int rows, int D);

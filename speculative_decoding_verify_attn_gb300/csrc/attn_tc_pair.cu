@@ -135,11 +135,12 @@ __device__ __forceinline__ void p_zero_v_tail(uint8_t* vb, int key0, int len, in
 template <int MASK>
 __global__ void __launch_bounds__(kPThreads, 1)
     attn_partial_tc_pair(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ AttnParams p) {
+                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();  // the merge may be scheduled as SMs free up
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kPStages], empty[kPStages];
   __shared__ uint64_t sfull[2][2], pfull[2][2], pvdone[2][2], ofree[2], qfull[2], drain[2];
+  __shared__ uint64_t qfirst[2];  // q_tma: the first part's Q rows of each block, by TMA
   __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
 
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       mbar_init(&pvdone[w][1], 1);
       mbar_init(&ofree[w], 4);
       mbar_init(&qfull[w], 4);
+      mbar_init(&qfirst[w], 1);
       mbar_init(&drain[w], 1);
     }
     s_abort = 0;
@@ -191,6 +193,24 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      // q_tma: the first part's Q rows of both blocks are the CTA's first copies (the rows of a
+      // block are 128 / G consecutive positions x the G heads of kv head g: one box per half of D)
+      bool q_issued = false;
+      if (p.q_tma && !p.debug_no_loads) {
+        Walker w0 = w;
+        int b0, g0, kb0, ke0, len0;
+        if (walker_next(p, w0, b0, g0, kb0, ke0, len0)) {
+          tma_prefetch_desc(&tmQ);
+          for (int blk = 0; blk < 2; ++blk) {
+            const int j0 = ((2 * pair + blk) * p.rows_per_group) / p.G;
+            uint8_t* qb = qs + blk * kPQBlock;
+            mbar_arrive_expect_tx(&qfirst[blk], (uint32_t)kPQBlock);
+            tma_load_4d(qb, &tmQ, &qfirst[blk], 0, g0 * p.G, j0, b0);
+            tma_load_4d(qb + kPQHalf, &tmQ, &qfirst[blk], 64, g0 * p.G, j0, b0);
+          }
+          q_issued = true;
+        }
+      }
       // every K/V tile is read once: let it leave L2 first (the records and Q stay)
       const uint64_t pol = l2_policy_evict_first();
       int t = 0;
@@ -211,10 +231,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tma_load_4d_hint(sk + h * kPHalf, &tmK, &full[s], h * 64, key0, g, b, pol);
             tma_load_4d_hint(sk + kPTile + h * kPHalf, &tmV, &full[s], h * 64, key0, g, b, pol);
           }
-          // the first part's Q rows are plain loads by the softmax threads: with every CTA's
-          // K/V ring filling at once they would queue behind ~25 MB of copies, so after the first
-          // tile the rest of the ring waits until both row blocks' Q rows have landed
-          if (t == 0 && (!mbar_wait_bounded(&qfull[0], 0, &s_abort) || !mbar_wait_bounded(&qfull[1], 0, &s_abort))) {
+          // the first part's Q rows as plain loads by the softmax threads would queue behind
+          // every CTA's ring fill (~25 MB of copies), so after the first tile the rest of the ring
+          // waits until both row blocks' Q rows have landed
+          if (t == 0 && !p.q_tma &&
+              (!mbar_wait_bounded(&qfull[0], 0, &s_abort) || !mbar_wait_bounded(&qfull[1], 0, &s_abort))) {
             fail();
             ok = false;
             ++t;
@@ -227,6 +248,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int tt = t - i;
           mbar_wait_bounded(&full[tt % kPStages], (tt / kPStages) & 1, nullptr);
         }
+        if (q_issued) {
+          mbar_wait_bounded(&qfirst[0], 0, nullptr);
+          mbar_wait_bounded(&qfirst[1], 0, nullptr);
+        }
       }
     }
   } else if (warp <= 2) {
@@ -238,7 +263,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint32_t qa0 = qs_u32 + wm * kPQBlock;
       // S_wm(t) = Q K_t^T into S buffer t & 1
       auto issue_qk = [&](int t, const PTile& T) -> bool {
-        if (T.i == 0 && !mbar_wait_bounded(&qfull[wm], T.part & 1, &s_abort)) return false;
+        if (T.i == 0) {
+          // the part's Q rows: by TMA for the first part (q_tma), else stored by the softmax warps
+          const bool by_tma = p.q_tma && T.part == 0;
+          if (!mbar_wait_bounded(by_tma ? &qfirst[wm] : &qfull[wm], by_tma ? 0u : (uint32_t)((T.part - p.q_tma) & 1),
+                                 &s_abort))
+            return false;
+        }
         const int s = t % kPStages;
         if (!mbar_wait_bounded(&full[s], (t / kPStages) & 1, &s_abort)) return false;
         tc::fence_after();
@@ -321,7 +352,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     walker_init(p, cta, w);
     int b, g, kb, ke, len;
     bool have = walker_next(p, w, b, g, kb, ke, len);
-    if (have) load_q(b, g);
+    if (have && !p.q_tma) load_q(b, g);
     int t = 0, pv_seen = 0;
     bool ok = true;
     while (have && ok) {
@@ -625,22 +656,22 @@ cudaError_t launch_merge_pair(const AttnParams& p, cudaStream_t stream) {
 
 template <int MASK>
 static cudaError_t launch_pair_mask(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                    cudaStream_t stream) {
+                                    const CUtensorMap* tmQ, cudaStream_t stream) {
   const size_t smem = attn_tc_pair_smem_bytes();
   auto kern = attn_partial_tc_pair<MASK>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.grid_x * ((p.tc_groups + 1) / 2), kPThreads, smem, stream>>>(*tmK, *tmV, p);
+  kern<<<p.grid_x * ((p.tc_groups + 1) / 2), kPThreads, smem, stream>>>(*tmK, *tmV, *tmQ, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_partial_tc_pair(const AttnParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                   cudaStream_t stream) {
+                                   const CUtensorMap* tmQ, cudaStream_t stream) {
   if (p.nks != 1 || p.tc_groups < 2) return cudaErrorInvalidValue;
   switch (p.mask) {
-    case kMaskNone: return launch_pair_mask<kMaskNone>(p, tmK, tmV, stream);
-    case kMaskChain: return launch_pair_mask<kMaskChain>(p, tmK, tmV, stream);
-    default: return launch_pair_mask<kMaskTree>(p, tmK, tmV, stream);
+    case kMaskNone: return launch_pair_mask<kMaskNone>(p, tmK, tmV, tmQ, stream);
+    case kMaskChain: return launch_pair_mask<kMaskChain>(p, tmK, tmV, tmQ, stream);
+    default: return launch_pair_mask<kMaskTree>(p, tmK, tmV, tmQ, stream);
   }
 }
 
