@@ -396,9 +396,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) sample_tree_stochastic(const 
       for (int ch = n + 1; ch < p.N; ++ch) {
         if (p.parent[ch] != n) continue;
         const float* rows[2] = {p.tl + (int64_t)b * p.tl_sb + (int64_t)ch * p.V, p.dl + (int64_t)b * p.dl_sb + (int64_t)ch * p.V};
-        for (int k = 0; k < 2; ++k)
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rows[k] + 4 * lo4), "r"(len4 * 16)
-                       : "memory");
+        for (int k = 0; k < 2; ++k) l2_prefetch_bulk(rows[k] + 4 * lo4, (uint32_t)len4 * 16u);
       }
     }
     TreeRow T, Dr;
