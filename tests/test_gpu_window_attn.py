@@ -77,6 +77,26 @@ def test_window_full_batch_ring_sizes(sv, W):
         assert np.array_equal(kr_np[b, :, s_], k_after[b, :, s_].astype(np.float32))
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,W", [(64, 32, 2, 100), (128, 16, 1, 200), (128, 64, 8, 72)])
+def test_window_group_sizes_and_ragged_rings(sv, D, Hq, Hkv, W):
+    """The per-segment window kernel at its largest GQA group (16 rows per kv head) and rings whose
+    last 64-key tile runs past the ring (W = 100, 200: the copy reads zeros there, masked), with
+    filling and full rings."""
+    B = 12
+    pos = np.array([1, 2, 63, 64, 65, W - 1, W, W + 1, 2 * W + 3, 5000, 70001, 3 * W], dtype=np.int32)
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, pos, "bf16", seed=70 + W)
+    q, kr, vr = to_dev(inp["q"], "bf16"), to_dev(inp["k_ring"], "bf16"), to_dev(inp["v_ring"], "bf16")
+    kn, vn = to_dev(inp["k_new"], "bf16"), to_dev(inp["v_new"], "bf16")
+    o, st = _run(sv, q, kr, vr, to_dev(pos, "i32"), kn, vn, "bf16")
+    ref, k_after, _ = oa.draft_window_attn(inp["q"], inp["k_ring"], inp["v_ring"], pos, inp["k_new"], inp["v_new"])
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what=f"window G={Hq // Hkv} W={W}")
+    kr_np = to_np(kr)
+    for b in range(B):
+        s_ = (pos[b] - 1) % W
+        assert np.array_equal(kr_np[b, :, s_], k_after[b, :, s_].astype(np.float32))
+
+
 def test_magicdec_draft_round_four_steps(sv):
     """Four draft steps of a round, each appending one token, on the MagicDec window shape."""
     cfg = CONFIGS["magicdec-64k"]
