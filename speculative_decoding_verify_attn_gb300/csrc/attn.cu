@@ -921,13 +921,14 @@ __device__ __forceinline__ void load_vec(const float* src, float (&v)[PER]) {
 // per record.
 template <int D>
 __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnParams p) {
-  pdl_wait();  // the partial kernel's records
   constexpr int PER = D / 32;
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 4 + warp;
   if (r >= p.rows) return;
   const int b = s / p.Hkv, g = s % p.Hkv;
+  // where the segment's records are depends on the lengths only (inputs, final before the partial
+  // kernel started): worked out while the partial kernel still runs
   int64_t total, cum_b;
   warp_scan_tiles(p, b, total, cum_b);
   const int len = seg_len(p, b);
@@ -936,6 +937,7 @@ __global__ void __launch_bounds__(128) attn_merge(const __grid_constant__ AttnPa
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  pdl_wait();  // the partial kernel's records
   if (len > 0) {
     const int ntiles = seg_tiles(len);
     const int64_t per = tiles_per_cta(p, total);

@@ -532,7 +532,6 @@ constexpr int kMergeCols = 8;
 constexpr int kMergeBatch = 6;
 
 __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ AttnParams p) {
-  pdl_wait();  // the partial kernel's records
   const int s = blockIdx.x, blk = blockIdx.y, cc = blockIdx.z;
   const int m = threadIdx.x;
   const int b = s / p.Hkv, g = s % p.Hkv;
@@ -547,6 +546,9 @@ __global__ void __launch_bounds__(128) attn_merge_pair(const __grid_constant__ A
   float acc[kMergeCols];
 #pragma unroll
   for (int e = 0; e < kMergeCols; ++e) acc[e] = 0.f;
+  // the record positions depend on the lengths only (inputs): worked out above while the partial
+  // kernel still runs; its records from here on
+  pdl_wait();
   if (len > 0 && real) {
     const int ntiles = seg_tiles(len);
     const int64_t per = tiles_per_cta(p, total);
