@@ -93,6 +93,22 @@ def test_tensor_core_row_blocks(sv, Hq, Hkv, nq, tree):
     assert_attn_close(o, ref, "bf16", what=f"rows {nq * Hq // Hkv}")
 
 
+@pytest.mark.parametrize("Hq,Hkv,nq,tree", [(64, 8, 32, False), (64, 8, 48, True), (32, 8, 64, True), (32, 1, 16, True)])
+def test_pair_kernel_q_rows_by_tma(sv, Hq, Hkv, nq, tree):
+    """Row counts that are whole multiples of 128 (256, 384, 256 and 512 rows), where the pair
+    kernel takes the first part's Q rows by TMA: a chain mask, a 3-block launch whose last pair
+    has one block entirely past the rows (its copy starts beyond the tensor and reads zeros), the
+    Medusa shape, and G = 32 (boxes of 32 heads x 4 positions)."""
+    kv_len = np.array([2900, 1400], dtype=np.int32)
+    parent = gen.random_tree(nq, 5, 8, 78 + nq) if tree else None
+    inp = gen.attn_inputs(2, Hq, Hkv, 128, nq, kv_len, 3000, "bf16", 95 + nq)
+    inp = gen.plant_tree_needles(inp, parent, "bf16", 96) if tree else gen.plant_chain_needles(inp, nq, "bf16", 96)
+    o, st = run_verify(sv, inp, "bf16", tree_parent=parent)
+    ref = oa.verify_attn(inp["q"], inp["k"], inp["v"], kv_len, tree_parent=parent)
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what=f"rows {nq * Hq // Hkv}")
+
+
 def test_chain_shaped_tree_matches_chain_on_gpu(sv):
     cfg = CONFIGS["llama3-8b-layer"]
     kv_len = np.array([640, 333], dtype=np.int32)
