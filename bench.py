@@ -963,6 +963,55 @@ def time_draft_cold(runner, K, device):
             "one_node_graph_floor_us": floor}
 
 
+def time_draft_rotating(runner, K, device, copies=4, calls=16):
+    """Draft-window calls back to back in one graph, each on a different copy of the rings
+    (`copies` of them, together several times the size of L2), so that every call streams a ring
+    the previous calls have evicted: the cold per-call figure of a run of draft steps, without the
+    launch of a graph per call.  Beside it, the same run on one ring (L2-resident after the first
+    call).  Returns both per-call times."""
+    import torch
+    cfg, inp = runner.cfg, runner.inp
+    ring_bytes = inp["k_ring"].numel() * inp["k_ring"].element_size() * 2
+    copies = max(copies, int(-(-3 * (126 << 20) // ring_bytes)) + 1)
+    rings = [(inp["k_ring"].clone(), inp["v_ring"].clone()) for _ in range(copies)]
+    i = inp
+    stream = torch.cuda.Stream(device=device)
+    flush = L2Flush(device)
+
+    def run(rotate):
+        for c in range(calls):
+            kr, vr = rings[c % copies] if rotate else rings[0]
+            s = c % cfg.draft_steps
+            runner.sv.spec_draft_window_attn(i["dq"][s], kr, vr, i["dpos"][s], i["do"], k_new=i["dk"][s],
+                                             v_new=i["dv"][s], workspace=runner.ws_w, n_sinks=runner.n_sinks)
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for rotate in (True, False):
+            run(rotate)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                run(rotate)
+            for _ in range(3):
+                g.replay()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            for e0, e1 in evs:
+                flush(1)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            out["rotating" if rotate else "same_ring"] = 1000 * float(np.mean([a.elapsed_time(b) for a, b in evs])) / calls
+    del rings
+    nb = step_bytes(cfg, inp)["window"]
+    return {"us": out["rotating"], "gbs": nb / (out["rotating"] * 1e-6) / 1e9, "bytes": nb,
+            "l2": f"{calls} calls back to back in one graph over {copies} copies of the rings "
+                  f"({copies * ring_bytes / 1e6:.0f} MB): every call streams a ring evicted by the calls before it",
+            "l2_resident": {"us": out["same_ring"], "gbs": nb / (out["same_ring"] * 1e-6) / 1e9,
+                            "l2": f"the same {calls} calls on one ring, L2-resident after the first call"}}
+
+
 def oracle_check_sampling(cfg, runner):
     """CPU-oracle leg: the oracle's spec_sample on the bench's own sampling inputs (copied back
     from the device), against the GPU's outputs of the last timed call.  Returns the counts the
@@ -1056,6 +1105,10 @@ def measure(cfg, args, pg, device, rank, world, full):
             cold = time_draft_cold(runner, max(5, min(args.steps, 50)), device)
             cold["gbs"] = sum_over_ranks(pg, cold["gbs"], device)
             rec["draft_window_cold"] = cold
+            rot = time_draft_rotating(runner, max(5, min(args.steps, 30)), device)
+            rot["gbs"] = sum_over_ranks(pg, rot["gbs"], device)
+            rot["l2_resident"]["gbs"] = sum_over_ranks(pg, rot["l2_resident"]["gbs"], device)
+            rec["draft_window_cold_run"] = rot
         e2e = None
         if not args.no_e2e:
             sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
@@ -1116,6 +1169,7 @@ def main():
         "draft_window_gbs_note": "in-round figure: steps 2-4 re-read a ring the step before left in L2 "
                                  "(see draft_window_cold for the L2-flushed call)" if cfg.window else None,
         "draft_window_cold": main_rec.get("draft_window_cold"),
+        "draft_window_cold_run": main_rec.get("draft_window_cold_run"),
         "sample_gbs": main_rec["sample_gbs"],
         "sample_hbm_frac": main_rec["sample_hbm_frac"],
         "sample_near_threshold": main_rec.get("sample_near_threshold"),

@@ -67,11 +67,12 @@ bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int 
                    int64_t stride_b, int box_keys = specv::kKeyTile) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)Hkv, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)stride_h * 2, (cuuint64_t)stride_b * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_keys, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+  // (column, key, half of D, head, batch): a box is a whole tile, its halves one after the other
+  cuuint64_t dims[5] = {64, (cuuint64_t)L, (cuuint64_t)D / 64, (cuuint64_t)Hkv, (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)stride_h * 2, (cuuint64_t)stride_b * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)box_keys, (cuuint32_t)D / 64, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

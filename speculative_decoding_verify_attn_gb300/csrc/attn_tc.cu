@@ -157,11 +157,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           uint8_t* sk = stages + s * 2 * kTile;
           mbar_arrive_expect_tx(&full[s], 2u * kTile);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_4d(sk + h * kHalf, &tmK, &full[s], h * 64, key0, g, b);
-            tma_load_4d(sk + kTile + h * kHalf, &tmV, &full[s], h * 64, key0, g, b);
-          }
+          tma_load_kv(sk, &tmK, &full[s], key0, g, b);
+          tma_load_kv(sk + kTile, &tmV, &full[s], key0, g, b);
         }
       }
       if (!ok || s_abort) {

@@ -226,11 +226,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
           uint8_t* sk = stages + s * 2 * kPTile;
           mbar_arrive_expect_tx(&full[s], 2u * kPTile);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_4d_hint(sk + h * kPHalf, &tmK, &full[s], h * 64, key0, g, b, pol);
-            tma_load_4d_hint(sk + kPTile + h * kPHalf, &tmV, &full[s], h * 64, key0, g, b, pol);
-          }
+          tma_load_kv_hint(sk, &tmK, &full[s], key0, g, b, pol);
+          tma_load_kv_hint(sk + kPTile, &tmV, &full[s], key0, g, b, pol);
           // the first part's Q rows as plain loads by the softmax threads would queue behind
           // every CTA's ring fill (~25 MB of copies), so after the first tile the rest of the ring
           // waits until both row blocks' Q rows have landed

@@ -182,6 +182,26 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, ui
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
+// K or V tiles: one 5-D box {64 columns, keys, D / 64 halves, 1, 1} of a map over
+// [B, Hkv, L, D] viewed as (column, key, half, head, batch), landing as the tile's halves one
+// after the other ([half][key][128 B]) -- the layout of one 4-D box per half, in one copy.  The
+// tensor-memory-access unit of an SM completes copies at a rate set more by their number than
+// by their size, so a whole tile per copy halves the copies of a D = 128 ring.
+__device__ __forceinline__ void tma_load_kv(void* smem_dst, const void* tmap, uint64_t* bar, int key0, int g, int b) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %2, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(key0), "r"(g), "r"(b), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_kv_hint(void* smem_dst, const void* tmap, uint64_t* bar, int key0, int g,
+                                                 int b, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %2, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(key0), "r"(g), "r"(b), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 // The same load with an L2 eviction-priority policy (for data read exactly once, so that it does
 // not push out data that is read again soon).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
