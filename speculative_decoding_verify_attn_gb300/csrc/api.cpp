@@ -95,15 +95,17 @@ bool encode_q_map(CUtensorMap* m, const spec_attn_args* a) {
   return r == CUDA_SUCCESS;
 }
 
-// 2-D bf16 [rows, cols] row-major (cols contiguous), boxes of 64 columns x box_rows, 128B swizzle
-bool encode_2d_map(CUtensorMap* m, const void* base, int cols, int rows, int box_rows) {
+// bf16 [rows, cols] row-major (cols contiguous, a multiple of 64) viewed as (column in chunk, row,
+// chunk of 64 columns): a box is box_rows rows x box_chunks chunks, landing chunk after chunk,
+// each chunk's rows 128 bytes apart with the 128-byte swizzle
+bool encode_chunk_map(CUtensorMap* m, const void* base, int cols, int rows, int box_rows, int box_chunks) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)cols / 64};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -502,13 +504,15 @@ int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
   p.npad = (p.nrows + 15) / 16 * 16;
   p.n_vtiles = (a->V + 127) / 128;
   p.tiles_per_pass = 512 / p.npad;
-  size_t smem;
-  specv::lmhead_layout(p.npad, &p.w_stages, &p.h_stages, &p.kgroup, &smem);
+  const specv::LmLayout lay = specv::lmhead_layout(p.npad);
+  p.w_stages = lay.w_stages; p.h_stages = lay.h_stages; p.kgroup = lay.kgroup;
+  p.wbox = lay.wbox; p.hbox = lay.hbox;
   p.tok = a->draft_tokens; p.tok_sb = a->tok_stride_b;
   p.out_cols = a->out_cols; p.out_tok = a->out_tokens; p.out_nacc = a->out_num_accepted; p.out_nodes = a->out_path_nodes;
   specv::lmhead_workspace_carve(a->workspace, &p);
   CUtensorMap tmW, tmH;
-  if (!encode_2d_map(&tmW, a->weight, a->d, a->V, 128) || !encode_2d_map(&tmH, a->hidden, a->d, p.nrows, p.npad))
+  if (!encode_chunk_map(&tmW, a->weight, a->d, a->V, 128, p.wbox) ||
+      !encode_chunk_map(&tmH, a->hidden, a->d, p.nrows, p.npad, p.hbox))
     return SPEC_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (!stochastic) {

@@ -41,29 +41,29 @@ constexpr int kLmSmemCap = 227 * 1024;        // dynamic shared memory of one CT
 constexpr int kLmWStagesMax = 16;
 constexpr int kLmHStagesMax = 8;
 
-// A tile takes `kgroup` K chunks in a row, so its accumulator sees chains of 4 kgroup MMAs.  On
-// GB300 a chain of 4 small-N MMAs costs about 660 cycles, of 16 about 1300: chains of 4 leave the
-// single issuer slower than the weight stream, so the group is 4 chunks where the hidden ring can
-// hold two groups of them (npad <= 96) and 2 otherwise.  The hidden ring holds two groups (the one
-// in use and the next; at least 4 chunks), one chunk less if that leaves fewer than 6 weight
-// stages; the rest of shared memory is weight.
-static void lmhead_layout_g(int npad, int g, int* w_stages, int* h_stages, int* kgroup, size_t* smem) {
-  const size_t hb = (size_t)npad * 128;
+// Ring layout.  A tile takes `kgroup` K chunks in a row, so its accumulator sees chains of
+// 4 kgroup MMAs: on GB300 a chain of 4 small-N MMAs costs about 660 cycles, of 16 about 1300, so
+// chains of 4 would leave the single issuer slower than the weight stream; the group is 4 chunks
+// where the hidden rows are few (npad <= 96) and 2 otherwise.  Both rings take several K chunks
+// per copy (3-D boxes): an SM's tensor-memory-access unit completes copies at a rate set more by
+// their number than by their size (about one per 0.3 us for 16-32 KB boxes), so 16 KB copies
+// alone would cap an SM near the HBM share it needs for the weight, and the hidden rows' copies
+// on top of those slow the weight stream down.  The hidden ring holds two groups (the one in use
+// and the next) in one copy each, or, above 192 rows, three one-chunk copies (a 64 KB group copy
+// would leave too little room for weight); the rest of shared memory is weight, two chunks per
+// copy.
+LmLayout lmhead_layout(int npad) {
+  LmLayout L;
   const size_t budget = kLmSmemCap - 1024 - 2560;  // alignment pad; static barriers and keys
-  int hs = 2 * g > 4 ? 2 * g : 4;
-  int ws = (int)((budget - hs * hb) / kLmWChunk);
-  if (ws < 6) {
-    hs = hs - 1 > g + 1 ? hs - 1 : g + 1;
-    ws = (int)((budget - hs * hb) / kLmWChunk);
-  }
-  ws = ws > kLmWStagesMax ? kLmWStagesMax : ws;
-  *w_stages = ws;
-  *h_stages = hs;
-  *kgroup = g;
-  *smem = 1024 + (size_t)ws * kLmWChunk + (size_t)hs * hb;
-}
-void lmhead_layout(int npad, int* w_stages, int* h_stages, int* kgroup, size_t* smem) {
-  lmhead_layout_g(npad, npad <= 96 ? 4 : 2, w_stages, h_stages, kgroup, smem);
+  L.kgroup = npad <= 96 ? 4 : 2;
+  L.wbox = 2;
+  L.hbox = npad <= 192 ? L.kgroup : 1;
+  L.h_stages = npad <= 192 ? 2 : 3;
+  const size_t hb = (size_t)npad * 128 * L.hbox, wb = (size_t)kLmWChunk * L.wbox;
+  int ws = (int)((budget - L.h_stages * hb) / wb);
+  L.w_stages = ws > kLmWStagesMax ? kLmWStagesMax : ws;
+  L.smem = 1024 + (size_t)L.w_stages * wb + (size_t)L.h_stages * hb;
+  return L;
 }
 
 // Keys: (ord(value) << 32) | ~id, so that the unsigned order is: larger value first, then smaller id.
@@ -84,11 +84,14 @@ __device__ __forceinline__ LmWalk lm_walk(const LmheadParams& p) {
   return w;
 }
 
-__device__ __forceinline__ void lm_tma_load_2d(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1) {
+// One box of a [rows, d] bf16 matrix viewed as (column in chunk, row, chunk): `box chunks` K
+// chunks of 64 columns of the box's rows, landing chunk after chunk ([chunk][row][128 B]).
+__device__ __forceinline__ void lm_tma_load_chunks(void* smem_dst, const void* tmap, uint64_t* bar, int row0,
+                                                   int chunk0) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(row0), "r"(chunk0), "r"(smem_u32(bar))
       : "memory");
 }
 // Whole warp: 16 consecutive 32-bit TMEM columns of this warp's 32 lanes, waited for in the same
@@ -110,16 +113,10 @@ __device__ __forceinline__ uint32_t lm_ord(float v) {
   if ((u << 1) == 0u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ uint32_t lm_redux_max(uint32_t x) {
-  uint32_t r;
-  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
-  return r;
-}
-__device__ __forceinline__ uint32_t lm_redux_min(uint32_t x) {
-  uint32_t r;
-  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(x));
-  return r;
-}
+// Warp reductions as compiler intrinsics (not volatile asm), so that the reductions of different
+// columns can overlap instead of each waiting for the one before it.
+__device__ __forceinline__ uint32_t lm_redux_max(uint32_t x) { return __reduce_max_sync(0xffffffffu, x); }
+__device__ __forceinline__ uint32_t lm_redux_min(uint32_t x) { return __reduce_min_sync(0xffffffffu, x); }
 __device__ __forceinline__ void lm_epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // NC consecutive accumulator columns (hidden rows) starting at TMEM address `col0` of tile 0, over
@@ -155,12 +152,14 @@ __device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt,
       }
     }
   }
+  uint32_t mo[NC];
+#pragma unroll
+  for (int e = 0; e < NC; ++e) mo[e] = lm_redux_max(o[e]);
 #pragma unroll
   for (int e = 0; e < NC; ++e) {
-    const uint32_t mo = lm_redux_max(o[e]);
-    const uint32_t mi = lm_redux_min(o[e] == mo ? ix[e] : 0xffffffffu);
+    const uint32_t mi = lm_redux_min(o[e] == mo[e] ? ix[e] : 0xffffffffu);
     if (lane == e) {
-      bo = mo;
+      bo = mo[e];
       bi = mi;
     }
   }
@@ -180,10 +179,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   __shared__ int s_abort;
   __shared__ unsigned long long s_key[kLmMaxRows];   // this CTA's running key per hidden row
   const uint32_t raw = smem_u32(smem_raw);
-  uint8_t* wring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // [stage][128 rows][128 B]
-  const int WS = p.w_stages, HS = p.h_stages;
-  const int hbytes = p.npad * 128;                                  // one hidden chunk, 1 KB multiple
-  uint8_t* hring = wring + WS * kLmWChunk;                          // [stage][npad rows][128 B]
+  const int WS = p.w_stages, HS = p.h_stages, WB = p.wbox, HB = p.hbox;
+  const int wslot = WB * kLmWChunk;                                 // one weight copy: WB chunks
+  const int hchunk = p.npad * 128;                                  // one hidden chunk, 1 KB multiple
+  const int hslot = HB * hchunk;                                    // one hidden copy: HB chunks
+  uint8_t* wring = smem_raw + (((raw + 1023u) & ~1023u) - raw);     // [slot][chunk][128 rows][128 B]
+  uint8_t* hring = wring + WS * wslot;                              // [slot][chunk][npad rows][128 B]
   const uint32_t wring_u32 = smem_u32(wring), hring_u32 = smem_u32(hring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const LmWalk W = lm_walk(p);
@@ -215,6 +216,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
   };
 
+  // Copies per group of gk chunks: ceil(gk / box) (a last group shorter than the box reads
+  // chunks past d, which the copy fills with zeros and no MMA reads).
   if (warp == 0) {
     // ------------------------------------------------------------------ weight producer
     if (lane == 0 && W.ntiles > 0) {
@@ -224,13 +227,14 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       for (int p0 = 0; ok && p0 < W.ntiles; p0 += W.tpp) {
         const int nt = min(W.tpp, W.ntiles - p0);
         for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
-          const int gk = min(p.kgroup, W.nk - kg);
-          for (int i = 0; i < nt * gk; ++i, ++wc) {
-            const int t = i / gk, kc = kg + i % gk;
-            const int ws = wc % WS;
-            if (!mbar_wait_bounded(&wempty[ws], ((wc / WS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
-            mbar_arrive_expect_tx(&wfull[ws], (uint32_t)kLmWChunk);
-            lm_tma_load_2d(wring + ws * kLmWChunk, &tmW, &wfull[ws], kc * 64, (W.tile0 + p0 + t) * 128);
+          const int nb = (min(p.kgroup, W.nk - kg) + WB - 1) / WB;
+          for (int t = 0; ok && t < nt; ++t) {
+            for (int i = 0; i < nb; ++i, ++wc) {
+              const int ws = wc % WS;
+              if (!mbar_wait_bounded(&wempty[ws], ((wc / WS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
+              mbar_arrive_expect_tx(&wfull[ws], (uint32_t)wslot);
+              lm_tma_load_chunks(wring + ws * wslot, &tmW, &wfull[ws], (W.tile0 + p0 + t) * 128, kg + i * WB);
+            }
           }
         }
       }
@@ -246,11 +250,14 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       int hc = 0;
       bool ok = true;
       for (int ps = 0; ok && ps < npass; ++ps) {
-        for (int kc = 0; kc < W.nk; ++kc, ++hc) {
-          const int hs = hc % HS;
-          if (!mbar_wait_bounded(&hempty[hs], ((hc / HS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(&hfull[hs], (uint32_t)hbytes);
-          lm_tma_load_2d(hring + hs * hbytes, &tmH, &hfull[hs], kc * 64, 0);
+        for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
+          const int nb = (min(p.kgroup, W.nk - kg) + HB - 1) / HB;
+          for (int i = 0; i < nb; ++i, ++hc) {
+            const int hs = hc % HS;
+            if (!mbar_wait_bounded(&hempty[hs], ((hc / HS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
+            mbar_arrive_expect_tx(&hfull[hs], (uint32_t)hslot);
+            lm_tma_load_chunks(hring + hs * hslot, &tmH, &hfull[hs], 0, kg + i * HB);
+          }
         }
       }
       if (!ok) {
@@ -262,12 +269,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     // One thread issues every MMA, so its instruction stream between MMAs sets the MMA rate: ring
     // slots and phases advance incrementally and descriptors are precomputed (a K step of 16 is
-    // +2 in the descriptor's address field, a weight slot +1024, a hidden slot +hbytes / 16).
+    // +2 in the descriptor's address field, a weight chunk +1024, a hidden chunk +hchunk / 16).
     if (lane == 0 && W.ntiles > 0) {
       const uint32_t idesc = tc::idesc_bf16(128, p.npad, 0, 0);
       const uint64_t ad0 = tc::smem_desc(wring_u32, 16, 1024);
       const uint64_t bd0 = tc::smem_desc(hring_u32, 16, 1024);
-      const uint32_t hstep = (uint32_t)hbytes >> 4;
+      const uint32_t hstep = (uint32_t)hchunk >> 4;
       int ws = 0, hs = 0;
       uint32_t wph = 0, hph = 0;
       bool ok = true;
@@ -276,7 +283,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         if (ps > 0 && !mbar_wait_bounded(&acc_empty, (ps - 1) & 1, &s_abort)) { ok = false; break; }
         for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
           const int gk = min(p.kgroup, W.nk - kg);
-          for (int j = 0, s2 = hs, ph = hph; j < gk; ++j) {
+          const int nwb = (gk + WB - 1) / WB, nhb = (gk + HB - 1) / HB;
+          for (int j = 0, s2 = hs, ph = hph; j < nhb; ++j) {
             if (!mbar_wait_bounded(&hfull[s2], ph, &s_abort)) { ok = false; break; }
             if (++s2 == HS) { s2 = 0; ph ^= 1; }
           }
@@ -284,31 +292,31 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           tc::fence_after();
           uint32_t tacc = tmem;
           // tile by tile, each taking the group's gk chunks as one chain on its accumulator; the
-          // chain's weight slots are released together after it
+          // chain's weight copies are released together after it
           for (int t = 0; t < nt; ++t, tacc += (uint32_t)p.npad) {
-            for (int j = 0, s2 = ws, ph = wph; j < gk; ++j) {
+            for (int j = 0, s2 = ws, ph = wph; j < nwb; ++j) {
               if (!mbar_wait_bounded(&wfull[s2], ph, &s_abort)) { ok = false; break; }
               if (++s2 == WS) { s2 = 0; ph ^= 1; }
             }
             if (!ok) break;
             tc::fence_after();
-            for (int j = 0, sw = ws, sh = hs; j < gk; ++j) {
-              const uint64_t ad = ad0 + (uint64_t)(sw * (kLmWChunk >> 4));
-              const uint64_t bd = bd0 + (uint64_t)(sh * hstep);
+            for (int j = 0, sw = ws, cw = 0, sh = hs, ch = 0; j < gk; ++j) {
+              const uint64_t ad = ad0 + (uint64_t)(sw * (wslot >> 4) + cw * (kLmWChunk >> 4));
+              const uint64_t bd = bd0 + (uint64_t)(sh * (hslot >> 4) + ch * hstep);
               tc::mma_ss(tacc, ad, bd, idesc, (kg + j) ? 1u : 0u);
               tc::mma_ss(tacc, ad + 2, bd + 2, idesc, 1u);
               tc::mma_ss(tacc, ad + 4, bd + 4, idesc, 1u);
               tc::mma_ss(tacc, ad + 6, bd + 6, idesc, 1u);
-              if (++sw == WS) sw = 0;
-              if (++sh == HS) sh = 0;
+              if (++cw == WB) { cw = 0; if (++sw == WS) sw = 0; }
+              if (++ch == HB) { ch = 0; if (++sh == HS) sh = 0; }
             }
-            for (int j = 0; j < gk; ++j) {
+            for (int j = 0; j < nwb; ++j) {
               tc::commit(&wempty[ws]);
               if (++ws == WS) { ws = 0; wph ^= 1; }
             }
           }
           if (!ok) break;
-          for (int j = 0; j < gk; ++j) {
+          for (int j = 0; j < nhb; ++j) {
             tc::commit(&hempty[hs]);
             if (++hs == HS) { hs = 0; hph ^= 1; }
           }
@@ -350,9 +358,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             }
             const int nc = min(32, p.npad - cc * 32);
             if (vm < (uint32_t)p.V) {
-              for (int e = 0; e < nc; ++e) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
                 const int n = cc * 32 + e;
-                if (n < p.nrows) p.logits[(int64_t)n * p.V + vm] = __uint_as_float(u[e]);
+                if (e < nc && n < p.nrows) p.logits[(int64_t)n * p.V + vm] = __uint_as_float(u[e]);
               }
             }
           }
@@ -450,6 +459,15 @@ __global__ void __launch_bounds__(256) lmhead_finalize(const __grid_constant__ L
   p.out_nacc[b] = dd;
 }
 
+// The kernel's rings follow the parameters; they must be the layout's (the rings fit the
+// dynamic shared memory it sizes, and each ring holds at least the copies of one group).
+static bool lmhead_layout_matches(const LmLayout& L, const LmheadParams& p) {
+  return L.w_stages == p.w_stages && L.h_stages == p.h_stages && L.kgroup == p.kgroup && L.wbox == p.wbox &&
+         L.hbox == p.hbox && L.w_stages >= (L.kgroup + L.wbox - 1) / L.wbox &&
+         L.h_stages >= (L.kgroup + L.hbox - 1) / L.hbox && L.w_stages <= kLmWStagesMax &&
+         L.h_stages <= kLmHStagesMax;
+}
+
 size_t lmhead_workspace_bytes(int nrows) { return 256 + (size_t)nrows * sizeof(unsigned long long); }
 
 void lmhead_workspace_carve(void* ws, LmheadParams* p) {
@@ -463,29 +481,25 @@ cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const C
   // the status word and the keys (0 lies below every real key) in one memset
   cudaError_t e = cudaMemsetAsync(p.status, 0, lmhead_workspace_bytes(p.nrows), stream);
   if (e != cudaSuccess) return e;
-  int ws, hs, kg;
-  size_t smem;
-  lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
-  if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup) return cudaErrorInvalidValue;
+  const LmLayout L = lmhead_layout(p.npad);
+  if (!lmhead_layout_matches(L, p)) return cudaErrorInvalidValue;
   // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
   e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<false>), kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
   const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
-  lmhead_gemm<false><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  lmhead_gemm<false><<<grid, kLmThreads, L.smem, stream>>>(*tmW, *tmH, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_dependent(lmhead_finalize, dim3(p.B), dim3(256), 0, stream, 0u, p);
 }
 
 cudaError_t launch_lmhead_logits(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
                                  cudaStream_t stream) {
-  int ws, hs, kg;
-  size_t smem;
-  lmhead_layout(p.npad, &ws, &hs, &kg, &smem);
-  if (ws != p.w_stages || hs != p.h_stages || kg != p.kgroup || !p.logits) return cudaErrorInvalidValue;
+  const LmLayout L = lmhead_layout(p.npad);
+  if (!lmhead_layout_matches(L, p) || !p.logits) return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<true>), kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
   const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
-  lmhead_gemm<true><<<grid, kLmThreads, smem, stream>>>(*tmW, *tmH, p);
+  lmhead_gemm<true><<<grid, kLmThreads, L.smem, stream>>>(*tmW, *tmH, p);
   return cudaGetLastError();
 }
 

@@ -17,8 +17,9 @@ struct LmheadParams {
   int nrows, npad;        // B * R, padded to a multiple of 16
   int n_vtiles;           // ceil(V / 128)
   int tiles_per_pass;     // vocabulary tiles whose accumulators fit in TMEM together
-  int w_stages, h_stages; // ring depths (lmhead_layout)
+  int w_stages, h_stages; // ring depths in copies (lmhead_layout)
   int kgroup;             // K chunks a tile takes in a row (one accumulator chain of 4 kgroup MMAs)
+  int wbox, hbox;         // K chunks per weight / hidden-row copy (one 3-D tensor-map box)
   const int32_t* tok;     // draft tokens [B][gamma] (chain) or node tokens [B][N] (tree)
   int64_t tok_sb;
   int out_cols;
@@ -32,7 +33,11 @@ struct LmheadParams {
   int8_t depth[kLmMaxNodes];
 };
 
-void lmhead_layout(int npad, int* w_stages, int* h_stages, int* kgroup, size_t* smem);
+struct LmLayout {
+  int w_stages, h_stages, kgroup, wbox, hbox;
+  size_t smem;            // dynamic shared memory of the GEMM
+};
+LmLayout lmhead_layout(int npad);
 size_t lmhead_workspace_bytes(int nrows);
 void lmhead_workspace_carve(void* ws, LmheadParams* p);
 cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
