@@ -12,16 +12,16 @@
 // at once, so each 64-element chunk of the hidden rows is staged once per pass for all of them.
 // The weight is read exactly once; the run is HBM-bound, so shared memory goes to as deep a
 // weight ring as fits beside the hidden-row ring:
-//   warp 0     weight producer: each tile's 128 x 64 chunk into a ring of 16 KB stages.
+//   warp 0     weight producer: each tile's 128-row chunks into a ring of multi-chunk copies.
 //   warp 1     MMA issuer (one lane) and TMEM owner: 4 MMAs (K = 16) per weight chunk, a tile
 //              taking several K chunks in a row (one accumulator chain; see lmhead_layout).
-//   warps 2-5  epilogue: per 32-column block of the pass's accumulators (32 hidden rows x this
-//              warp's 32 vocabulary rows of every tile), each lane's maximum over the tiles, then
-//              two warp reductions per column (the maximum, then the smallest id reaching it;
-//              entries past V excluded) give one key per hidden row, kept in registers across
-//              passes; at the end the four warps' keys meet in shared memory and go to global
-//              memory with one 64-bit atomic max per row and CTA.
-//   warp 6     hidden-row producer: each pass's 64-column chunks into their own ring.
+//   warps 2-5, 7-10  epilogue, two warps per TMEM lane quadrant, taking alternate 32-column
+//              blocks of the pass's accumulators (32 hidden rows x the warp's 32 vocabulary rows
+//              of every tile): each lane's maximum over the tiles, then two warp reductions per
+//              column (the maximum, then the smallest id reaching it; entries past V excluded)
+//              give one key per hidden row, merged into the CTA's keys in shared memory; at the
+//              end one 64-bit atomic max per row and CTA into global memory.
+//   warp 6     hidden-row producer: each pass's K chunks into their own ring.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,7 +35,8 @@
 
 namespace specv {
 
-constexpr int kLmThreads = 224;
+constexpr int kLmThreads = 352;               // 11 warps: producers, issuer, 8 epilogue warps
+constexpr int kLmEpiWarps = 8;
 constexpr int kLmWChunk = 128 * 128;          // bytes: 128 vocabulary rows x 64 bf16
 constexpr int kLmSmemCap = 227 * 1024;        // dynamic shared memory of one CTA
 constexpr int kLmWStagesMax = 16;
@@ -49,16 +50,16 @@ constexpr int kLmHStagesMax = 8;
 // their number than by their size (about one per 0.3 us for 16-32 KB boxes), so 16 KB copies
 // alone would cap an SM near the HBM share it needs for the weight, and the hidden rows' copies
 // on top of those slow the weight stream down.  The hidden ring holds two groups (the one in use
-// and the next) in one copy each, or, above 192 rows, three one-chunk copies (a 64 KB group copy
-// would leave too little room for weight); the rest of shared memory is weight, two chunks per
-// copy.
+// and the next) in one copy each; the rest of shared memory is weight, two chunks per copy (at
+// 256 rows only two copies, which measured faster than three one-chunk hidden copies beside three
+// weight copies).
 LmLayout lmhead_layout(int npad) {
   LmLayout L;
   const size_t budget = kLmSmemCap - 1024 - 2560;  // alignment pad; static barriers and keys
   L.kgroup = npad <= 96 ? 4 : 2;
   L.wbox = 2;
-  L.hbox = npad <= 192 ? L.kgroup : 1;
-  L.h_stages = npad <= 192 ? 2 : 3;
+  L.hbox = L.kgroup;
+  L.h_stages = 2;
   const size_t hb = (size_t)npad * 128 * L.hbox, wb = (size_t)kLmWChunk * L.wbox;
   int ws = (int)((budget - L.h_stages * hb) / wb);
   L.w_stages = ws > kLmWStagesMax ? kLmWStagesMax : ws;
@@ -117,7 +118,7 @@ __device__ __forceinline__ uint32_t lm_ord(float v) {
 // columns can overlap instead of each waiting for the one before it.
 __device__ __forceinline__ uint32_t lm_redux_max(uint32_t x) { return __reduce_max_sync(0xffffffffu, x); }
 __device__ __forceinline__ uint32_t lm_redux_min(uint32_t x) { return __reduce_min_sync(0xffffffffu, x); }
-__device__ __forceinline__ void lm_epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void lm_epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kLmEpiWarps * 32) : "memory"); }
 
 // NC consecutive accumulator columns (hidden rows) starting at TMEM address `col0` of tile 0, over
 // the pass's nt tiles (tile t at column offset t * npad; this lane's vocabulary id vm0 + 128 t):
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       mbar_init(&hempty[i], 1);
     }
     mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, 4);
+    mbar_init(&acc_empty, kLmEpiWarps);
     mbar_init(&drain, 1);
     s_abort = 0;
     fence_mbar_init();
@@ -330,11 +331,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (warps 2-5)
+    // ------------------------------------------------------------------ epilogue (warps 2-5, 7-10)
     const int sub = warp & 3;           // TMEM lanes 32 sub .. 32 sub + 31 = vocabulary rows
-    unsigned long long kbest[kLmMaxRows / 32];   // lane's running key of hidden row 32 cc + lane
-#pragma unroll
-    for (int cc = 0; cc < kLmMaxRows / 32; ++cc) kbest[cc] = 0ull;
+    const int half = warp >= 7 ? 1 : 0; // the 32-column blocks this warp takes: half, half + 2, ...
+    const int eidx = (warp - 2 - half) * 32 + lane;   // 0 .. 255 over the epilogue threads
     for (int ps = 0; ps < npass; ++ps) {
       const int nt = min(W.tpp, W.ntiles - ps * W.tpp);
       const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full, ps & 1, &s_abort));
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       if constexpr (STORE) {
         for (int t = 0; t < nt; ++t) {
           const uint32_t vm = vm0 + 128u * (uint32_t)t;
-          for (int cc = 0; cc * 32 < p.npad; ++cc) {
+          for (int cc = half; cc * 32 < p.npad; cc += 2) {
             uint32_t u[32];
             if (cc * 32 + 32 <= p.npad) {
               tc::ld32(tb + (uint32_t)(t * p.npad + cc * 32), u);
@@ -367,17 +367,19 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
         }
       } else {
-#pragma unroll
-        for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
-          if (cc * 32 >= p.npad) break;
+        // one 32-column block at a time, not unrolled: the unrolled blocks made a straight run of
+        // tens of KB of code executed once per pass, whose instruction fetches set the pace; the
+        // block's keys go straight into the CTA's shared keys
+#pragma unroll 1
+        for (int cc = half; cc * 32 < p.npad; cc += 2) {
           uint32_t bo = 0, bi = 0xffffffffu;
           if (cc * 32 + 32 <= p.npad)
             lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
           else
             lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
-          const unsigned long long key =
-              bi < (uint32_t)p.V ? (((unsigned long long)bo << 32) | (uint32_t)~bi) : 0ull;
-          kbest[cc] = key > kbest[cc] ? key : kbest[cc];
+          const int row = cc * 32 + lane;
+          if (row < p.nrows && bi < (uint32_t)p.V)
+            atomicMax(&s_key[row], ((unsigned long long)bo << 32) | (uint32_t)~bi);
         }
       }
       tc::fence_before();
@@ -385,15 +387,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       if (lane == 0) mbar_arrive(&acc_empty);
     }
     if constexpr (!STORE) {
-      // the four warps' keys into the CTA's, then one global atomic per row
-#pragma unroll
-      for (int cc = 0; cc < kLmMaxRows / 32; ++cc) {
-        const int row = cc * 32 + lane;
-        if (row < p.nrows && kbest[cc] != 0ull) atomicMax(&s_key[row], kbest[cc]);
-      }
+      // the CTA's keys (the epilogue warps met in shared memory), one global atomic per row
       lm_epi_sync();
       unsigned long long* keys = reinterpret_cast<unsigned long long*>(p.rec);
-      for (int r = threadIdx.x - 64; r < p.nrows; r += 128)
+      for (int r = eidx; r < p.nrows; r += kLmEpiWarps * 32)
         if (s_key[r] != 0ull) atomicMax(&keys[r], s_key[r]);
     }
   }
