@@ -456,11 +456,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
           uint8_t* sK = stages + stage * 2 * TILE;
           uint8_t* sV = sK + TILE;
           mbar_arrive_expect_tx(&full[stage], 2u * TILE);
-#pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_4d(sK + h * (kKeyTile * 128), &tmK, &full[stage], h * 64, key0, g, b);
-            tma_load_4d(sV + h * (kKeyTile * 128), &tmV, &full[stage], h * 64, key0, g, b);
-          }
+          tma_load_kv(sK, &tmK, &full[stage], key0, g, b);
+          tma_load_kv(sV, &tmV, &full[stage], key0, g, b);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -531,11 +528,8 @@ __global__ void __launch_bounds__(kWinThreads, 2)
     uint8_t* sK = stages + s * 2 * TILE;
     uint64_t* bar = &full[t % kWinGroups][s];
     mbar_arrive_expect_tx(bar, 2u * TILE);
-#pragma unroll
-    for (int h = 0; h < D / 64; ++h) {
-      tma_load_4d(sK + h * (KT * 128), &tmK, bar, h * 64, t * KT, g, b);
-      tma_load_4d(sK + TILE + h * (KT * 128), &tmV, bar, h * 64, t * KT, g, b);
-    }
+    tma_load_kv(sK, &tmK, bar, t * KT, g, b);
+    tma_load_kv(sK + TILE, &tmV, bar, t * KT, g, b);
     s_last[s] = t;
   };
   // ---------------- every thread: the segment's length, the group's rows (padded to 16) and the

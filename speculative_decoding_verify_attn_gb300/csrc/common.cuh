@@ -202,20 +202,12 @@ __device__ __forceinline__ void tma_load_kv_hint(void* smem_dst, const void* tma
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(key0), "r"(g), "r"(b), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// The same load with an L2 eviction-priority policy (for data read exactly once, so that it does
-// not push out data that is read again soon).
+// An L2 eviction-priority policy for copies of data read exactly once, so that it does not push
+// out data that is read again soon.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
-}
-__device__ __forceinline__ void tma_load_4d_hint(void* smem_dst, const void* tmap, uint64_t* bar, int c0, int c1,
-                                                 int c2, int c3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
 }
 // Bulk prefetch of [gsrc, gsrc + bytes) into L2 (16-byte aligned address, bytes a multiple of 16).
 __device__ __forceinline__ void l2_prefetch_bulk(const void* gsrc, uint32_t bytes) {
