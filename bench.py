@@ -1206,8 +1206,8 @@ def main():
 
 # Revision tag of each verify kernel that profiles/roofline_counters.json was measured on; a
 # counter taken on another revision is not reported.
-KERNEL_REVS = {"magicdec-64k": "mma8w-kt128-v3", "llama3-70b-layer": "tc2wg-kt128-v2",
-               "llama3-8b-layer": "mma8w-kt128-v3", "medusa-tree-8k": "pair-kt64-v7"}
+KERNEL_REVS = {"magicdec-64k": "mma8w-kt128-v4", "llama3-70b-layer": "tc2wg-kt128-v3",
+               "llama3-8b-layer": "mma8w-kt128-v4", "medusa-tree-8k": "pair-kt64-v8"}
 
 if __name__ == "__main__":
     sys.exit(main())
