@@ -767,7 +767,11 @@ def time_e2e(runner, K, W, device):
     it issues the step's successor.  The copies of step k + 1 run on a second stream into the
     other of two device input buffers while step k computes, as a serving loop overlaps its input
     transfers with compute; the verify call appends the new K/V rows to the cache itself (k_new,
-    v_new, the fused append)."""
+    v_new, the fused append).  As a serving loop's decode step would be, the step's calls (draft
+    window x4, verify with append, spec_sample) are captured once per input buffer through the
+    binding into a CUDA graph and replayed each step (eager calls if capture is unavailable); the
+    copies, the waits and the read-back stay outside the graphs, every step.  Returns (seconds
+    per step, H2D bytes, D2H bytes, how the calls were issued)."""
     import torch
     cfg, inp, sv = runner.cfg, runner.inp, runner.sv
     B, nq = cfg.B, cfg.nq
@@ -783,7 +787,7 @@ def time_e2e(runner, K, W, device):
     nacc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * 4 + nacc_h.numel() * 4
-    comp = torch.cuda.current_stream(device)
+    comp = torch.cuda.Stream(device=device)
     copy_s = torch.cuda.Stream(device=device)
     ready = [torch.cuda.Event() for _ in range(2)]   # buffer i holds its step's inputs
     free = [torch.cuda.Event() for _ in range(2)]    # the step that read buffer i is done
@@ -797,9 +801,7 @@ def time_e2e(runner, K, W, device):
                 bufs[i][n].copy_(t, non_blocking=True)
             ready[i].record(copy_s)
 
-    def compute(k):
-        i = k % 2
-        comp.wait_event(ready[i])
+    def calls(i):
         b = bufs[i]
         for n in names:
             inp[n] = b[n]
@@ -808,10 +810,35 @@ def time_e2e(runner, K, W, device):
         sv.spec_verify_attn(inp["q"], inp["k"], inp["v"], inp["kv_len"], inp["o"], tree_parent=inp["tree"],
                             workspace=runner.ws_v, k_new=b["k_new"], v_new=b["v_new"])
         runner.sample()
-        free[i].record(comp)
-        out_h.copy_(inp["out"], non_blocking=True)
-        nacc_h.copy_(inp["nacc"], non_blocking=True)
-        done.record(comp)
+
+    graphs = None
+    try:
+        with torch.cuda.stream(comp):
+            for i in range(2):
+                calls(i)
+            comp.synchronize()
+            graphs = []
+            for i in range(2):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=comp, capture_error_mode="thread_local"):
+                    calls(i)
+                graphs.append(g)
+    except Exception:
+        graphs = None
+        torch.cuda.synchronize()
+
+    def compute(k):
+        i = k % 2
+        with torch.cuda.stream(comp):
+            comp.wait_event(ready[i])
+            if graphs is not None:
+                graphs[i].replay()
+            else:
+                calls(i)
+            free[i].record(comp)
+            out_h.copy_(inp["out"], non_blocking=True)
+            nacc_h.copy_(inp["nacc"], non_blocking=True)
+            done.record(comp)
 
     def run(n):
         copy_in(0)
@@ -830,7 +857,9 @@ def time_e2e(runner, K, W, device):
     torch.cuda.synchronize()
     sec = (time.perf_counter() - t0) / K
     inp.update(saved)
-    return sec, h2d, d2h
+    how = ("one CUDA graph per input buffer (the step's API calls captured once), replayed each step"
+           if graphs is not None else "eager calls through the binding")
+    return sec, h2d, d2h, how
 
 
 # ---------------------------------------------------------------------------- CPU oracle timing
@@ -1111,11 +1140,11 @@ def measure(cfg, args, pg, device, rank, world, full):
             rec["draft_window_cold_run"] = rot
         e2e = None
         if not args.no_e2e:
-            sec, h2d, d2h = time_e2e(runner, max(3, args.steps // 2), 3, device)
+            sec, h2d, d2h, how = time_e2e(runner, max(3, args.steps // 2), 3, device)
             sec = max_over_ranks(pg, sec, device)
             e2e = {"value": sum_over_ranks(pg, float(nb["verify_kv"]), device) / sec / 1e9, "unit": "GB/s",
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                   "ms_per_step": 1000 * sec, "rounds_per_s": world * cfg.B / sec}
+                   "ms_per_step": 1000 * sec, "rounds_per_s": world * cfg.B / sec, "launch": how}
         extra["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
         rec["sample_near_threshold"] = oracle_check_sampling(cfg, runner)

@@ -110,6 +110,22 @@ def test_chain_gamma_zero(sv):
     assert np.all(k == 0)
 
 
+def test_chain_many_tiles_per_cta(sv):
+    """230 vocabulary tiles (V = 29 435, a ragged last tile), d = 1024 (four K groups of four
+    chunks), 40 rows: more tiles than SMs, so CTAs take two tiles each in one pass."""
+    inp = gen.lmhead_inputs(8, 5, 1024, 29435, 312)
+    k = _chain(sv, inp, 4, 6)
+    assert k.max() >= 1
+
+
+def test_chain_many_tiles_several_passes(sv):
+    """600 vocabulary tiles (V = 76 797), d = 256 (two K groups), 160 rows: three tiles fill TMEM,
+    so a CTA's four tiles take two passes (the hidden rows staged once per pass)."""
+    inp = gen.lmhead_inputs(32, 5, 256, 76797, 313)
+    k = _chain(sv, inp, 4, 23)
+    assert k.max() >= 1
+
+
 def test_chain_256_rows(sv):
     """B * (gamma + 1) = 255 hidden rows: the widest accumulator (N = 256), two tiles per pass."""
     inp = gen.lmhead_inputs(51, 5, 64, 300, 303)
