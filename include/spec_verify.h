@@ -190,6 +190,9 @@ int spec_verify_attn_noalloc(const spec_attn_args* args, spec_stream_t stream);
  * NULL; o [B, Hq, D] (o_stride_b, o_stride_h); pos [B] int32 device.
  * Types and limits as spec_verify_attn (nq = 1); W >= 1; 0 <= n_sinks < W (else
  * SPEC_ERR_INVALID_ARG).
+ * Workspace: spec_draft_window_attn_workspace() bytes, status word at byte 0, cleared by the call.
+ *   For bf16 rings with up to 16 query rows per kv head the kernel clears it itself (no separate
+ *   memset on the stream) and tags workspace bytes 8-15 with its launch.
  * ---------------------------------------------------------------------------------------- */
 typedef struct spec_window_args {
   int32_t B, Hq, Hkv, D, W;

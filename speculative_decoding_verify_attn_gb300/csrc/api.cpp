@@ -78,6 +78,30 @@ bool encode_kv_map(CUtensorMap* m, const void* base, int D, int L, int Hkv, int 
   return r == CUDA_SUCCESS;
 }
 
+// K and V together, for the draft window kernel: (column, key, half of D, tensor, segment) over the
+// lower-addressed of the two rings, the fourth dimension stepping to the other ring; segment
+// s = b * Hkv + g (rings whose batch stride is Hkv head strides).  A box is one tile of both
+// tensors.  Returns false (the caller falls back to one map per tensor) when the rings are 2^40
+// bytes or more apart; *swap = 1 when V is the lower-addressed ring (a tile then lands V first).
+bool encode_kv_pair_map(CUtensorMap* m, const void* k, const void* v, int D, int L, int segs, int64_t stride_h,
+                        int box_keys, int* swap) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || k == v) return false;
+  const uintptr_t ka = reinterpret_cast<uintptr_t>(k), va = reinterpret_cast<uintptr_t>(v);
+  const uintptr_t lo = ka < va ? ka : va, dist = ka < va ? va - ka : ka - va;
+  if (dist >= (uintptr_t(1) << 40) || (dist % 16) != 0) return false;
+  cuuint64_t dims[5] = {64, (cuuint64_t)L, (cuuint64_t)D / 64, 2, (cuuint64_t)segs};
+  cuuint64_t strides[4] = {(cuuint64_t)D * 2, 128, (cuuint64_t)dist, (cuuint64_t)stride_h * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)box_keys, (cuuint32_t)D / 64, 2, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, reinterpret_cast<void*>(lo), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  *swap = va < ka ? 1 : 0;
+  return true;
+}
+
 // Q of the verify call as [B, nq, Hq, D] bf16 for the pair kernel: a box is one half of D (64
 // elements, 128-byte swizzle) of the G heads of one kv head over 128 / G consecutive positions,
 // i.e. 128 consecutive query rows of a row block in the kernel's row order.
@@ -324,9 +348,16 @@ int spec_draft_window_attn(const spec_window_args* a, spec_stream_t stream) {
   CUtensorMap tmK, tmV;
   if (bf16) {
     const int box = specv::window_tile_keys(p.rows, a->D, bf16);
-    if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box) ||
-        !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box))
+    // the small window kernel takes K and V of a tile in one copy when the rings' heads are
+    // contiguous over the batch (one segment index) and the two rings lie under 2^40 bytes apart
+    if (specv::window_uses_small_kernel(p.rows, a->D, bf16) && a->ring_stride_b == (int64_t)a->Hkv * a->ring_stride_h &&
+        encode_kv_pair_map(&tmK, a->k_ring, a->v_ring, a->D, a->W, a->B * a->Hkv, a->ring_stride_h, box, &p.kv_swap)) {
+      p.kv_pair = 1;
+      tmV = tmK;
+    } else if (!encode_kv_map(&tmK, a->k_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box) ||
+               !encode_kv_map(&tmV, a->v_ring, a->D, a->W, a->Hkv, a->B, a->ring_stride_h, a->ring_stride_b, box)) {
       return SPEC_ERR_CUDA;
+    }
   }
   cudaError_t e = specv::launch_attention(p, bf16 ? &tmK : nullptr, bf16 ? &tmV : nullptr, bf16, cs);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -523,13 +523,18 @@ __global__ void __launch_bounds__(kWinThreads, 2)
   uint8_t* sQ = stages + kWinStages * 2 * TILE;  // 16 rows x D bf16, 128-byte swizzle
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x, b = seg / p.Hkv, g = seg % p.Hkv;
+  if (seg == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);  // no memset before this launch
   auto issue = [&](int t) {  // one thread: tile t into stage t % kWinStages
     const int s = t % kWinStages;
-    uint8_t* sK = stages + s * 2 * TILE;
+    uint8_t* st = stages + s * 2 * TILE;
     uint64_t* bar = &full[t % kWinGroups][s];
     mbar_arrive_expect_tx(bar, 2u * TILE);
-    tma_load_kv(sK, &tmK, bar, t * KT, g, b);
-    tma_load_kv(sK + TILE, &tmV, bar, t * KT, g, b);
+    if (p.kv_pair) {
+      tma_load_kv_pair(st, &tmK, bar, t * KT, seg);
+    } else {
+      tma_load_kv(st, &tmK, bar, t * KT, g, b);
+      tma_load_kv(st + TILE, &tmV, bar, t * KT, g, b);
+    }
     s_last[s] = t;
   };
   // ---------------- every thread: the segment's length, the group's rows (padded to 16) and the
@@ -618,12 +623,12 @@ __global__ void __launch_bounds__(kWinThreads, 2)
     const int s = t % kWinStages;
     if (!mbar_wait_bounded(&full[grp][s], (t / (kWinGroups * kWinStages)) & 1, &s_abort)) {
       s_abort = 1;
-      if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+      if (lane == 0) status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
       bad = true;
       break;
     }
-    const uint8_t* sK = stages + s * 2 * TILE;
-    const uint8_t* sV = sK + TILE;
+    const uint8_t* sK = stages + s * 2 * TILE + (p.kv_swap ? TILE : 0);
+    const uint8_t* sV = stages + s * 2 * TILE + (p.kv_swap ? 0 : TILE);
     const int key0 = t * KT;
     // S = Q.K^T for this warp's 16 keys: two 8-key halves x two K-dimension halves, four
     // independent accumulator chains
@@ -755,7 +760,7 @@ __global__ void __launch_bounds__(kWinThreads, 2)
       const int tl = s_last[i];
       if (tl >= 0 && (tl >= ntiles || s_abort) && !mbar_wait_bounded(&full[tl % kWinGroups][i], (tl / (kWinGroups * kWinStages)) & 1, nullptr)) {
         s_abort = 1;
-        atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+        status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
       }
     }
   }
@@ -833,7 +838,7 @@ __global__ void __launch_bounds__(kWinThreads, 2)
       }
     }
   }
-  if (len == 0 && warp == 0 && lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
+  if (len == 0 && warp == 0 && lane == 0) status_report(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
 }
 
 // ------------------------------------------------------------------ fp32 partial kernel
@@ -1207,8 +1212,12 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   // bf16: one 288-thread CTA per SM (a 3-stage ring of 64 KB K+V stages); fp32: 2 per SM.
   const int per_sm = kv_bf16 ? 1 : 2;
   p.grid_x = sms * per_sm < kMaxGridX ? sms * per_sm : kMaxGridX;
-  e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
+  // the small draft window kernel clears the status word itself (a memset node before it would
+  // cost about a third of its time)
+  if (!(p.is_window && window_uses_small_kernel(p.rows, p.D, kv_bf16))) {
+    e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
+    if (e != cudaSuccess) return e;
+  }
   if (p.verify_append) {
     const int64_t rows = (int64_t)p.B * p.nq * p.Hkv;
     verify_append_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);

@@ -62,6 +62,8 @@ struct AttnParams {
   int verify_append;
   int64_t new_st;
   int debug_no_loads;              // test hook: the producers issue no K/V copies (waits run out)
+  int kv_pair;                     // draft window kernel: tmK maps K and V together (one copy per tile)
+  int kv_swap;                     //   ... with V at the lower address, so a tile lands V first
   int q_tma;                       // pair kernel: the first part's Q rows come by TMA (tmQ)
   unsigned long long anc[64];      // tree: bit m of anc[i] set iff node m is on i's root path
 };

@@ -164,6 +164,33 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ---------------------------------------------------------------- status word cleared in-kernel
+// For a launch that clears its status word itself instead of a memset before it (a memset node
+// costs a short launch several microseconds): CTA 0 clears word 0, then tags header bytes 8-15
+// with the launch's %gridid (unique per launch in the context).  A CTA with something to report
+// first waits (bounded; in practice never) until it sees its own launch's tag, so the clear can
+// never erase a report of the same launch.
+__device__ __forceinline__ unsigned long long launch_id() {
+  unsigned long long v;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(v));
+  return v;
+}
+__device__ __forceinline__ void status_clear_for_launch(uint32_t* status) {
+  *reinterpret_cast<volatile uint32_t*>(status) = 0u;
+  __threadfence();
+  *reinterpret_cast<volatile unsigned long long*>(status + 2) = launch_id();
+}
+__device__ __forceinline__ void status_report(uint32_t* status, uint32_t bits) {
+  const unsigned long long me = launch_id();
+  volatile unsigned long long* tag = reinterpret_cast<volatile unsigned long long*>(status + 2);
+  if (*tag != me) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (*tag != me && globaltimer_ns() - t0 < kWaitLimitNs) __nanosleep(256);
+  }
+  __threadfence();
+  atomicOr(status, bits);
+}
+
 // ---------------------------------------------------------------- TMA (tiled, 4-D, no multicast)
 // Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
 // completing `bytes` transactions on `bar`.
@@ -200,6 +227,16 @@ __device__ __forceinline__ void tma_load_kv_hint(void* smem_dst, const void* tma
       "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %2, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(key0), "r"(g), "r"(b), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// K and V tiles of one segment in one copy: a 5-D map (column, key, half of D, K-or-V, segment)
+// whose fourth dimension steps from one tensor to the other, so the box lands [tensor][half][key]
+// -- the two tiles one after the other, each as tma_load_kv lays it out.
+__device__ __forceinline__ void tma_load_kv_pair(void* smem_dst, const void* tmap, uint64_t* bar, int key0, int seg) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %2, %2, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(0), "r"(key0), "r"(seg), "r"(smem_u32(bar))
       : "memory");
 }
 // An L2 eviction-priority policy for copies of data read exactly once, so that it does not push
