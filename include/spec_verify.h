@@ -272,6 +272,9 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  *   sequence's vocabulary (a thread-block cluster) in the low byte, and bit 8 set when the draw
  *   re-reads the residual row from memory instead of scanning values kept on chip.  No result
  *   depends on it; tests read it to know which code path a shape exercised.
+ * Status: the status word at byte 0 of the workspace is cleared by the call; with V > 2048 (chain
+ *   and greedy modes) the first kernel clears it itself (no separate memset on the stream) and
+ *   tags workspace bytes 8-15 with its launch.
  * ---------------------------------------------------------------------------------------- */
 enum { SPEC_SAMPLE_CHAIN = 0, SPEC_SAMPLE_CHAIN_GREEDY = 1, SPEC_SAMPLE_TREE_GREEDY = 2, SPEC_SAMPLE_TREE = 3 };
 

@@ -259,6 +259,9 @@ constexpr int kWarps = kSampleThreads / 32;
 template <bool GREEDY>
 __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_constant__ SampleParams p) {
   pdl_launch_dependents();  // the finishing kernel may be scheduled as SMs free up
+  // the call's status word: cleared here, by CTA 0, unless the caller already cleared it (no memset
+  // node before this launch); the finishing kernels report only after waiting for this grid
+  if (!p.status_zeroed && blockIdx.x == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);
   constexpr int PER = kStatChunk / 128;  // float4 per lane per item
   extern __shared__ float4 s_ring[];     // [kStatWarps][kStatSlots][kStatChunk / 4]
   __shared__ uint64_t s_bar[kStatWarps][kStatSlots];
@@ -406,7 +409,10 @@ __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_
   if (!ok) {
     // a copy never completed: flag it, and wait (bounded) for the copies still in flight into
     // this warp's slots before the CTA can leave
-    if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+    if (lane == 0) {
+      if (p.status_zeroed) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+      else status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+    }
     const int done = (int)((it - (c_begin + warp)) / kStatWarps);
     for (int k = done; k < issued; ++k)
       mbar_wait_bounded(&bar[k % kStatSlots], (uint32_t)((k / kStatSlots) & 1), nullptr);
@@ -966,8 +972,7 @@ void sample_workspace_carve(void* ws, SampleParams* p) {
 
 static cudaError_t launch_large(const SampleParams& p, cudaStream_t stream) {
   const int rows = p.rows_t + p.rows_d;
-  cudaError_t e = p.status_zeroed ? cudaSuccess : cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;   // the statistics kernel clears the status word (no memset node)
   const long long items = (long long)p.schunks * rows * p.B;
   // persistent statistics grid: one CTA per SM (its shared-memory rings fill the SM)
   const long long need = (items + kStatWarps - 1) / kStatWarps;  // CTAs with at least a full set of items
