@@ -523,6 +523,10 @@ __global__ void __launch_bounds__(kWinThreads, 2)
   uint8_t* sQ = stages + kWinStages * 2 * TILE;  // 16 rows x D bf16, 128-byte swizzle
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x, b = seg / p.Hkv, g = seg % p.Hkv;
+  // programmatic dependent launch: the next kernel of the stream may be scheduled while this one
+  // runs, and this one starts while its predecessor finishes, touching no memory before the wait
+  pdl_launch_dependents();
+  pdl_wait();
   if (seg == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);  // no memset before this launch
   auto issue = [&](int t) {  // one thread: tile t into stage t % kWinStages
     const int s = t % kWinStages;
@@ -1193,8 +1197,7 @@ static cudaError_t launch_window_small(const AttnParams& p, const CUtensorMap* t
   auto kern = attn_window_bf16<D>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<p.B * p.Hkv, kWinThreads, smem, stream>>>(*tmK, *tmV, p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(p.B * p.Hkv), dim3(kWinThreads), smem, stream, 0u, *tmK, *tmV, p);
 }
 
 bool q_tma_possible(int D, int G, int nq) {
