@@ -137,7 +137,7 @@ __device__ __forceinline__ int combine_part(const AttnParams& p, float (&o)[D / 
           vr[lane + 32 * e] = vn[lane + 32 * e];
         }
       }
-      if (len == 0 && warp == 0 && lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
+      if (len == 0 && warp == 0 && lane == 0) status_report(p.status, (uint32_t)SPEC_STATUS_BAD_POS);
     }
     // ---- combine the rows this warp owns (slice weights relative to the row maximum, the new
     // key included; recomputed per pass to keep registers free)
@@ -255,7 +255,7 @@ __device__ void consumer_loop(const AttnParams& p, uint8_t* stages, uint8_t* sQ,
     for (int key0 = kb; key0 < ke; key0 += KT) {
       if (!mbar_wait_bounded(&full[stage], phase, s_abort)) {
         *s_abort = 1;
-        if (lane == 0) atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+        if (lane == 0) status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
         bad = 1;
         break;
       }
@@ -409,6 +409,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     attn_partial_bf16(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();  // the merge may be scheduled as SMs free up
+  // the call's status word is cleared here (no memset node before the call's first kernel)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);
   constexpr int TILE = kKeyTile * D * 2;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bars[2 * kStages];
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
         for (int key0 = kb; key0 < ke; key0 += kKeyTile) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, &s_abort)) {
             s_abort = 1;
-            atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+            status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
             ok = false;
             break;
           }
@@ -1215,9 +1217,9 @@ cudaError_t launch_attention(const AttnParams& p_in, const CUtensorMap* tmK, con
   // bf16: one 288-thread CTA per SM (a 3-stage ring of 64 KB K+V stages); fp32: 2 per SM.
   const int per_sm = kv_bf16 ? 1 : 2;
   p.grid_x = sms * per_sm < kMaxGridX ? sms * per_sm : kMaxGridX;
-  // the small draft window kernel clears the status word itself (a memset node before it would
-  // cost about a third of its time)
-  if (!(p.is_window && window_uses_small_kernel(p.rows, p.D, kv_bf16))) {
+  // bf16 K/V: the call's first attention kernel clears the status word itself (a memset node
+  // before a short call costs it several microseconds); fp32 K/V: a memset
+  if (!kv_bf16) {
     e = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), stream);
     if (e != cudaSuccess) return e;
   }

@@ -92,6 +92,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     attn_partial_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();  // the merge may be scheduled as SMs free up
+  // the call's status word is cleared here (no memset node before the call's first kernel)
+  if (blockIdx.x == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kTcStages], empty[kTcStages];
   __shared__ uint64_t sfull[kTcSlices], pfull[kTcSlices], pvdone[kTcSlices], ofree[kTcSlices];
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   auto fail = [&]() {
     s_abort = 1;
-    atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+    status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
   };
 
   if (warp == 0) {

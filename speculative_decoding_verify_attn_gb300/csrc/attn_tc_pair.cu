@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     attn_partial_tc_pair(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ AttnParams p) {
   pdl_launch_dependents();  // the merge may be scheduled as SMs free up
+  // the call's status word is cleared here (no memset node before the call's first kernel)
+  if (blockIdx.x == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kPStages], empty[kPStages];
   __shared__ uint64_t sfull[2][2], pfull[2][2], pvdone[2][2], ofree[2], qfull[2], drain[2];
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
   auto fail = [&]() {
     s_abort = 1;
-    atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
+    status_report(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
   };
 
   if (warp == 0) {
