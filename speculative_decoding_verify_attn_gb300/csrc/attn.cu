@@ -528,6 +528,15 @@ __global__ void __launch_bounds__(kWinThreads, 2)
   // programmatic dependent launch: the next kernel of the stream may be scheduled while this one
   // runs, and this one starts while its predecessor finishes, touching no memory before the wait
   pdl_launch_dependents();
+  if (threadIdx.x == kWinThreads - 32 && !p.debug_no_loads) {
+    // while the previous kernel of the stream finishes: the segment's first tiles into L2 (a
+    // prefetch may see data the previous kernel is still writing; the copies after the wait
+    // read L2, which then holds the written values)
+    const int pre = min(kWinStages, (p.Lmax + KT - 1) / KT);
+    const size_t off = ((size_t)b * p.kv_sb + (size_t)g * p.kv_sh) * 2;
+    l2_prefetch_bulk(static_cast<const uint8_t*>(p.k) + off, (uint32_t)(pre * KT * D * 2));
+    l2_prefetch_bulk(static_cast<const uint8_t*>(p.v) + off, (uint32_t)(pre * KT * D * 2));
+  }
   pdl_wait();
   if (seg == 0 && threadIdx.x == 0) status_clear_for_launch(p.status);  // no memset before this launch
   auto issue = [&](int t) {  // one thread: tile t into stage t % kWinStages
