@@ -534,16 +534,16 @@ int spec_lmhead_sample(const spec_lmhead_args* a, spec_stream_t stream) {
   p.nrows = a->B * R;
   p.npad = (p.nrows + 15) / 16 * 16;
   p.n_vtiles = (a->V + 127) / 128;
-  const specv::LmLayout lay = specv::lmhead_layout(p.npad, p.n_vtiles);
+  p.tiles_per_pass = 512 / p.npad;
+  const specv::LmLayout lay = specv::lmhead_layout(p.npad);
   p.w_stages = lay.w_stages; p.h_stages = lay.h_stages; p.kgroup = lay.kgroup;
-  p.wbox = lay.wbox; p.hbox = lay.hbox; p.pair = lay.pair;
-  p.tiles_per_pass = specv::lmhead_tiles_per_pass(lay, p.npad);
+  p.wbox = lay.wbox; p.hbox = lay.hbox;
   p.tok = a->draft_tokens; p.tok_sb = a->tok_stride_b;
   p.out_cols = a->out_cols; p.out_tok = a->out_tokens; p.out_nacc = a->out_num_accepted; p.out_nodes = a->out_path_nodes;
   specv::lmhead_workspace_carve(a->workspace, &p);
   CUtensorMap tmW, tmH;
   if (!encode_chunk_map(&tmW, a->weight, a->d, a->V, 128, p.wbox) ||
-      !encode_chunk_map(&tmH, a->hidden, a->d, p.nrows, specv::lmhead_hidden_box_rows(lay, p.npad), p.hbox))
+      !encode_chunk_map(&tmH, a->hidden, a->d, p.nrows, p.npad, p.hbox))
     return SPEC_ERR_CUDA;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (!stochastic) {

@@ -164,29 +164,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// ---------------------------------------------------------------- thread-block cluster
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// All threads of every CTA of the cluster (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Store a 32-bit value at `dst`'s offset in the shared memory of cluster CTA `rank`.
-__device__ __forceinline__ void st_remote_u32(uint32_t* dst, uint32_t rank, uint32_t v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(dst)), "r"(rank));
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
-}
-// Arrive once on the mbarrier at `bar`'s offset in the shared memory of cluster CTA `rank`.
-__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-}
-
 // ---------------------------------------------------------------- status word cleared in-kernel
 // For a launch that clears its status word itself instead of a memset before it (a memset node
 // costs a short launch several microseconds): CTA 0 clears word 0, then tags header bytes 8-15

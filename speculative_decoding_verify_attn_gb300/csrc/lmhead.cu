@@ -37,14 +37,8 @@ namespace specv {
 
 constexpr int kLmThreads = 352;               // 11 warps: producers, issuer, 8 epilogue warps
 constexpr int kLmEpiWarps = 8;
-// Hidden rows (padded) from which the pair-CTA form is used: there the hidden rows are as many
-// bytes per K chunk as one weight tile's or more, and staging half of them per SM pays.
-constexpr int kLmPairMinRows = 128;
-// TMEM columns of the pair form's allocation (in both CTAs of the pair)
-constexpr int kLmPairTmemCols = 512;
 constexpr int kLmWChunk = 128 * 128;          // bytes: 128 vocabulary rows x 64 bf16
-constexpr int kLmSmemCap = 227 * 1024;        // shared memory of one CTA
-constexpr int kLmStaticSmem = 3072;          // reserved for the kernel's static shared memory (barriers, keys)
+constexpr int kLmSmemCap = 227 * 1024;        // dynamic shared memory of one CTA
 constexpr int kLmWStagesMax = 16;
 constexpr int kLmHStagesMax = 8;
 
@@ -59,17 +53,14 @@ constexpr int kLmHStagesMax = 8;
 // and the next) in one copy each; the rest of shared memory is weight, two chunks per copy (at
 // 256 rows only two copies, which measured faster than three one-chunk hidden copies beside three
 // weight copies).
-int lmhead_tiles_per_pass(const LmLayout& L, int npad) { return (L.pair ? kLmPairTmemCols : 512) / npad; }
-
-LmLayout lmhead_layout(int npad, int n_vtiles) {
+LmLayout lmhead_layout(int npad) {
   LmLayout L;
-  const size_t budget = kLmSmemCap - 1024 - kLmStaticSmem;  // alignment pad; static barriers and keys
-  L.pair = (npad >= kLmPairMinRows && n_vtiles >= 2) ? 1 : 0;
+  const size_t budget = kLmSmemCap - 1024 - 2560;  // alignment pad; static barriers and keys
   L.kgroup = npad <= 96 ? 4 : 2;
   L.wbox = 2;
   L.hbox = L.kgroup;
   L.h_stages = 2;
-  const size_t hb = (size_t)lmhead_hidden_box_rows(L, npad) * 128 * L.hbox, wb = (size_t)kLmWChunk * L.wbox;
+  const size_t hb = (size_t)npad * 128 * L.hbox, wb = (size_t)kLmWChunk * L.wbox;
   int ws = (int)((budget - L.h_stages * hb) / wb);
   L.w_stages = ws > kLmWStagesMax ? kLmWStagesMax : ws;
   L.smem = 1024 + (size_t)L.w_stages * wb + (size_t)L.h_stages * hb;
@@ -81,20 +72,14 @@ __device__ __forceinline__ int lm_key_id(unsigned long long k) { return (int)(~(
 
 // The steps of a CTA's run of vocabulary tiles: passes of up to `tpp` tiles; per pass, per group
 // of kgroup K chunks, per tile of the pass, the group's weight chunks of that tile.
-// PAIR: the units are pairs of tiles and a cluster of two CTAs owns a run of them (tile0 and
-// ntiles count pairs; the CTA of cluster rank r takes tile 2u + r of pair u).
 struct LmWalk {
   int tile0, ntiles, tpp, nk;
 };
-template <bool PAIR>
 __device__ __forceinline__ LmWalk lm_walk(const LmheadParams& p) {
   LmWalk w;
-  const int units = PAIR ? (p.n_vtiles + 1) / 2 : p.n_vtiles;
-  const int owners = PAIR ? (int)gridDim.x / 2 : (int)gridDim.x;
-  const int owner = PAIR ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-  const int per = (units + owners - 1) / owners;
-  w.tile0 = min(owner * per, units);
-  w.ntiles = min(per, units - w.tile0);
+  const int per = (p.n_vtiles + gridDim.x - 1) / gridDim.x;
+  w.tile0 = min((int)blockIdx.x * per, p.n_vtiles);
+  w.ntiles = min(per, p.n_vtiles - w.tile0);
   w.tpp = p.tiles_per_pass;
   w.nk = p.d / 64;
   return w;
@@ -141,8 +126,8 @@ __device__ __forceinline__ void lm_epi_sync() { asm volatile("bar.sync 1, %0;" :
 // smaller id; ids >= V excluded), then per column the warp's maximum and the smallest id reaching
 // it.  Lane e keeps column e's pair in (bo, bi).
 template <int NC>
-__device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt, uint32_t vm0, uint32_t vstep,
-                                                uint32_t V, int lane, uint32_t& bo, uint32_t& bi) {
+__device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt, uint32_t vm0, uint32_t V, int lane,
+                                                uint32_t& bo, uint32_t& bi) {
   uint32_t o[NC], ix[NC];
 #pragma unroll
   for (int e = 0; e < NC; ++e) {
@@ -157,7 +142,7 @@ __device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt,
     } else {
       lm_ld16(col0 + (uint32_t)(t * npad), *reinterpret_cast<uint32_t(*)[16]>(u));
     }
-    const uint32_t vm = vm0 + vstep * (uint32_t)t;
+    const uint32_t vm = vm0 + 128u * (uint32_t)t;
     const bool valid = vm < V;
 #pragma unroll
     for (int e = 0; e < NC; ++e) {
@@ -184,79 +169,47 @@ __device__ __forceinline__ void lm_reduce_tiles(uint32_t col0, int npad, int nt,
 // STORE: write the fp32 logits [nrows][V] instead of reducing them to argmax keys (stochastic
 // modes); for a fixed hidden row a warp's 32 lanes hold 32 consecutive vocabulary rows, so each
 // column of a TMEM load is one 128-byte store.
-// PAIR: a cluster of two CTAs shares each pair of vocabulary tiles (the even CTA's tile 2u, the
-// odd CTA's tile 2u + 1): the even CTA issues M = 256 pair MMAs (cta_group::2) for both, each CTA
-// staging its own tile's weight rows and half of the hidden rows (N / 2; the tensor core pairs
-// the halves), so an SM stages half the hidden-row bytes and the MMA count per weight byte halves.
-// The odd CTA forwards the completion of each of its copies to the even CTA's barriers (remote
-// mbarrier arrives); the even CTA's MMA commits free the ring slots and report finished
-// accumulators in both CTAs (multicast); each CTA's epilogue reads its own tensor memory, and the
-// odd CTA's epilogue warps report a drained pass to the even CTA.
-template <bool STORE, bool PAIR>
+template <bool STORE>
 __global__ void __launch_bounds__(kLmThreads, 1)
     lmhead_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                 const __grid_constant__ LmheadParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t wfull[kLmWStagesMax], wempty[kLmWStagesMax], hfull[kLmHStagesMax], hempty[kLmHStagesMax];
-  __shared__ uint64_t pwfull[PAIR ? kLmWStagesMax : 1], phfull[PAIR ? kLmHStagesMax : 1];  // the odd CTA's copies
   __shared__ uint64_t acc_full, acc_empty, drain;
-  __shared__ uint32_t tmem_base, s_peer_base;
+  __shared__ uint32_t tmem_base;
   __shared__ int s_abort;
   __shared__ unsigned long long s_key[kLmMaxRows];   // this CTA's running key per hidden row
   const uint32_t raw = smem_u32(smem_raw);
   const int WS = p.w_stages, HS = p.h_stages, WB = p.wbox, HB = p.hbox;
-  const int hrows = PAIR ? p.npad / 2 : p.npad;                     // hidden rows this CTA stages
   const int wslot = WB * kLmWChunk;                                 // one weight copy: WB chunks
-  const int hchunk = hrows * 128;                                   // one hidden chunk, 1 KB multiple
+  const int hchunk = p.npad * 128;                                  // one hidden chunk, 1 KB multiple
   const int hslot = HB * hchunk;                                    // one hidden copy: HB chunks
   uint8_t* wring = smem_raw + (((raw + 1023u) & ~1023u) - raw);     // [slot][chunk][128 rows][128 B]
-  uint8_t* hring = wring + WS * wslot;                              // [slot][chunk][hrows][128 B]
+  uint8_t* hring = wring + WS * wslot;                              // [slot][chunk][npad rows][128 B]
   const uint32_t wring_u32 = smem_u32(wring), hring_u32 = smem_u32(hring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_rank() : 0u;
-  const bool leader = rank == 0;
-  const LmWalk W = lm_walk<PAIR>(p);
+  const LmWalk W = lm_walk(p);
   const int npass = (W.ntiles + W.tpp - 1) / W.tpp;
-  // vocabulary tile of the CTA's local tile t (pair: every other tile, from the CTA's rank)
-  auto vtile = [&](int t) { return PAIR ? 2 * (W.tile0 + t) + (int)rank : W.tile0 + t; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < WS; ++i) {
       mbar_init(&wfull[i], 1);
       mbar_init(&wempty[i], 1);
-      if constexpr (PAIR) mbar_init(&pwfull[i], 1);
     }
     for (int i = 0; i < HS; ++i) {
       mbar_init(&hfull[i], 1);
       mbar_init(&hempty[i], 1);
-      if constexpr (PAIR) mbar_init(&phfull[i], 1);
     }
     mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, PAIR ? 2 * kLmEpiWarps : kLmEpiWarps);
+    mbar_init(&acc_empty, kLmEpiWarps);
     mbar_init(&drain, 1);
     s_abort = 0;
     fence_mbar_init();
   }
   for (int r = threadIdx.x; r < kLmMaxRows; r += blockDim.x) s_key[r] = 0ull;
-  if (warp == 1) {
-    if constexpr (PAIR) tc::alloc_pair(&tmem_base, kLmPairTmemCols);
-    else tc::alloc(&tmem_base, 512);
-  }
+  if (warp == 1) tc::alloc(&tmem_base, 512);
   tc::fence_before();
-  if constexpr (PAIR) {
-    cluster_sync_all();   // both CTAs' barriers initialised (before any remote arrive) and TMEM allocated
-    // the pair's accumulators live at the same TMEM address in both CTAs: checked, so that a
-    // mismatch ends the call with a status instead of wrong results
-    if (!leader && threadIdx.x == 0) st_remote_u32(&s_peer_base, 0u, tmem_base);
-    cluster_sync_all();
-    if (leader && threadIdx.x == 0 && s_peer_base != tmem_base) {
-      s_abort = 1;
-      atomicOr(p.status, (uint32_t)SPEC_STATUS_TIMEOUT);
-    }
-    __syncthreads();
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   tc::fence_after();
   const uint32_t tmem = tmem_base;
   auto fail = [&]() {
@@ -281,7 +234,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               const int ws = wc % WS;
               if (!mbar_wait_bounded(&wempty[ws], ((wc / WS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
               mbar_arrive_expect_tx(&wfull[ws], (uint32_t)wslot);
-              lm_tma_load_chunks(wring + ws * wslot, &tmW, &wfull[ws], vtile(p0 + t) * 128, kg + i * WB);
+              lm_tma_load_chunks(wring + ws * wslot, &tmW, &wfull[ws], (W.tile0 + p0 + t) * 128, kg + i * WB);
             }
           }
         }
@@ -304,7 +257,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const int hs = hc % HS;
             if (!mbar_wait_bounded(&hempty[hs], ((hc / HS) & 1) ^ 1u, &s_abort)) { ok = false; break; }
             mbar_arrive_expect_tx(&hfull[hs], (uint32_t)hslot);
-            lm_tma_load_chunks(hring + hs * hslot, &tmH, &hfull[hs], (int)rank * hrows, kg + i * HB);
+            lm_tma_load_chunks(hring + hs * hslot, &tmH, &hfull[hs], 0, kg + i * HB);
           }
         }
       }
@@ -313,13 +266,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         for (int i = 1; i <= min(hc, HS); ++i) mbar_wait_bounded(&hfull[(hc - i) % HS], ((hc - i) / HS) & 1, nullptr);
       }
     }
-  } else if (warp == 1 && (!PAIR || leader)) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // One thread issues every MMA, so its instruction stream between MMAs sets the MMA rate: ring
     // slots and phases advance incrementally and descriptors are precomputed (a K step of 16 is
     // +2 in the descriptor's address field, a weight chunk +1024, a hidden chunk +hchunk / 16).
-    if (lane == 0 && W.ntiles > 0 && !s_abort) {
-      const uint32_t idesc = tc::idesc_bf16(PAIR ? 256 : 128, p.npad, 0, 0);
+    if (lane == 0 && W.ntiles > 0) {
+      const uint32_t idesc = tc::idesc_bf16(128, p.npad, 0, 0);
       const uint64_t ad0 = tc::smem_desc(wring_u32, 16, 1024);
       const uint64_t bd0 = tc::smem_desc(hring_u32, 16, 1024);
       const uint32_t hstep = (uint32_t)hchunk >> 4;
@@ -334,7 +287,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           const int nwb = (gk + WB - 1) / WB, nhb = (gk + HB - 1) / HB;
           for (int j = 0, s2 = hs, ph = hph; j < nhb; ++j) {
             if (!mbar_wait_bounded(&hfull[s2], ph, &s_abort)) { ok = false; break; }
-            if (PAIR && !mbar_wait_bounded(&phfull[s2], ph, &s_abort)) { ok = false; break; }
             if (++s2 == HS) { s2 = 0; ph ^= 1; }
           }
           if (!ok) break;
@@ -345,7 +297,6 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           for (int t = 0; t < nt; ++t, tacc += (uint32_t)p.npad) {
             for (int j = 0, s2 = ws, ph = wph; j < nwb; ++j) {
               if (!mbar_wait_bounded(&wfull[s2], ph, &s_abort)) { ok = false; break; }
-              if (PAIR && !mbar_wait_bounded(&pwfull[s2], ph, &s_abort)) { ok = false; break; }
               if (++s2 == WS) { s2 = 0; ph ^= 1; }
             }
             if (!ok) break;
@@ -353,72 +304,31 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             for (int j = 0, sw = ws, cw = 0, sh = hs, ch = 0; j < gk; ++j) {
               const uint64_t ad = ad0 + (uint64_t)(sw * (wslot >> 4) + cw * (kLmWChunk >> 4));
               const uint64_t bd = bd0 + (uint64_t)(sh * (hslot >> 4) + ch * hstep);
-              const uint32_t acc0 = (kg + j) ? 1u : 0u;
-              if constexpr (PAIR) {
-                tc::mma_ss_pair(tacc, ad, bd, idesc, acc0);
-                tc::mma_ss_pair(tacc, ad + 2, bd + 2, idesc, 1u);
-                tc::mma_ss_pair(tacc, ad + 4, bd + 4, idesc, 1u);
-                tc::mma_ss_pair(tacc, ad + 6, bd + 6, idesc, 1u);
-              } else {
-                tc::mma_ss(tacc, ad, bd, idesc, acc0);
-                tc::mma_ss(tacc, ad + 2, bd + 2, idesc, 1u);
-                tc::mma_ss(tacc, ad + 4, bd + 4, idesc, 1u);
-                tc::mma_ss(tacc, ad + 6, bd + 6, idesc, 1u);
-              }
+              tc::mma_ss(tacc, ad, bd, idesc, (kg + j) ? 1u : 0u);
+              tc::mma_ss(tacc, ad + 2, bd + 2, idesc, 1u);
+              tc::mma_ss(tacc, ad + 4, bd + 4, idesc, 1u);
+              tc::mma_ss(tacc, ad + 6, bd + 6, idesc, 1u);
               if (++cw == WB) { cw = 0; if (++sw == WS) sw = 0; }
               if (++ch == HB) { ch = 0; if (++sh == HS) sh = 0; }
             }
             for (int j = 0; j < nwb; ++j) {
-              if constexpr (PAIR) tc::commit_pair_mc(&wempty[ws], (uint16_t)3);
-              else tc::commit(&wempty[ws]);
+              tc::commit(&wempty[ws]);
               if (++ws == WS) { ws = 0; wph ^= 1; }
             }
           }
           if (!ok) break;
           for (int j = 0; j < nhb; ++j) {
-            if constexpr (PAIR) tc::commit_pair_mc(&hempty[hs], (uint16_t)3);
-            else tc::commit(&hempty[hs]);
+            tc::commit(&hempty[hs]);
             if (++hs == HS) { hs = 0; hph ^= 1; }
           }
         }
-        if (ok) {
-          if constexpr (PAIR) tc::commit_pair_mc(&acc_full, (uint16_t)3);
-          else tc::commit(&acc_full);
-        }
+        if (ok) tc::commit(&acc_full);
       }
-      if (!ok) fail();
-      // every MMA and every commit of this thread complete before the CTA (and its pair) leaves
-      if constexpr (PAIR) tc::commit_pair(&drain);
-      else tc::commit(&drain);
-      mbar_wait_bounded(&drain, 0, nullptr);
-    }
-  } else if (PAIR && warp == 1) {
-    // ------------------------------------------------------------------ odd CTA: copy forwarder
-    // The even CTA's MMAs read this CTA's weight rows and hidden-row half: each completed copy is
-    // reported to the barrier of the same slot in the even CTA, in the order the issuer waits.
-    if (lane == 0 && W.ntiles > 0) {
-      int ws = 0, hs = 0;
-      uint32_t wph = 0, hph = 0;
-      bool ok = true;
-      for (int ps = 0; ok && ps < npass; ++ps) {
-        const int nt = min(W.tpp, W.ntiles - ps * W.tpp);
-        for (int kg = 0; ok && kg < W.nk; kg += p.kgroup) {
-          const int gk = min(p.kgroup, W.nk - kg);
-          const int nwb = (gk + WB - 1) / WB, nhb = (gk + HB - 1) / HB;
-          for (int j = 0; ok && j < nhb; ++j) {
-            if (!mbar_wait_bounded(&hfull[hs], hph, &s_abort)) { ok = false; break; }
-            mbar_arrive_remote(&phfull[hs], 0u);
-            if (++hs == HS) { hs = 0; hph ^= 1; }
-          }
-          for (int t = 0; ok && t < nt; ++t)
-            for (int j = 0; ok && j < nwb; ++j) {
-              if (!mbar_wait_bounded(&wfull[ws], wph, &s_abort)) { ok = false; break; }
-              mbar_arrive_remote(&pwfull[ws], 0u);
-              if (++ws == WS) { ws = 0; wph ^= 1; }
-            }
-        }
+      if (!ok) {
+        fail();
+        tc::commit(&drain);
+        mbar_wait_bounded(&drain, 0, nullptr);
       }
-      if (!ok) fail();
     }
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2-5, 7-10)
@@ -433,13 +343,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tc::fence_after();
-      // the pass's first tile's vocabulary id of this lane; consecutive local tiles are `vstep` apart
-      const uint32_t vm0 = (uint32_t)(vtile(ps * W.tpp) * 128 + sub * 32 + lane);
-      const uint32_t vstep = PAIR ? 256u : 128u;
+      const uint32_t vm0 = (uint32_t)((W.tile0 + ps * W.tpp) * 128 + sub * 32 + lane);  // tile 0's vocabulary id
       const uint32_t tb = tmem + ((uint32_t)(sub * 32) << 16);
       if constexpr (STORE) {
         for (int t = 0; t < nt; ++t) {
-          const uint32_t vm = vm0 + vstep * (uint32_t)t;
+          const uint32_t vm = vm0 + 128u * (uint32_t)t;
           for (int cc = half; cc * 32 < p.npad; cc += 2) {
             uint32_t u[32];
             if (cc * 32 + 32 <= p.npad) {
@@ -466,9 +374,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         for (int cc = half; cc * 32 < p.npad; cc += 2) {
           uint32_t bo = 0, bi = 0xffffffffu;
           if (cc * 32 + 32 <= p.npad)
-            lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, vstep, (uint32_t)p.V, lane, bo, bi);
+            lm_reduce_tiles<32>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
           else
-            lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, vstep, (uint32_t)p.V, lane, bo, bi);
+            lm_reduce_tiles<16>(tb + cc * 32, p.npad, nt, vm0, (uint32_t)p.V, lane, bo, bi);
           const int row = cc * 32 + lane;
           if (row < p.nrows && bi < (uint32_t)p.V)
             atomicMax(&s_key[row], ((unsigned long long)bo << 32) | (uint32_t)~bi);
@@ -476,10 +384,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if (PAIR && !leader) mbar_arrive_remote(&acc_empty, 0u);   // the even CTA issues the next pass
-        else mbar_arrive(&acc_empty);
-      }
+      if (lane == 0) mbar_arrive(&acc_empty);
     }
     if constexpr (!STORE) {
       // the CTA's keys (the epilogue warps met in shared memory), one global atomic per row
@@ -490,18 +395,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     }
   }
   tc::fence_before();
-  if constexpr (PAIR) {
-    // no CTA of the pair leaves while the other may still arrive on its barriers, and the pair's
-    // tensor memory is released by both once every MMA has completed
-    cluster_sync_all();
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc::fence_after();
-    if constexpr (PAIR) tc::dealloc_pair(tmem, kLmPairTmemCols);
-    else tc::dealloc(tmem, 512);
+    tc::dealloc(tmem, 512);
   }
 }
 
@@ -562,7 +460,7 @@ __global__ void __launch_bounds__(256) lmhead_finalize(const __grid_constant__ L
 // dynamic shared memory it sizes, and each ring holds at least the copies of one group).
 static bool lmhead_layout_matches(const LmLayout& L, const LmheadParams& p) {
   return L.w_stages == p.w_stages && L.h_stages == p.h_stages && L.kgroup == p.kgroup && L.wbox == p.wbox &&
-         L.hbox == p.hbox && L.pair == p.pair && L.w_stages >= (L.kgroup + L.wbox - 1) / L.wbox &&
+         L.hbox == p.hbox && L.w_stages >= (L.kgroup + L.wbox - 1) / L.wbox &&
          L.h_stages >= (L.kgroup + L.hbox - 1) / L.hbox && L.w_stages <= kLmWStagesMax &&
          L.h_stages <= kLmHStagesMax;
 }
@@ -575,67 +473,31 @@ void lmhead_workspace_carve(void* ws, LmheadParams* p) {
   p->rec = b + 256;
 }
 
-// The GEMM launch: one CTA per SM (at most one per tile), or clusters of two CTAs sharing pairs of
-// tiles in the pair form.  Not a programmatic dependent: the kernel reads its inputs at once.
-template <bool STORE>
-static cudaError_t launch_gemm(const LmheadParams& p, const LmLayout& L, const CUtensorMap* tmW,
-                               const CUtensorMap* tmH, int num_sms, cudaStream_t stream) {
-  if (!lmhead_layout_matches(L, p)) return cudaErrorInvalidValue;
-  if (!L.pair) {
-    // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<STORE, false>), kLmSmemCap - kLmStaticSmem);
-    if (e != cudaSuccess) return e;
-    const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
-    lmhead_gemm<STORE, false><<<grid, kLmThreads, L.smem, stream>>>(*tmW, *tmH, p);
-    return cudaGetLastError();
-  }
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<STORE, true>), kLmSmemCap - kLmStaticSmem);
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return e;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kLmThreads, 1, 1);
-  cfg.dynamicSmemBytes = L.smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // as many pairs as can be resident at once (one wave), at most one per pair of tiles
-  const int units = (p.n_vtiles + 1) / 2;
-  int pairs = num_sms / 2;
-  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  int active = 0;
-  if (max_active_clusters(&active, reinterpret_cast<const void*>(lmhead_gemm<STORE, true>), &cfg) == cudaSuccess &&
-      active > 0 && active < pairs)
-    pairs = active;
-  (void)cudaGetLastError();
-  if (units < pairs) pairs = units;
-  if (pairs < 1) return cudaErrorInvalidValue;
-  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, lmhead_gemm<STORE, true>, *tmW, *tmH, p);
-  if (e != cudaSuccess) (void)cudaGetLastError();   // a rejected launch must not fail the next call
-  return e;
-}
-
 cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
                           cudaStream_t stream) {
   // the status word and the keys (0 lies below every real key) in one memset
   cudaError_t e = cudaMemsetAsync(p.status, 0, lmhead_workspace_bytes(p.nrows), stream);
   if (e != cudaSuccess) return e;
-  e = launch_gemm<false>(p, lmhead_layout(p.npad, p.n_vtiles), tmW, tmH, num_sms, stream);
+  const LmLayout L = lmhead_layout(p.npad);
+  if (!lmhead_layout_matches(L, p)) return cudaErrorInvalidValue;
+  // the limit is the largest layout's (a fixed value, so concurrent calls never race on it)
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<false>), kLmSmemCap - 2560);
   if (e != cudaSuccess) return e;
+  const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
+  lmhead_gemm<false><<<grid, kLmThreads, L.smem, stream>>>(*tmW, *tmH, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_dependent(lmhead_finalize, dim3(p.B), dim3(256), 0, stream, 0u, p);
 }
 
 cudaError_t launch_lmhead_logits(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
                                  cudaStream_t stream) {
-  if (!p.logits) return cudaErrorInvalidValue;
-  return launch_gemm<true>(p, lmhead_layout(p.npad, p.n_vtiles), tmW, tmH, num_sms, stream);
+  const LmLayout L = lmhead_layout(p.npad);
+  if (!lmhead_layout_matches(L, p) || !p.logits) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(lmhead_gemm<true>), kLmSmemCap - 2560);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_vtiles < num_sms ? p.n_vtiles : num_sms;
+  lmhead_gemm<true><<<grid, kLmThreads, L.smem, stream>>>(*tmW, *tmH, p);
+  return cudaGetLastError();
 }
 
 }  // namespace specv

@@ -20,7 +20,6 @@ struct LmheadParams {
   int w_stages, h_stages; // ring depths in copies (lmhead_layout)
   int kgroup;             // K chunks a tile takes in a row (one accumulator chain of 4 kgroup MMAs)
   int wbox, hbox;         // K chunks per weight / hidden-row copy (one 3-D tensor-map box)
-  int pair;               // clusters of two CTAs, M = 256 pair MMAs, each CTA staging npad / 2 hidden rows
   const int32_t* tok;     // draft tokens [B][gamma] (chain) or node tokens [B][N] (tree)
   int64_t tok_sb;
   int out_cols;
@@ -36,15 +35,9 @@ struct LmheadParams {
 
 struct LmLayout {
   int w_stages, h_stages, kgroup, wbox, hbox;
-  int pair;               // the pair-CTA form (see lmhead_gemm)
   size_t smem;            // dynamic shared memory of the GEMM
 };
-// Ring layout and form for npad hidden rows over n_vtiles vocabulary tiles.
-LmLayout lmhead_layout(int npad, int n_vtiles);
-// Vocabulary tiles whose accumulators fit the GEMM's TMEM allocation together.
-int lmhead_tiles_per_pass(const LmLayout& L, int npad);
-// Rows of each hidden-row copy (the tensor map's box): npad, or npad / 2 in the pair form.
-inline int lmhead_hidden_box_rows(const LmLayout& L, int npad) { return L.pair ? npad / 2 : npad; }
+LmLayout lmhead_layout(int npad);
 size_t lmhead_workspace_bytes(int nrows);
 void lmhead_workspace_carve(void* ws, LmheadParams* p);
 cudaError_t launch_lmhead(const LmheadParams& p, const CUtensorMap* tmW, const CUtensorMap* tmH, int num_sms,
