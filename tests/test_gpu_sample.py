@@ -262,3 +262,24 @@ def test_host_validation_rejects_before_launch(sv):
     with pytest.raises(sv.SpecError) as e:
         sv.spec_sample(sv.SPEC_SAMPLE_CHAIN_GREEDY, tl, out, nacc, draft_tokens=out[:, :2])
     assert e.value.status in (sv.SPEC_ERR_UNSUPPORTED, sv.SPEC_ERR_INVALID_ARG)
+
+
+def test_status_cleared_by_the_next_call(sv):
+    """With V > 2048 the statistics kernel clears the call's status word itself (no memset before
+    it): a call that flags SPEC_STATUS_BAD_TOKEN, then a clean call on the same workspace (filled
+    with ones before the first), reads 0."""
+    torch = torch_mod()
+    V = 8192
+    good = gen.chain_sample_inputs(4, 3, V, 5, 2.0, 1.0)
+    bad = {k: v.copy() for k, v in good.items()}
+    bad["draft_tokens"][1, 2] = V
+    tl = to_dev(good["target_logits"])
+    ws = torch.full((sv.spec_sample_workspace(sv.SPEC_SAMPLE_CHAIN, tl),), 255, dtype=torch.uint8, device=tl.device)
+    out = torch.empty((4, 4), dtype=torch.int32, device=tl.device)
+    nacc = torch.empty((4,), dtype=torch.int32, device=tl.device)
+    for inp, want in ((bad, 4), (good, 0)):
+        sv.spec_sample(sv.SPEC_SAMPLE_CHAIN, to_dev(inp["target_logits"]), out, nacc,
+                       draft_logits=to_dev(inp["draft_logits"]), draft_tokens=to_dev(inp["draft_tokens"], "i32"),
+                       uniforms=to_dev(inp["uniforms"]), workspace=ws)
+        torch.cuda.synchronize()
+        assert sv.read_status(ws) == want

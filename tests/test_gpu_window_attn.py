@@ -236,3 +236,57 @@ def test_sink_window_round_matches_the_shift_left_cache(sv):
                                   1.0 / np.sqrt(D)) for h in range(Hq)])
         assert st == 0
         assert_attn_close(o, ref[None], "bf16", what=f"step {t}")
+
+
+@pytest.mark.parametrize("layout", ["v_below_k", "heads_strided"])
+def test_window_ring_layouts(sv, layout):
+    """Where the rings lie decides how a tile is copied: K and V of a tile in one copy when each
+    ring's heads are contiguous over the batch (the lower-addressed ring's tile landing first),
+    one copy per ring otherwise.  v_below_k: both rings in one allocation with V first;
+    heads_strided: each ring the first Hkv heads of a buffer with three more (batch stride is not
+    Hkv head strides)."""
+    torch = torch_mod()
+    B, Hq, Hkv, D, W = 5, 32, 8, 128, 256
+    pos = np.array([1, 77, 256, 257, 9000], dtype=np.int32)
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, pos, "bf16", seed=41)
+    if layout == "v_below_k":
+        buf = torch.empty((2, B, Hkv, W, D), dtype=torch.bfloat16, device="cuda")
+        buf[0].copy_(to_dev(inp["v_ring"], "bf16"))
+        buf[1].copy_(to_dev(inp["k_ring"], "bf16"))
+        kr, vr = buf[1], buf[0]
+    else:
+        kb = torch.zeros((B, Hkv + 3, W, D), dtype=torch.bfloat16, device="cuda")
+        vb = torch.zeros_like(kb)
+        kb[:, :Hkv].copy_(to_dev(inp["k_ring"], "bf16"))
+        vb[:, :Hkv].copy_(to_dev(inp["v_ring"], "bf16"))
+        kr, vr = kb[:, :Hkv], vb[:, :Hkv]
+    o, st = _run(sv, to_dev(inp["q"], "bf16"), kr, vr, to_dev(pos, "i32"), to_dev(inp["k_new"], "bf16"),
+                 to_dev(inp["v_new"], "bf16"), "bf16")
+    ref, k_after, v_after = oa.draft_window_attn(inp["q"], inp["k_ring"], inp["v_ring"], pos, inp["k_new"],
+                                                 inp["v_new"])
+    assert st == 0
+    assert_attn_close(o, ref, "bf16", what=layout)
+    kr_np, vr_np = to_np(kr), to_np(vr)
+    for b in range(B):
+        s = (pos[b] - 1) % W
+        assert np.array_equal(kr_np[b, :, s], k_after[b, :, s].astype(np.float32))
+        assert np.array_equal(vr_np[b, :, s], v_after[b, :, s].astype(np.float32))
+
+
+def test_window_status_cleared_by_the_next_call(sv):
+    """The draft window kernel clears the call's status word itself (no memset before it): a call
+    that flags SPEC_STATUS_BAD_POS, then a clean call on the same workspace (filled with ones
+    before the first), reads 0."""
+    torch = torch_mod()
+    B, Hq, Hkv, D, W = 2, 32, 8, 128, 64
+    pos_bad, pos_ok = np.array([0, 10], np.int32), np.array([5, 10], np.int32)
+    inp = gen.window_inputs(B, Hq, Hkv, D, W, np.maximum(pos_bad, 1), "bf16", seed=43)
+    q, kr, vr = to_dev(inp["q"], "bf16"), to_dev(inp["k_ring"], "bf16"), to_dev(inp["v_ring"], "bf16")
+    o = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    ws = torch.full((sv.spec_draft_window_attn_workspace(q, kr, o),), 255, dtype=torch.uint8, device=q.device)
+    sv.spec_draft_window_attn(q, kr, vr, to_dev(pos_bad, "i32"), o, workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.read_status(ws) == 2
+    sv.spec_draft_window_attn(q, kr, vr, to_dev(pos_ok, "i32"), o, workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.read_status(ws) == 0
