@@ -496,6 +496,11 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
 // states are combined through shared memory (the stage buffers, once every copy has landed) with
 // the new key (the current token, whose slot is masked in the ring), and the output and the ring
 // slot are written.
+// Launch: K and V of a tile come in one copy when the rings' heads are contiguous over the batch
+// (a map over both rings), else one copy each.  The kernel is a programmatic dependent of the
+// previous kernel of the stream: before the grid-dependency wait it only sends its first tiles to
+// L2, and it clears the call's status word itself, so back-to-back draft calls have no memset node
+// between them and each overlaps its launch with the previous call's tail.
 constexpr int kWinKeys = 64;
 constexpr int kWinStages = 3;
 constexpr int kWinGroups = 2;

@@ -191,7 +191,7 @@ __device__ __forceinline__ void status_report(uint32_t* status, uint32_t bits) {
   atomicOr(status, bits);
 }
 
-// ---------------------------------------------------------------- TMA (tiled, 4-D, no multicast)
+// ---------------------------------------------------------------- TMA (tiled, no multicast)
 // Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of 16),
 // completing `bytes` transactions on `bar`.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
