@@ -10,8 +10,11 @@ namespace specv {
 constexpr int kSampleThreads = 256;
 constexpr int kSmallVocab = 2048;   // V at or below: one warp per sequence does the whole step
 constexpr int kStatChunk = 1024;    // statistics item: 1024 logits of one row, one warp
-constexpr int kStatWarps = 16;      // statistics CTA: warps, each with its own ring of item slots
-constexpr int kStatSlots = 3;       // items in flight per warp (4 KB each)
+// statistics CTA: warps, each with its own ring of item slots, and the items each keeps in flight
+// (4 KB each).  Twenty warps of two slots (a 160 KB ring) measured faster than sixteen of three or
+// twenty-four of two (192 KB rings) at every batch tried, and as fast as rings of 8 KB items.
+constexpr int kStatWarps = 20;
+constexpr int kStatSlots = 2;
 constexpr int kMaxGamma = 32;
 constexpr int kMaxTreeNodes = 64;
 
