@@ -103,14 +103,15 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16 burst (no MEASURED_PEAKS.json)"
 
 
-def profile_counters(workload):
+def profile_counters(cfg):
     """ncu counters committed for a workload's verify kernel (profiles/roofline_counters.json),
-    or None when absent or taken on another kernel revision than the one built now."""
+    or None when absent, taken on another kernel revision than the one built now, or when this
+    run's sizes are not the workload's own (a --batch or --context override)."""
     path = os.path.join(ROOT, "profiles", "roofline_counters.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or cfg != get_config(cfg.name):
         return None
-    d = json.load(open(path)).get(workload)
-    if not d or d.get("kernel_rev") != KERNEL_REVS.get(workload):
+    d = json.load(open(path)).get(cfg.name)
+    if not d or d.get("kernel_rev") != KERNEL_REVS.get(cfg.name):
         return None
     return d
 
@@ -1089,7 +1090,7 @@ def measure(cfg, args, pg, device, rank, world, full):
     tpeak, tpeak_kind = tensor_peak()
     achieved = nb["verify_total"] / (t["verify_ms"] * 1e-3) / 1e9
     tflops = verify_flops(cfg, inp) / (t["verify_ms"] * 1e-3) / 1e12
-    counters = profile_counters(cfg.name)
+    counters = profile_counters(cfg)
     rec = {
         "workload": cfg.name,
         "config": {"batch": cfg.B, "q_heads": cfg.Hq, "kv_heads": cfg.Hkv, "head_dim": cfg.D,

@@ -98,3 +98,18 @@ def test_algorithmic_bytes_match_the_closed_forms():
     nb = bench.step_bytes(b8, {"kv_len_h": lens})
     assert nb["verify_kv"] == int(lens.sum()) * 8 * 128 * 4
     assert nb["window"] == 0
+
+
+def test_committed_counters_attach_only_to_the_workloads_own_sizes():
+    """roofline.traffic comes from an ncu capture of one kernel revision at one workload's sizes:
+    a run with a --batch or --context override must not carry it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads.configs import get_config, scaled
+    for name in ("magicdec-64k", "llama3-8b-layer"):
+        cfg = get_config(name)
+        full = bench.profile_counters(cfg)
+        if full is not None:
+            assert full.get("kernel_rev") == bench.KERNEL_REVS[name]
+        assert bench.profile_counters(scaled(cfg, ctx=(4096, 4096))) is None
+        assert bench.profile_counters(scaled(cfg, B=2)) is None
