@@ -405,18 +405,20 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 
 // One CTA per sequence: each row's argmax from its key, then the greedy rule of the mode.
 __global__ void __launch_bounds__(256) lmhead_finalize(const __grid_constant__ LmheadParams p) {
-  pdl_wait();  // the GEMM's keys
   __shared__ int s_a[kLmMaxNodes];
+  __shared__ int32_t tok[kLmMaxNodes];  // the sequence's node or draft tokens, staged by all threads
   const int b = blockIdx.x;
-  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(p.rec);
-  for (int r = threadIdx.x; r < p.R; r += blockDim.x) s_a[r] = lm_key_id(keys[(int64_t)b * p.R + r]);
-  __syncthreads();
-  if (threadIdx.x != 0) return;
-  const int32_t* tok = p.tok + (int64_t)b * p.tok_sb;
-  int32_t* out = p.out_tok + (int64_t)b * p.out_cols;
-  int32_t* nodes = p.out_nodes ? p.out_nodes + (int64_t)b * p.out_cols : nullptr;
   const bool tree = p.mode == SPEC_SAMPLE_TREE_GREEDY;
   const int nt = tree ? p.R : p.R - 1;  // tokens to check: node tokens 1..N-1, or drafts 0..gamma-1
+  // the tokens are inputs of the call, not of the GEMM: loaded before the wait
+  for (int i = threadIdx.x; i < nt; i += blockDim.x) tok[i] = p.tok[(int64_t)b * p.tok_sb + i];
+  pdl_wait();  // the GEMM's keys
+  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(p.rec);
+  for (int r = threadIdx.x; r < p.R; r += blockDim.x) s_a[r] = lm_key_id(__ldcg(keys + (int64_t)b * p.R + r));
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  int32_t* out = p.out_tok + (int64_t)b * p.out_cols;
+  int32_t* nodes = p.out_nodes ? p.out_nodes + (int64_t)b * p.out_cols : nullptr;
   bool bad = false;
   for (int i = tree ? 1 : 0; i < nt; ++i) bad |= tok[i] < 0 || tok[i] >= p.V;
   for (int c = 0; c < p.out_cols; ++c) {

@@ -206,13 +206,14 @@ __device__ void write_chain_out(const SampleParams& p, int b, int k, int y, cons
   }
   p.out_nacc[b] = k;
 }
+
 __device__ void write_chain_out(const SampleParams& p, int b, int k, int y) {
   write_chain_out(p, b, k, y, p.tok + (int64_t)b * p.tok_sb);
 }
 
-// Greedy tree: a[] holds the argmax of every node's row.  Writes the outputs of sequence b.
-__device__ void tree_select_write(const SampleParams& p, int b, const int* a) {
-  const int32_t* tk = p.tok + (int64_t)b * p.tok_sb;
+// Greedy tree: a[] holds the argmax of every node's row, tk[] the node tokens of sequence b (in
+// global or shared memory).  Writes the outputs of sequence b.
+__device__ void tree_select_write(const SampleParams& p, int b, const int* a, const int32_t* tk) {
   int32_t* out = p.out_tok + (int64_t)b * p.out_cols;
   int32_t* nodes = p.out_nodes ? p.out_nodes + (int64_t)b * p.out_cols : nullptr;
   bool bad = false;
@@ -241,6 +242,9 @@ __device__ void tree_select_write(const SampleParams& p, int b, const int* a) {
   }
   out[d] = a[best];
   p.out_nacc[b] = d;
+}
+__device__ void tree_select_write(const SampleParams& p, int b, const int* a) {
+  tree_select_write(p, b, a, p.tok + (int64_t)b * p.tok_sb);
 }
 
 // ------------------------------------------------------------------ large-V kernels
@@ -420,34 +424,66 @@ __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_
 }
 
 // Greedy modes, one CTA per sequence: merges the item argmaxes of its rows and applies the greedy
-// chain or tree rule.
+// chain or tree rule.  A warp loads the item records of up to kFinRowBatch rows before it reduces
+// any of them (one L2 round trip per 32 items of kFinRowBatch rows, not per row), and the
+// sequence's tokens are staged in shared memory by all threads before thread 0 applies the rule.
+// The argmax combination (larger value, ties to the smaller id) does not depend on the order in
+// which records meet, so the result is that of any merge order.
+constexpr int kFinRowBatch = 8;
 __global__ void __launch_bounds__(kSampleThreads) sample_finalize(const __grid_constant__ SampleParams p) {
-  pdl_wait();  // the statistics kernel's per-item records
   __shared__ int sa[kMaxTreeNodes > kMaxGamma + 1 ? kMaxTreeNodes : kMaxGamma + 1];
+  __shared__ int32_t s_tok[kMaxTreeNodes > kMaxGamma ? kMaxTreeNodes : kMaxGamma];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rows = p.rows_t + p.rows_d;
-  for (int rr = warp; rr < rows; rr += kWarps) {
-    const int64_t oo = ((int64_t)b * rows + rr) * p.schunks;
-    float v = neg_inf();
-    int i = INT_MAX;
-    for (int cc = lane; cc < p.schunks; cc += 32) argmax_combine(v, i, p.st_m[oo + cc], p.st_arg[oo + cc]);
-    warp_argmax(v, i);
-    if (lane == 0) sa[rr] = i;
+  const bool tree = p.mode == SPEC_SAMPLE_TREE_GREEDY;
+  const int ntok = tree ? p.N : p.gamma;
+  // the tokens are inputs of the call, not of the statistics kernel: loaded before the wait
+  if (tid < ntok) s_tok[tid] = p.tok[(int64_t)b * p.tok_sb + tid];
+  pdl_wait();  // the statistics kernel's per-item records
+  for (int r0 = warp; r0 < rows; r0 += kWarps * kFinRowBatch) {
+    float v[kFinRowBatch];
+    int ix[kFinRowBatch];
+#pragma unroll
+    for (int u = 0; u < kFinRowBatch; ++u) {
+      v[u] = neg_inf();
+      ix[u] = INT_MAX;
+    }
+    for (int c0 = 0; c0 < p.schunks; c0 += 32) {
+      const int cc = c0 + lane;
+      float mv[kFinRowBatch];
+      int ma[kFinRowBatch];
+#pragma unroll
+      for (int u = 0; u < kFinRowBatch; ++u) {
+        const int rr = r0 + u * kWarps;
+        const bool in = rr < rows && cc < p.schunks;
+        const int64_t o = ((int64_t)b * rows + rr) * p.schunks + cc;
+        mv[u] = in ? __ldcg(p.st_m + o) : neg_inf();
+        ma[u] = in ? __ldcg(p.st_arg + o) : INT_MAX;
+      }
+#pragma unroll
+      for (int u = 0; u < kFinRowBatch; ++u) argmax_combine(v[u], ix[u], mv[u], ma[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kFinRowBatch; ++u) {
+      warp_argmax(v[u], ix[u]);
+      const int rr = r0 + u * kWarps;
+      if (lane == 0 && rr < rows) sa[rr] = ix[u];
+    }
   }
   __syncthreads();
   if (tid == 0) {
-    if (p.mode == SPEC_SAMPLE_TREE_GREEDY) {
-      tree_select_write(p, b, sa);
+    if (tree) {
+      tree_select_write(p, b, sa, s_tok);
     } else {
       int k = p.gamma;
       for (int i = 0; i < p.gamma; ++i) {
-        const int xi = p.tok[(int64_t)b * p.tok_sb + i];
+        const int xi = s_tok[i];
         if (xi < 0 || xi >= p.V) { k = -1; break; }
       }
       if (k >= 0)
         for (int i = 0; i < p.gamma; ++i)
-          if (p.tok[(int64_t)b * p.tok_sb + i] != sa[i]) { k = i; break; }
-      write_chain_out(p, b, k, k >= 0 ? sa[k] : -1);
+          if (s_tok[i] != sa[i]) { k = i; break; }
+      write_chain_out(p, b, k, k >= 0 ? sa[k] : -1, s_tok);
     }
   }
 }
