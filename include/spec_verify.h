@@ -229,7 +229,8 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  *   if no index qualifies through rounding, the largest y with r_y > 0).
  *   Output: out_tokens[b, 0..k] = x_1..x_k, y; the rest of the row -1; out_num_accepted[b] = k.
  * SPEC_SAMPLE_CHAIN_GREEDY (n = gamma >= 0): x_i accepted while it equals argmax P_i (ties to the
- *   smallest id); then the argmax of row k+1 is emitted.  draft_logits and uniforms unused.
+ *   smallest id, so a row of all -inf gives id 0); then the argmax of row k+1 is emitted.
+ *   draft_logits and uniforms unused.
  * SPEC_SAMPLE_TREE_GREEDY (n = N nodes, tree_parent HOST [N]): row i of target_logits holds the
  *   logits after node i; node i >= 1 is accepted iff its parent is accepted and
  *   draft_tokens[b, i] (the node's token) equals the argmax of its parent's row; node 0 (the last

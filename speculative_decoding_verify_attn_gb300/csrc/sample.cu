@@ -393,8 +393,8 @@ __global__ void __launch_bounds__(kStatWarps * 32, 1) sample_stats(const __grid_
         const int idx = base + i * 128 + lane * 4;
         const float e[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (idx + j < p.V && e[j] > bv) { bv = e[j]; bi = idx + j; }
+        for (int j = 0; j < 4; ++j)  // the lane's first -inf seeds it, so an all -inf row gives id 0
+          if (idx + j < p.V && (e[j] > bv || (bi == INT_MAX && e[j] == neg_inf()))) { bv = e[j]; bi = idx + j; }
       }
       warp_argmax(bv, bi);
       if (lane == 0) {
@@ -884,8 +884,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_small(const __grid_cons
     if (greedy) {
       float v = neg_inf();
       int i = INT_MAX;
-      for (int e = e0; e < e1; ++e)
-        if (row[e] > v) { v = row[e]; i = e; }
+      for (int e = e0; e < e1; ++e)  // the lane's first -inf seeds it, so an all -inf row gives id 0
+        if (row[e] > v || (i == INT_MAX && row[e] == neg_inf())) { v = row[e]; i = e; }
       warp_argmax(v, i);
       if (lane == 0) a[r] = i;
     } else {

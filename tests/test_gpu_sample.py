@@ -215,6 +215,37 @@ def test_greedy_chain(sv, V):
     assert np.array_equal(nacc, ref_k) and np.array_equal(out, ref_out)
 
 
+@pytest.mark.parametrize("V", [1024, 5120])
+def test_greedy_rows_of_all_neg_inf(sv, V):
+    """A row whose logits are all -inf ties everywhere: its argmax is id 0 (ties to the smallest
+    id), as in the oracle, on the one-warp path (V 1024) and the item path (V 5120); a row with -inf
+    everywhere but one finite logit picks that one."""
+    B, gamma = 3, 3
+    r = np.random.default_rng(7)
+    t = (2 * r.standard_normal((B, gamma + 1, V))).astype(np.float32)
+    t[0, 0] = -np.inf                       # row 1 of sequence 0: no finite logit
+    t[1, 2] = -np.inf                       # sequence 1, row 3: one finite logit, late in the row
+    t[1, 2, V - 3] = -5.0
+    t[2, :] = -np.inf                       # every row of sequence 2
+    x = np.argmax(t[:, :gamma], -1).astype(np.int32)
+    x[0, 0] = 0
+    inp = dict(target_logits=t, draft_tokens=x)
+    out, nacc, st = gpu_chain(sv, inp, mode=sv.SPEC_SAMPLE_CHAIN_GREEDY)
+    ref_out, ref_k = osm.greedy_chain(t, x)
+    assert st == 0
+    assert np.array_equal(nacc, ref_k) and np.array_equal(out, ref_out)
+    assert ref_k[2] == gamma and ref_out[2].tolist() == [0] * (gamma + 1)
+    parent = np.array([-1, 0, 0, 1], np.int32)
+    tok = np.zeros((B, 4), np.int32)
+    tok[:, 1:] = r.integers(V, size=(B, 3))
+    tok[2, 1] = 0
+    tok[2, 3] = 0
+    o, nodes, k = _gpu_tree(sv, t, tok, parent, 3)
+    r_o, r_nodes, r_k = osm.tree_greedy(t, tok, parent, 3)
+    assert np.array_equal(k, r_k) and np.array_equal(o, r_o) and np.array_equal(nodes, r_nodes)
+    assert r_k[2] == 2
+
+
 def _gpu_tree(sv, tl, tok, parent, out_cols):
     torch = torch_mod()
     tld = to_dev(tl)
