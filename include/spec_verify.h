@@ -258,8 +258,9 @@ int spec_draft_window_attn(const spec_window_args* args, spec_stream_t stream);
  *   1 <= B; chain: 1 <= gamma <= 32 (stochastic), 0 <= gamma <= 32 (greedy),
  *   out_cols >= gamma + 1; tree: 1 <= N <= 64, out_cols >= max depth + 1.
  *   Logits hold no NaN, and in the stochastic modes every row the rule reads holds a value above
- *   -inf (a softmax needs one); otherwise the emitted tokens are unspecified (the kernels still
- *   touch no memory outside the call's buffers).  -inf entries are allowed.
+ *   -inf (a softmax needs one); otherwise the outputs (tokens, counts, paths) are unspecified,
+ *   though the kernels still touch no memory outside the call's buffers.  -inf entries are
+ *   allowed.
  * Floating point: V > 2048 (the statistics + finish kernels) uses no fp64 at all.  Each thread
  *   sums its own elements in fp32 (pairwise or compensated); every sum above that -- across lanes,
  *   warps, CTAs and the cluster -- is float-float (Knuth's TwoSum, about 44 significant bits), in a
